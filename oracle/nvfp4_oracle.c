@@ -1,0 +1,331 @@
+/*
+ * nvfp4_oracle.c -- plain, slow CPU oracle for the NVFP4 paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the independent reference that the
+ * CUDA library is checked against.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it; the product path never does.  It
+ * shares no code, header, table or constant generator with the CUDA sources.
+ *
+ * Sources (web pages on NVFP4 KV-cache quantisation):
+ *  - "nvfp4-kv-cache-memory-wall" (grer.cn blog), section 2 (two-level
+ *    scaling): E2M1 data values +-{0,0.5,1,1.5,2,3,4,6}; one FP8 E4M3 scale per
+ *    16 consecutive values; one FP32 scale for the whole tensor; the demo maps
+ *    each block's amax onto 6 and snaps every value to the nearest E2M1 value.
+ *  - same page, section 1: 16 E2M1 values pack into 8 bytes plus 1 scale byte,
+ *    i.e. 9/16 byte per value.
+ *  - same page, section 3 (three data flows): new K/V are quantised to NVFP4 on
+ *    the way into the paged cache; decode dequantises inside the attention
+ *    kernel; chunked prefill/extend dequantises the cached prefix into one FP8
+ *    E4M3 workspace shared by all layers.
+ *  - "NVFP4: breaking the memory wall" (cloud.tencent.com), technical
+ *    breakdown: E2M1 is 1 sign, 2 exponent and 1 mantissa bit; the micro-block
+ *    scale is E4M3; the tensor-level scale is FP32.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - E2M1 and E4M3 encoders round to nearest, ties to the even code, and
+ *    saturate at the largest finite value (+-6, +-448).  The sign of the input
+ *    is kept, so a small negative value encodes as -0.
+ *  - Block scale: sb = E4M3(amax / (6*g)); value code: E2M1(x / (E4M3val(sb)*g)).
+ *    Every step is one IEEE binary32 operation rounded to nearest (this file
+ *    is compiled with -ffp-contract=off, so no multiply-add is fused).
+ *  - If E4M3val(sb)*g is 0 the block stores signed zeros.
+ *  - Blocks run along head_dim; element 2i is the low nibble of byte i.
+ *  - Attention is evaluated in binary64 over the dequantised cache.
+ *  - FP8 workspace: w = E4M3(fp32(fp32(e2m1*E4M3val(sb)) * g) / s_ws), signed.
+ *
+ * Cache layout (a proposal the pages leave open): data pages
+ * [num_pages][num_kv_heads][page_size][head_dim/2] bytes, scale pages
+ * [num_pages][num_kv_heads][page_size][head_dim/16] E4M3 bytes; a slot s names
+ * page s / page_size, row s % page_size.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "nvfp4_oracle.h"
+
+/* ------------------------------------------------------------------------- */
+/* Formats, from their bit-field definitions.                                */
+/* ------------------------------------------------------------------------- */
+
+/* E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa.  Exponent 0
+ * is subnormal: value = m * 0.5.  Otherwise value = 2^(e-1) * (1 + m/2). */
+double nvfp4_oracle_e2m1_value(uint8_t code) {
+  int s = (code >> 3) & 1;
+  int e = (code >> 1) & 3;
+  int m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+/* E4M3 ("fn" flavour: no infinities, 0x7F/0xFF are NaN): bit 7 sign, bits
+ * 6..3 exponent (bias 7), bits 2..0 mantissa.  Exponent 0 is subnormal:
+ * value = m/8 * 2^-6. */
+double nvfp4_oracle_e4m3_value(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 3) & 15;
+  int m = code & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    mag = ldexp(m / 8.0, -6);
+  else
+    mag = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* Nearest-value search over the non-negative codes 0..max_code of a format
+ * whose values increase with the code.  Ties pick the even code (the one whose
+ * mantissa LSB, which is the code LSB, is zero).  Saturating: anything beyond
+ * the largest finite value maps to it. */
+static uint8_t nearest_code(double mag, int max_code, double (*value)(uint8_t)) {
+  /* at or beyond the largest finite value: saturate (distances to the
+   * candidates would also lose their differences for huge inputs) */
+  if (mag >= value((uint8_t)max_code)) return (uint8_t)max_code;
+  int best = 0;
+  double best_d = fabs(mag - value(0));
+  for (int c = 1; c <= max_code; ++c) {
+    double d = fabs(mag - value((uint8_t)c));
+    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)best;
+}
+
+uint8_t nvfp4_oracle_e2m1_encode(float y) {
+  uint8_t mag = nearest_code(fabs((double)y), 7, nvfp4_oracle_e2m1_value);
+  return (uint8_t)(mag | (signbit(y) ? 0x8 : 0x0));
+}
+
+uint8_t nvfp4_oracle_e4m3_encode(float z) {
+  uint8_t mag = nearest_code(fabs((double)z), 0x7E, nvfp4_oracle_e4m3_value);
+  return (uint8_t)(mag | (signbit(z) ? 0x80 : 0x00));
+}
+
+/* bf16 is the top half of a binary32 bit pattern. */
+float nvfp4_oracle_bf16_to_float(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* One 16-value block: two-level scaling.                                    */
+/* ------------------------------------------------------------------------- */
+
+void nvfp4_oracle_quantize_block(const float x[NVFP4_ORACLE_BLOCK], float g,
+                                 uint8_t packed[NVFP4_ORACLE_BLOCK / 2], uint8_t* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < NVFP4_ORACLE_BLOCK; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float t = 6.0f * g;          /* the block's amax lands on E2M1's largest value */
+  float ratio = amax / t;
+  uint8_t sb = nvfp4_oracle_e4m3_encode(ratio);
+  float den = (float)nvfp4_oracle_e4m3_value(sb) * g;
+  uint8_t codes[NVFP4_ORACLE_BLOCK];
+  for (int i = 0; i < NVFP4_ORACLE_BLOCK; ++i) {
+    if (den == 0.0f) {
+      codes[i] = signbit(x[i]) ? 0x8 : 0x0;
+    } else {
+      float y = x[i] / den;
+      codes[i] = nvfp4_oracle_e2m1_encode(y);
+    }
+  }
+  for (int i = 0; i < NVFP4_ORACLE_BLOCK / 2; ++i)
+    packed[i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
+  *scale = sb;
+}
+
+double nvfp4_oracle_dequant_value(uint8_t code, uint8_t scale, float g) {
+  return nvfp4_oracle_e2m1_value(code) * nvfp4_oracle_e4m3_value(scale) * (double)g;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The page demo's arithmetic (binary64, unrounded block scale, global scale */
+/* 1, ties to the first entry of the value list in ascending order).         */
+/* ------------------------------------------------------------------------- */
+
+void nvfp4_oracle_demo_fake_quant(const double* x, int64_t n, int64_t block, double* out) {
+  /* the 16 E2M1 values in ascending order, -0 before +0 */
+  double list[16];
+  int k = 0;
+  for (int c = 7; c >= 0; --c) list[k++] = nvfp4_oracle_e2m1_value((uint8_t)(c | 8));
+  for (int c = 0; c <= 7; ++c) list[k++] = nvfp4_oracle_e2m1_value((uint8_t)c);
+  for (int64_t b0 = 0; b0 < n; b0 += block) {
+    int64_t b1 = b0 + block < n ? b0 + block : n;
+    double amax = 0.0;
+    for (int64_t i = b0; i < b1; ++i)
+      if (fabs(x[i]) > amax) amax = fabs(x[i]);
+    double scale = amax > 1e-12 ? amax / 6.0 : 1.0;
+    for (int64_t i = b0; i < b1; ++i) {
+      double y = x[i] / scale;
+      int best = 0;
+      for (int j = 1; j < 16; ++j)
+        if (fabs(list[j] - y) < fabs(list[best] - y)) best = j;
+      out[i] = list[best] * scale;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Paged cache: sizes and addressing.                                        */
+/* ------------------------------------------------------------------------- */
+
+int64_t nvfp4_oracle_row_bytes(int head_dim) { return head_dim / 2; }
+int64_t nvfp4_oracle_row_scale_bytes(int head_dim) { return head_dim / NVFP4_ORACLE_BLOCK; }
+
+static int64_t row_index(int64_t page, int h, int off, int num_kv_heads, int page_size) {
+  return (page * num_kv_heads + h) * page_size + off;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Quantize-append: every new token's K and V rows into their slots.         */
+/* ------------------------------------------------------------------------- */
+
+int nvfp4_oracle_quantize_append(const nvfp4_oracle_cache* c, const uint16_t* k_bf16,
+                                 const uint16_t* v_bf16, const int64_t* slot_mapping,
+                                 int64_t num_tokens) {
+  int bad = 0;
+  const int d = c->head_dim, H = c->num_kv_heads, P = c->page_size;
+  const int64_t rb = nvfp4_oracle_row_bytes(d), sbk = nvfp4_oracle_row_scale_bytes(d);
+  float x[NVFP4_ORACLE_BLOCK];
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    int64_t s = slot_mapping[t];
+    if (s < 0) continue;                      /* padding token */
+    if (s >= c->num_pages * P) { bad = 1; continue; }
+    int64_t page = s / P;
+    int off = (int)(s % P);
+    for (int h = 0; h < H; ++h) {
+      int64_t r = row_index(page, h, off, H, P);
+      for (int which = 0; which < 2; ++which) {
+        const uint16_t* src = (which == 0 ? k_bf16 : v_bf16) + (t * H + h) * d;
+        uint8_t* data = (which == 0 ? c->k_data : c->v_data) + r * rb;
+        uint8_t* scl = (which == 0 ? c->k_scale : c->v_scale) + r * sbk;
+        float g = which == 0 ? c->k_global_scale : c->v_global_scale;
+        for (int j = 0; j < d / NVFP4_ORACLE_BLOCK; ++j) {
+          for (int i = 0; i < NVFP4_ORACLE_BLOCK; ++i)
+            x[i] = nvfp4_oracle_bf16_to_float(src[j * NVFP4_ORACLE_BLOCK + i]);
+          nvfp4_oracle_quantize_block(x, g, data + j * (NVFP4_ORACLE_BLOCK / 2), scl + j);
+        }
+      }
+    }
+  }
+  return bad;
+}
+
+/* Dequantised element d of the cached row for (page, kv head, row-in-page). */
+static double cached_value(const nvfp4_oracle_cache* c, int which, int64_t page, int h, int off,
+                           int dd) {
+  const int d = c->head_dim;
+  int64_t r = row_index(page, h, off, c->num_kv_heads, c->page_size);
+  const uint8_t* data = (which == 0 ? c->k_data : c->v_data) + r * nvfp4_oracle_row_bytes(d);
+  const uint8_t* scl = (which == 0 ? c->k_scale : c->v_scale) + r * nvfp4_oracle_row_scale_bytes(d);
+  uint8_t byte = data[dd / 2];
+  uint8_t code = (dd & 1) ? (byte >> 4) : (byte & 0xF);
+  float g = which == 0 ? c->k_global_scale : c->v_global_scale;
+  return nvfp4_oracle_dequant_value(code, scl[dd / NVFP4_ORACLE_BLOCK], g);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decode attention: one query token per sequence, softmax over all cached   */
+/* tokens of that sequence, GQA (query head h reads KV head h / G).          */
+/* ------------------------------------------------------------------------- */
+
+int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q_bf16,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                  double softmax_scale, double* out) {
+  const int d = c->head_dim, H = c->num_kv_heads, P = c->page_size;
+  const int G = num_q_heads / H;
+  int bad = 0;
+  if (d > 512 || d % NVFP4_ORACLE_BLOCK != 0 || H <= 0 || num_q_heads % H != 0) return -1;
+  for (int32_t b = 0; b < batch; ++b) {
+    int64_t L = seq_lens[b];
+    if (L < 0 || L > (int64_t)max_pages * P) { bad = 1; L = L < 0 ? 0 : (int64_t)max_pages * P; }
+    for (int hq = 0; hq < num_q_heads; ++hq) {
+      double* o = out + ((int64_t)b * num_q_heads + hq) * d;
+      for (int dd = 0; dd < d; ++dd) o[dd] = 0.0;
+      if (L == 0) continue;
+      const int hk = hq / G;
+      double q[512];
+      for (int dd = 0; dd < d; ++dd)
+        q[dd] = nvfp4_oracle_bf16_to_float(q_bf16[((int64_t)b * num_q_heads + hq) * d + dd]);
+      double* s = (double*)malloc(sizeof(double) * (size_t)L);
+      int* valid = (int*)malloc(sizeof(int) * (size_t)L);
+      double m = -INFINITY;
+      for (int64_t t = 0; t < L; ++t) {
+        int32_t page = page_table[(int64_t)b * max_pages + t / P];
+        valid[t] = page >= 0 && page < c->num_pages;
+        if (!valid[t]) { bad = 1; continue; }
+        double acc = 0.0;
+        for (int dd = 0; dd < d; ++dd) acc += q[dd] * cached_value(c, 0, page, hk, (int)(t % P), dd);
+        s[t] = softmax_scale * acc;
+        if (s[t] > m) m = s[t];
+      }
+      double l = 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        if (!valid[t]) continue;
+        double w = exp(s[t] - m);
+        l += w;
+        int32_t page = page_table[(int64_t)b * max_pages + t / P];
+        for (int dd = 0; dd < d; ++dd) o[dd] += w * cached_value(c, 1, page, hk, (int)(t % P), dd);
+      }
+      if (l > 0.0)
+        for (int dd = 0; dd < d; ++dd) o[dd] /= l;
+      free(s);
+      free(valid);
+    }
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 E4M3 workspace for chunked prefill / extend.                          */
+/* ------------------------------------------------------------------------- */
+
+int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int32_t* page_table,
+                                          int32_t max_pages, const int32_t* prefix_lens,
+                                          const int64_t* cu_prefix, int32_t batch,
+                                          float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                          uint8_t* ws_v) {
+  const int d = c->head_dim, H = c->num_kv_heads, P = c->page_size;
+  int bad = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    int64_t L = prefix_lens[b];
+    if (L < 0 || L > (int64_t)max_pages * P) { bad = 1; L = L < 0 ? 0 : (int64_t)max_pages * P; }
+    for (int64_t t = 0; t < L; ++t) {
+      int64_t row = cu_prefix[b] + t;
+      int32_t page = page_table[(int64_t)b * max_pages + t / P];
+      int ok = page >= 0 && page < c->num_pages;
+      if (!ok) bad = 1;
+      for (int h = 0; h < H; ++h) {
+        for (int which = 0; which < 2; ++which) {
+          uint8_t* w = (which == 0 ? ws_k : ws_v) + (row * H + h) * d;
+          float g = which == 0 ? c->k_global_scale : c->v_global_scale;
+          float sws = which == 0 ? k_ws_scale : v_ws_scale;
+          for (int dd = 0; dd < d; ++dd) {
+            if (!ok) { w[dd] = 0; continue; }
+            int64_t r = row_index(page, h, (int)(t % P), H, P);
+            const uint8_t* data = (which == 0 ? c->k_data : c->v_data) + r * nvfp4_oracle_row_bytes(d);
+            const uint8_t* scl =
+                (which == 0 ? c->k_scale : c->v_scale) + r * nvfp4_oracle_row_scale_bytes(d);
+            uint8_t byte = data[dd / 2];
+            uint8_t code = (dd & 1) ? (byte >> 4) : (byte & 0xF);
+            float v = (float)(nvfp4_oracle_e2m1_value(code) *
+                              nvfp4_oracle_e4m3_value(scl[dd / NVFP4_ORACLE_BLOCK]));
+            float vg = v * g;
+            float z = vg / sws;
+            w[dd] = nvfp4_oracle_e4m3_encode(z);
+          }
+        }
+      }
+    }
+  }
+  return bad;
+}

@@ -1,0 +1,65 @@
+/*
+ * nvfp4_oracle.h -- declarations of the CPU oracle (test infrastructure only).
+ *
+ * The oracle is the slow, obviously correct reference for the NVFP4 paged KV
+ * cache; only tests, the smoke check and the benchmark's CPU-baseline leg use
+ * it.  It has no GPU dependency and shares nothing with the CUDA library.
+ * All pointers are host pointers.  Functions that walk page tables return 0,
+ * or 1 when an out-of-range slot, page id or length was skipped or clamped.
+ */
+#ifndef NVFP4_ORACLE_H
+#define NVFP4_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_ORACLE_BLOCK 16 /* values sharing one E4M3 block scale */
+
+typedef struct {
+  uint8_t* k_data;  /* [num_pages][num_kv_heads][page_size][head_dim/2]  */
+  uint8_t* v_data;
+  uint8_t* k_scale; /* [num_pages][num_kv_heads][page_size][head_dim/16] */
+  uint8_t* v_scale;
+  int64_t num_pages;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  float k_global_scale;
+  float v_global_scale;
+} nvfp4_oracle_cache;
+
+double nvfp4_oracle_e2m1_value(uint8_t code);
+double nvfp4_oracle_e4m3_value(uint8_t code);
+uint8_t nvfp4_oracle_e2m1_encode(float y);
+uint8_t nvfp4_oracle_e4m3_encode(float z);
+float nvfp4_oracle_bf16_to_float(uint16_t bits);
+
+void nvfp4_oracle_quantize_block(const float x[NVFP4_ORACLE_BLOCK], float g,
+                                 uint8_t packed[NVFP4_ORACLE_BLOCK / 2], uint8_t* scale);
+double nvfp4_oracle_dequant_value(uint8_t code, uint8_t scale, float g);
+void nvfp4_oracle_demo_fake_quant(const double* x, int64_t n, int64_t block, double* out);
+
+int64_t nvfp4_oracle_row_bytes(int head_dim);
+int64_t nvfp4_oracle_row_scale_bytes(int head_dim);
+
+int nvfp4_oracle_quantize_append(const nvfp4_oracle_cache* c, const uint16_t* k_bf16,
+                                 const uint16_t* v_bf16, const int64_t* slot_mapping,
+                                 int64_t num_tokens);
+int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q_bf16,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                  double softmax_scale, double* out);
+int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int32_t* page_table,
+                                          int32_t max_pages, const int32_t* prefix_lens,
+                                          const int64_t* cu_prefix, int32_t batch,
+                                          float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                          uint8_t* ws_v);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
