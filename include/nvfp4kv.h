@@ -1,0 +1,191 @@
+/*
+ * nvfp4kv.h -- C ABI of libnvfp4kv.so: an NVFP4 paged KV cache on one GB300
+ * (sm_103a).
+ *
+ * Format ("nvfp4-kv-cache-memory-wall", section 2, two-level scaling; "NVFP4:
+ * breaking the memory wall", technical breakdown): each value is a 4-bit E2M1
+ * code (1 sign, 2 exponent, 1 mantissa bit: +-{0,0.5,1,1.5,2,3,4,6}); every 16
+ * consecutive values of one token and one head (along head_dim) share one
+ * FP8 E4M3 block scale; each tensor (one layer's K, or its V) has one FP32
+ * global scale g.  A value dequantises to e2m1 * e4m3 * g.  Storage is 9/16
+ * byte per value ("nvfp4-kv-cache-memory-wall", section 1).
+ *
+ * Quantisation of one block (the amax of the block lands on E2M1's 6):
+ *     sb   = E4M3_rne_satfinite(amax / (6 * g))
+ *     code = E2M1_rne_satfinite(x / (E4M3val(sb) * g))
+ * each step one IEEE binary32 operation rounded to nearest; rounding ties go
+ * to the even code; a block whose E4M3val(sb) * g is 0 stores signed zeros.
+ * Inputs (K, V, q) must be finite; non-finite inputs give unspecified codes
+ * and outputs (never an out-of-bounds access).
+ *
+ * Cache layout (all arrays caller-owned device memory, byte-addressed):
+ *     k_data, v_data   : uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
+ *                        element 2i of a row in the low nibble of byte i
+ *     k_scale, v_scale : uint8 [num_pages][num_kv_heads][page_size][head_dim/16]
+ *                        E4M3 block scale j covers elements 16j..16j+15
+ * A slot s is row (s % page_size) of page (s / page_size).  Supported:
+ * head_dim = 128, page_size = 16.  All four base pointers must be 16-byte
+ * aligned.
+ *
+ * Conventions for every call:
+ *   - All pointers named device are CUDA device pointers; the library never
+ *     allocates, frees or synchronises, and never keeps a pointer past a call.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous with respect to the host.  Calls keep no
+ *     state between them and may be made from several host threads.
+ *   - The return value is a host-side status (NVFP4KV_OK or an NVFP4KV_ERR_*
+ *     code).  Argument errors are detected on the host before anything is
+ *     enqueued; nothing is written then.
+ *   - Indices read on the device (slots, page ids, lengths) are range-checked
+ *     by the kernels.  An out-of-range index skips the access it guards (see
+ *     each call) and, if `device_status` is not NULL, ORs an NVFP4KV_DEVERR_*
+ *     bit into that device int32 (the caller zeroes it and reads it back).
+ */
+#ifndef NVFP4KV_H
+#define NVFP4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without CUDA headers. */
+typedef struct CUstream_st* nvfp4kv_stream_t;
+
+/* Host-side status codes. */
+enum {
+  NVFP4KV_OK = 0,
+  NVFP4KV_ERR_INVALID_ARGUMENT = -1, /* null pointer, bad size, misaligned pool, bad scale */
+  NVFP4KV_ERR_UNSUPPORTED = -2,      /* head_dim != 128, page_size != 16, GQA group > 8, or
+                                        sizes whose indices would not fit in 32 bits */
+  NVFP4KV_ERR_CUDA = -3,             /* a CUDA runtime call or launch failed */
+  NVFP4KV_ERR_WORKSPACE = -4         /* workspace null, too small or misaligned */
+};
+
+/* Device-side error bits (ORed into *device_status when it is given). */
+enum {
+  NVFP4KV_DEVERR_SLOT = 1,   /* a slot >= num_pages * page_size: that token was skipped */
+  NVFP4KV_DEVERR_PAGE = 2,   /* a page id outside [0, num_pages): that page was skipped */
+  NVFP4KV_DEVERR_LENGTH = 4, /* a length < 0 or > max_pages_per_seq * page_size: clamped */
+  NVFP4KV_DEVERR_TIMEOUT = 8 /* a copy into shared memory did not complete within ~1 s: the
+                                call's outputs are not valid */
+};
+
+/* One layer's paged NVFP4 cache.  The struct itself is read on the host only. */
+typedef struct nvfp4kv_cache {
+  uint8_t* k_data;      /* device, [num_pages][num_kv_heads][page_size][head_dim/2] */
+  uint8_t* v_data;      /* device, same shape */
+  uint8_t* k_scale;     /* device, [num_pages][num_kv_heads][page_size][head_dim/16] */
+  uint8_t* v_scale;     /* device, same shape */
+  int64_t num_pages;    /* > 0 */
+  int32_t num_kv_heads; /* > 0 */
+  int32_t head_dim;     /* 128 */
+  int32_t page_size;    /* 16 */
+  float k_global_scale; /* g of K: finite, > 0 (the public setting is 1.0) */
+  float v_global_scale; /* g of V: finite, > 0 */
+} nvfp4kv_cache;
+
+/*
+ * Bytes of one data pool and of one scale pool (each of K and V) for a cache
+ * of this shape: num_pages*num_kv_heads*page_size*head_dim/2 and /16.  The
+ * per-value total is 9/16 byte ("nvfp4-kv-cache-memory-wall", section 1).
+ * Host only.  Returns NVFP4KV_OK or NVFP4KV_ERR_INVALID_ARGUMENT.
+ */
+int nvfp4kv_cache_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t page_size, size_t* data_bytes, size_t* scale_bytes);
+
+/*
+ * Quantise new K and V tokens into the cache ("nvfp4-kv-cache-memory-wall",
+ * section 3, flowchart and item 1: new K/V are written to the cache as NVFP4;
+ * nmedialink repost of NVIDIA's blog, figure 3: new keys and values are
+ * quantised before they are appended).
+ *   k, v          device bf16 [num_tokens][num_kv_heads][head_dim], rows contiguous
+ *   slot_mapping  device int64 [num_tokens]; token t goes to slot slot_mapping[t];
+ *                 a negative slot skips the token (padding); a slot past the
+ *                 pool skips the token and raises NVFP4KV_DEVERR_SLOT
+ *   num_tokens    >= 0 (0 enqueues nothing)
+ * K uses cache->k_global_scale and V uses cache->v_global_scale.  Two tokens
+ * mapped to one slot race (unspecified which one lands).
+ */
+int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const void* v,
+                            const int64_t* slot_mapping, int64_t num_tokens,
+                            int32_t* device_status, nvfp4kv_stream_t stream);
+
+/*
+ * Bytes of device workspace nvfp4kv_decode_attention needs for this batch
+ * shape on the current CUDA device (split-K partial results and per-(sequence,
+ * KV head) arrival counters).  Host only; query it with the device current
+ * that will run the decode.
+ */
+int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                  size_t* bytes);
+
+/*
+ * Paged decode attention with the NVFP4 dequantisation inside the kernel
+ * ("nvfp4-kv-cache-memory-wall", section 3, item 3: decode dequantises in
+ * registers, with no separate dequantisation pass, because decode is bound by
+ * the KV read).  For every sequence b and query head h (KV head h / G,
+ * G = num_q_heads / num_kv_heads):
+ *     s_t = softmax_scale * sum_d q[b,h,d] * Khat[t,d]      t < seq_lens[b]
+ *     out[b,h,:] = sum_t softmax(s)_t * Vhat[t,:]
+ * over the dequantised cache (Khat = e2m1*e4m3*g_K, Vhat = e2m1*e4m3*g_V).
+ *   q               device bf16 [batch][num_q_heads][head_dim]
+ *   out             device fp32 [batch][num_q_heads][head_dim]; a sequence of
+ *                   length 0 gets zeros
+ *   page_table      device int32 [batch][max_pages_per_seq]; row b lists the
+ *                   pages of sequence b in token order; entries past
+ *                   ceil(seq_lens[b]/page_size) are not read
+ *   seq_lens        device int32 [batch]
+ *   softmax_scale   finite, > 0 (usually 1/sqrt(head_dim))
+ *   workspace       device, >= nvfp4kv_decode_workspace_size() bytes, 256-byte
+ *                   aligned, ZEROED before its first use; every call leaves it
+ *                   zeroed again, so it can be reused without clearing.  Calls
+ *                   that overlap on the GPU must not share a workspace.
+ * Requires 1 <= G <= 8.  A page id out of range is skipped (its tokens do
+ * not take part) with NVFP4KV_DEVERR_PAGE; a length out of range is clamped
+ * with NVFP4KV_DEVERR_LENGTH.
+ */
+int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* out,
+                             const int32_t* page_table, int32_t max_pages_per_seq,
+                             const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             int32_t* device_status, nvfp4kv_stream_t stream);
+
+/*
+ * Dequantise cached prefixes into an FP8 E4M3 workspace for chunked prefill /
+ * extend ("nvfp4-kv-cache-memory-wall", section 3, item 2: the NVFP4 prefix is
+ * dequantised into one FP8 workspace pair that every layer reuses, so the
+ * workspace does not eat the memory NVFP4 saved).  For token t < prefix_lens[b]
+ * of sequence b, head h, element d:
+ *     ws[cu_prefix[b] + t][h][d] = E4M3_rne_satfinite(fp32(fp32(e2m1*e4m3) * g) / ws_scale)
+ * (sign kept, so -0 is 0x80); a consumer multiplies by ws_scale to recover
+ * e2m1*e4m3*g.
+ *   page_table      device int32 [batch][max_pages_per_seq]
+ *   prefix_lens     device int32 [batch]
+ *   cu_prefix       device int64 [batch + 1], non-decreasing, with
+ *                   cu_prefix[b] + prefix_lens[b] <= cu_prefix[b+1] and
+ *                   cu_prefix[batch] <= total_rows; rows between a prefix's end
+ *                   and the next sequence's start are left untouched
+ *   total_rows      rows of each workspace (host value)
+ *   k_ws_scale, v_ws_scale   finite, > 0
+ *   ws_k, ws_v      device uint8 E4M3 [total_rows][num_kv_heads][head_dim],
+ *                   16-byte aligned
+ * A page id out of range writes zeros for its rows with NVFP4KV_DEVERR_PAGE.
+ */
+int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* page_table,
+                                     int32_t max_pages_per_seq, const int32_t* prefix_lens,
+                                     const int64_t* cu_prefix, int32_t batch, int64_t total_rows,
+                                     float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                     uint8_t* ws_v, int32_t* device_status,
+                                     nvfp4kv_stream_t stream);
+
+/* A static, human-readable string for a status code (never NULL). */
+const char* nvfp4kv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4KV_H */

@@ -1,6 +1,218 @@
-"""nvfp4kv: NVFP4 paged KV cache for one GB300 (sm_103a).
+"""nvfp4kv: an NVFP4 paged KV cache for one GB300 (sm_103a).
 
-The compute lives in the CUDA library ``libnvfp4kv.so`` (see
-``include/nvfp4kv.h``); this package is a thin ctypes binding over it plus
-seeded workload generators (``inputs``).
+All compute lives in the CUDA library ``libnvfp4kv.so`` whose C ABI is
+declared in ``include/nvfp4kv.h``.  This module is a thin ctypes binding with
+the same function names: it only turns torch tensors into pointers and sizes
+and raises on a non-zero status.  PyTorch provides device memory and streams.
+There is no CPU fallback: if the library cannot be loaded, every call raises.
+
+The seeded workload generators live in ``nvfp4_quantized_paged_quantize_gb300.inputs``.
 """
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "_build", "libnvfp4kv.so")
+
+NVFP4KV_OK = 0
+NVFP4KV_ERR_INVALID_ARGUMENT = -1
+NVFP4KV_ERR_UNSUPPORTED = -2
+NVFP4KV_ERR_CUDA = -3
+NVFP4KV_ERR_WORKSPACE = -4
+
+NVFP4KV_DEVERR_SLOT = 1
+NVFP4KV_DEVERR_PAGE = 2
+NVFP4KV_DEVERR_LENGTH = 4
+NVFP4KV_DEVERR_TIMEOUT = 8
+
+HEAD_DIM = 128
+PAGE_SIZE = 16
+
+_lib = None
+
+
+class Nvfp4kvError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        msg = nvfp4kv_status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{func} failed: {msg} ({status})")
+
+
+class _CCache(ctypes.Structure):
+    _fields_ = [
+        ("k_data", ctypes.c_void_p),
+        ("v_data", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int64),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("k_global_scale", ctypes.c_float),
+        ("v_global_scale", ctypes.c_float),
+    ]
+
+
+def load(path: str | None = None, build_if_missing: bool = True):
+    """Load libnvfp4kv.so (building it in-tree first if it is missing or stale).
+
+    Raises if the library cannot be built or loaded: there is no fallback path.
+    """
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = LIB_PATH
+        if build_if_missing:
+            from . import build as _build
+
+            path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libnvfp4kv.so not found at {path}; run build() first")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    pc = ctypes.POINTER(_CCache)
+    L.nvfp4kv_cache_bytes.argtypes = [i64, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.nvfp4kv_quantize_append.argtypes = [pc, vp, vp, vp, i64, vp, vp]
+    L.nvfp4kv_decode_workspace_size.argtypes = [pc, i32, i32, ctypes.POINTER(sz)]
+    L.nvfp4kv_decode_attention.argtypes = [pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz, vp, vp]
+    L.nvfp4kv_dequant_to_fp8_workspace.argtypes = [pc, vp, i32, vp, vp, i32, i64, f32, f32, vp, vp, vp, vp]
+    L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
+    L.nvfp4kv_status_string.restype = ctypes.c_char_p
+    for name in ("nvfp4kv_cache_bytes", "nvfp4kv_quantize_append", "nvfp4kv_decode_workspace_size",
+                 "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _L():
+    return _lib if _lib is not None else load()
+
+
+def _ptr(x) -> int | None:
+    """Device pointer of a tensor (or an int address); None stays NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(func: str, status: int) -> None:
+    if status != NVFP4KV_OK:
+        raise Nvfp4kvError(func, status)
+
+
+@dataclass
+class Cache:
+    """One layer's paged NVFP4 cache: four caller-owned device byte tensors.
+
+    k_data/v_data: uint8 [num_pages, num_kv_heads, page_size, head_dim // 2]
+    k_scale/v_scale: uint8 [num_pages, num_kv_heads, page_size, head_dim // 16] (E4M3)
+    """
+    k_data: object
+    v_data: object
+    k_scale: object
+    v_scale: object
+    num_pages: int
+    num_kv_heads: int
+    k_global_scale: float = 1.0
+    v_global_scale: float = 1.0
+    head_dim: int = HEAD_DIM
+    page_size: int = PAGE_SIZE
+
+    @classmethod
+    def empty(cls, num_pages, num_kv_heads, device="cuda", k_global_scale=1.0, v_global_scale=1.0,
+              zero=False):
+        import torch
+
+        mk = torch.zeros if zero else torch.empty
+        shape_d = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 2)
+        shape_s = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 16)
+        return cls(mk(shape_d, dtype=torch.uint8, device=device), mk(shape_d, dtype=torch.uint8, device=device),
+                   mk(shape_s, dtype=torch.uint8, device=device), mk(shape_s, dtype=torch.uint8, device=device),
+                   num_pages, num_kv_heads, k_global_scale, v_global_scale)
+
+    def c_struct(self) -> _CCache:
+        return _CCache(_ptr(self.k_data), _ptr(self.v_data), _ptr(self.k_scale), _ptr(self.v_scale),
+                       int(self.num_pages), int(self.num_kv_heads), int(self.head_dim), int(self.page_size),
+                       float(self.k_global_scale), float(self.v_global_scale))
+
+
+def nvfp4kv_status_string(status: int) -> str:
+    return _L().nvfp4kv_status_string(int(status)).decode()
+
+
+def nvfp4kv_cache_bytes(num_pages: int, num_kv_heads: int, head_dim: int = HEAD_DIM,
+                        page_size: int = PAGE_SIZE) -> tuple[int, int]:
+    d, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("nvfp4kv_cache_bytes",
+           _L().nvfp4kv_cache_bytes(num_pages, num_kv_heads, head_dim, page_size, ctypes.byref(d),
+                                    ctypes.byref(s)))
+    return d.value, s.value
+
+
+def nvfp4kv_quantize_append(cache: Cache, k, v, slot_mapping, device_status=None, stream=None) -> None:
+    """k, v: bf16 [n, Hkv, 128] device tensors; slot_mapping: int64 [n] device tensor."""
+    n = int(slot_mapping.shape[0]) if hasattr(slot_mapping, "shape") else int(slot_mapping[1])
+    c = cache.c_struct()
+    _check("nvfp4kv_quantize_append",
+           _L().nvfp4kv_quantize_append(ctypes.byref(c), _ptr(k), _ptr(v), _ptr(slot_mapping), n,
+                                        _ptr(device_status), _stream(stream)))
+
+
+def nvfp4kv_decode_workspace_size(cache: Cache, batch: int, num_q_heads: int) -> int:
+    n = ctypes.c_size_t()
+    c = cache.c_struct()
+    _check("nvfp4kv_decode_workspace_size",
+           _L().nvfp4kv_decode_workspace_size(ctypes.byref(c), batch, num_q_heads, ctypes.byref(n)))
+    return n.value
+
+
+def nvfp4kv_decode_attention(cache: Cache, q, out, page_table, seq_lens, softmax_scale: float, workspace,
+                             device_status=None, stream=None, workspace_bytes: int | None = None) -> None:
+    """q: bf16 [B, Hq, 128]; out: fp32 [B, Hq, 128]; page_table: int32 [B, max_pages];
+    seq_lens: int32 [B]; workspace: zero-initialised device buffer (see the header)."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    maxp = int(page_table.shape[1])
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    c = cache.c_struct()
+    _check("nvfp4kv_decode_attention",
+           _L().nvfp4kv_decode_attention(ctypes.byref(c), _ptr(q), _ptr(out), _ptr(page_table), maxp,
+                                         _ptr(seq_lens), B, Hq, float(softmax_scale), _ptr(workspace),
+                                         workspace_bytes, _ptr(device_status), _stream(stream)))
+
+
+def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_prefix, ws_k, ws_v,
+                                     k_ws_scale: float = 1.0, v_ws_scale: float = 1.0, device_status=None,
+                                     stream=None) -> None:
+    """ws_k, ws_v: uint8 [total_rows, Hkv, 128] device tensors (E4M3 bytes)."""
+    B = int(prefix_lens.shape[0])
+    maxp = int(page_table.shape[1])
+    total_rows = int(ws_k.shape[0])
+    c = cache.c_struct()
+    _check("nvfp4kv_dequant_to_fp8_workspace",
+           _L().nvfp4kv_dequant_to_fp8_workspace(ctypes.byref(c), _ptr(page_table), maxp, _ptr(prefix_lens),
+                                                 _ptr(cu_prefix), B, total_rows, float(k_ws_scale),
+                                                 float(v_ws_scale), _ptr(ws_k), _ptr(ws_v),
+                                                 _ptr(device_status), _stream(stream)))
+
+
+__all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quantize_append",
+           "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
+           "nvfp4kv_status_string"]

@@ -1,0 +1,172 @@
+// api.cu -- the C ABI of libnvfp4kv.so (declared in include/nvfp4kv.h): host
+// validation, size queries and kernel launches.  Nothing here allocates device
+// memory or synchronises; every launch goes to the caller's stream.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "nvfp4kv.h"
+#include "nvfp4kv_launch.h"
+
+namespace {
+
+constexpr int kHeadDim = 128;
+
+constexpr int kPageSize = 16;
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];  // 0 = not queried yet
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool positive_finite(float x) { return std::isfinite(x) && x > 0.0f; }
+
+// SM count of the current device (cached; the query is a host call).
+int current_num_sms(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4KV_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) {
+    int cached = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (cached > 0) {
+      *num_sms = cached;
+      return NVFP4KV_OK;
+    }
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return NVFP4KV_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) g_num_sms[dev].store(n, std::memory_order_relaxed);
+  *num_sms = n;
+  return NVFP4KV_OK;
+}
+
+// Shape and pointer checks common to every call that reads or writes the pool.
+int check_cache(const nvfp4kv_cache* c) {
+  if (c == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (c->head_dim != kHeadDim || c->page_size != kPageSize) return NVFP4KV_ERR_UNSUPPORTED;
+  if (c->num_pages <= 0 || c->num_kv_heads <= 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  // row indices (page * heads + head) * page_size stay below 2^31
+  if (c->num_pages * (int64_t)c->num_kv_heads * kPageSize >= (int64_t(1) << 31))
+    return NVFP4KV_ERR_UNSUPPORTED;
+  if (!c->k_data || !c->v_data || !c->k_scale || !c->v_scale) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!aligned(c->k_data, 16) || !aligned(c->v_data, 16) || !aligned(c->k_scale, 16) ||
+      !aligned(c->v_scale, 16))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!positive_finite(c->k_global_scale) || !positive_finite(c->v_global_scale))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  return NVFP4KV_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4kv_cache_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                        size_t* data_bytes, size_t* scale_bytes) {
+  if (data_bytes == nullptr || scale_bytes == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_pages <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || head_dim % 16 != 0)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  const int64_t rows = num_pages * num_kv_heads * (int64_t)page_size;
+  *data_bytes = (size_t)(rows * (head_dim / 2));
+  *scale_bytes = (size_t)(rows * (head_dim / 16));
+  return NVFP4KV_OK;
+}
+
+int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const void* v,
+                            const int64_t* slot_mapping, int64_t num_tokens, int32_t* device_status,
+                            nvfp4kv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != NVFP4KV_OK) return st;
+  if (num_tokens < 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return NVFP4KV_OK;
+  if (num_tokens * (int64_t)cache->num_kv_heads >= (int64_t(1) << 31)) return NVFP4KV_ERR_UNSUPPORTED;
+  if (!k || !v || !slot_mapping) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
+  return cuda_status(nvfp4kv::launch_quantize_append(
+      *cache, static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slot_mapping, num_tokens,
+      device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                  size_t* bytes) {
+  if (bytes == nullptr || cache == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (cache->num_kv_heads <= 0 || batch < 0 || num_q_heads <= 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  int st = current_num_sms(&nsm);
+  if (st != NVFP4KV_OK) return st;
+  *bytes = nvfp4kv::decode_workspace_bytes(nvfp4kv::decode_num_ctas(nsm), batch, cache->num_kv_heads);
+  return NVFP4KV_OK;
+}
+
+int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* out,
+                             const int32_t* page_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                             int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
+                             size_t workspace_bytes, int32_t* device_status, nvfp4kv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != NVFP4KV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % cache->num_kv_heads != 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  const int group = num_q_heads / cache->num_kv_heads;
+  if (group > 8) return NVFP4KV_ERR_UNSUPPORTED;
+  if (!positive_finite(softmax_scale)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return NVFP4KV_OK;
+  // global page-head indices (sequence pages times KV heads) stay below 2^31
+  if ((int64_t)batch * max_pages_per_seq * cache->num_kv_heads >= (int64_t(1) << 31) ||
+      (int64_t)max_pages_per_seq * kPageSize >= (int64_t(1) << 31))
+    return NVFP4KV_ERR_UNSUPPORTED;
+  if (!q || !out || !page_table || !seq_lens) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
+  const size_t need = nvfp4kv::decode_workspace_bytes(nvfp4kv::decode_num_ctas(nsm), batch,
+                                                      cache->num_kv_heads);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return NVFP4KV_ERR_WORKSPACE;
+  return cuda_status(nvfp4kv::launch_decode(*cache, static_cast<const uint16_t*>(q), out, page_table,
+                                            max_pages_per_seq, seq_lens, batch, num_q_heads, softmax_scale,
+                                            workspace, device_status, nsm,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* page_table,
+                                     int32_t max_pages_per_seq, const int32_t* prefix_lens,
+                                     const int64_t* cu_prefix, int32_t batch, int64_t total_rows,
+                                     float k_ws_scale, float v_ws_scale, uint8_t* ws_k, uint8_t* ws_v,
+                                     int32_t* device_status, nvfp4kv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != NVFP4KV_OK) return st;
+  if (batch < 0 || total_rows < 0 || max_pages_per_seq <= 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!positive_finite(k_ws_scale) || !positive_finite(v_ws_scale)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (batch == 0 || total_rows == 0) return NVFP4KV_OK;
+  if ((int64_t)max_pages_per_seq * kPageSize >= (int64_t(1) << 31)) return NVFP4KV_ERR_UNSUPPORTED;
+  if (total_rows * cache->num_kv_heads >= (int64_t(1) << 40)) return NVFP4KV_ERR_UNSUPPORTED;
+  if (!page_table || !prefix_lens || !cu_prefix || !ws_k || !ws_v) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!aligned(page_table, 4) || !aligned(prefix_lens, 4) || !aligned(cu_prefix, 8) || !aligned(ws_k, 16) ||
+      !aligned(ws_v, 16))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
+  return cuda_status(nvfp4kv::launch_dequant_fp8(*cache, page_table, max_pages_per_seq, prefix_lens, cu_prefix,
+                                                 batch, total_rows, k_ws_scale, v_ws_scale, ws_k, ws_v,
+                                                 device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* nvfp4kv_status_string(int status) {
+  switch (status) {
+    case NVFP4KV_OK: return "ok";
+    case NVFP4KV_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case NVFP4KV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NVFP4KV_ERR_CUDA: return "CUDA error (see cudaGetLastError)";
+    case NVFP4KV_ERR_WORKSPACE: return "workspace null, too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,772 @@
+// decode_attention.cu -- paged GQA decode attention over the NVFP4 cache with
+// the dequantisation inside the kernel ("nvfp4-kv-cache-memory-wall", section
+// 3, item 3: decode dequantises in registers with no separate pass, because
+// decode is bound by the KV read; a round trip through memory would read and
+// write the whole cache once more).
+//
+// Work partition (split-K, balanced): the flattened list of (sequence, KV
+// head, page) items -- "page-heads" -- is cut into gridDim.x contiguous ranges
+// whose sizes differ by at most one, one per CTA, and each CTA range into kNW
+// such ranges, one per warp.
+// A warp streams its pages through a private ring of kStages shared-memory
+// stages filled by 1-D TMA bulk copies (K data 1 KiB, V data 1 KiB, K and V
+// scales 128 B each per page and head), completion counted on one mbarrier
+// per stage.  For each page it
+//   1. converts K's E2M1 pairs to f16x2 with cvt.rn.f16x2.e2m1x2, multiplies
+//      by the E4M3 block scale (exact in f16), and computes S^T = Khat q^T for
+//      the 16 tokens x G query heads with mma.sync m16n8k16 (f16 in, f32 acc);
+//   2. runs the online softmax in base 2 (scores scaled by softmax_scale *
+//      log2(e) * g_K); the running max is only raised when a score exceeds it
+//      by more than 8, so the rescale of the accumulators is rare;
+//   3. transposes P (f16) with movmatrix and accumulates O^T += Vhat^T P^T,
+//      Vhat^T built from nibble-interleaved V bytes and scaled per token.
+// A (sequence, KV head) pair that lies inside one warp range is finished by
+// that warp.  Pieces of pairs cut by warp boundaries are merged in shared
+// memory; pieces cut by CTA boundaries are written to the workspace, and the
+// last CTA to arrive on the pair's counter (atomicAdd, no spinning) merges
+// them and resets the counter to 0.
+//
+// Exactness: e2m1 * E4M3 has at most 6 significant bits in [2^-10, 2688], so
+// Khat and Vhat are exact in f16.  q is bf16; it is multiplied by a power of
+// two per head so its largest element sits in [2^14, 2^15) before rounding to
+// f16, and the factor is folded back into the score scale.
+#include <cstdint>
+
+#include "nvfp4kv_device.cuh"
+#include "nvfp4kv_launch.h"
+
+namespace nvfp4kv {
+namespace {
+
+constexpr int kNW = 4;          // warps per CTA (each streams its own pages)
+constexpr int kStages = 4;      // pages in flight per warp
+constexpr int kCtasPerSm = 4;   // resident CTAs per SM the launch is sized for
+constexpr int kGMax = 8;        // query heads per KV head (one MMA n-tile)
+constexpr float kLazy = 8.0f;   // running-max slack (log2 units): P <= 2^8 in f16
+
+// stage layout: K data | V data | K scales | V scales
+constexpr int kOffKD = 0;
+constexpr int kOffVD = kPageDataBytes;
+constexpr int kOffKS = 2 * kPageDataBytes;
+constexpr int kOffVS = 2 * kPageDataBytes + kPageScaleBytes;
+constexpr int kStageBytes = 2 * kPageDataBytes + 2 * kPageScaleBytes;  // 2304
+
+// a (partial) result record: O[kGMax][128] unnormalised, m[kGMax] (base 2), l[kGMax]
+constexpr int kRecFloats = kGMax * kHeadDim + 2 * kGMax;
+constexpr int kOffM = kGMax * kHeadDim;
+constexpr int kOffL = kGMax * kHeadDim + kGMax;
+
+constexpr int kRingBytes = kNW * kStages * kStageBytes;
+constexpr int kBarBytes = kNW * kStages * 8;
+constexpr int kSlot0Bytes = kNW * kRecFloats * 4;
+constexpr int kSmemBytes = kRingBytes + kBarBytes + kSlot0Bytes;
+static_assert(kStages * kStageBytes >= kRecFloats * 4, "a warp's ring must hold one record");
+
+struct DecodeParams {
+  const uint8_t* k_data;
+  const uint8_t* v_data;
+  const uint8_t* k_scale;
+  const uint8_t* v_scale;
+  int32_t num_pages;
+  int32_t hkv;
+  const uint16_t* q;
+  float* out;
+  const int32_t* page_table;
+  int32_t max_pages;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t hq;
+  int32_t group;
+  float score_scale;  // softmax_scale * log2(e) * g_K
+  float v_gscale;     // g_V
+  float* part;        // [num_ctas + batch * hkv] records
+  int32_t* counters;  // [batch * hkv]
+  int32_t* status;
+};
+
+struct SlotInfo {
+  int pair;        // b * hkv + h, or -1 for an empty slot
+  int first_page;  // pages [first_page, last_page] of the pair are merged here
+  int last_page;
+  int np;          // pages of the pair
+  long long r_first;  // global page-head index of first_page
+};
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
+  int L = __ldg(p.seq_lens + b);
+  const int lmax = p.max_pages * kPage;
+  if (L < 0 || L > lmax) {
+    flag_error(p.status, NVFP4KV_DEVERR_LENGTH);
+    L = L < 0 ? 0 : lmax;
+  }
+  return L;
+}
+
+__device__ __forceinline__ int pages_of(const DecodeParams& p, int b) {
+  return (clamp_len(p, b) + kPage - 1) / kPage;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t dup_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
+__device__ __forceinline__ uint32_t dup_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
+
+template <int K>
+__device__ __forceinline__ uint32_t cvt_sel(uint32_t w) { return e2m1x2_to_f16x2<K>(w); }
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Balanced partition of W page-heads over N CTAs: the first W % N CTAs take
+// W / N + 1, the rest W / N, so CTAs with an empty range (W < N) all come last
+// and the CTAs that cover any pair are consecutive.
+__device__ __forceinline__ long long cta_start(long long c, long long W, long long N) {
+  const long long q = W / N, rem = W % N;
+  return c * q + (c < rem ? c : rem);
+}
+
+// The CTA whose range holds global page-head r (0 <= r < W).
+__device__ __forceinline__ long long cta_of(long long r, long long W, long long N) {
+  const long long q = W / N, rem = W % N, big = rem * (q + 1);
+  return r < big ? r / (q + 1) : rem + (r - big) / q;
+}
+
+// Where each item of a 32-item chunk of a warp's range lives (one per lane).
+struct ItemMap {
+  int row;     // physical row pid * hkv + h of the page-head, -1 if the page id is invalid
+  int pair;    // b * hkv + h, -1 past the warp's range
+  int page;    // page index within the sequence
+  int np;      // pages of the pair
+  int nvalid;  // valid tokens in the page (1..16)
+};
+
+// Map items [i0, i0 + 32) of the warp range starting at wr0 (n items) to pages.
+// (cb, ccu) is a sequence whose first page-head is <= the chunk's first item;
+// on return it is the sequence of the chunk's last valid item.
+__device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr0, int i0, int n, int& cb,
+                                             int& ccu, int lane) {
+  ItemMap m;
+  m.row = -1;
+  m.pair = -1;
+  m.page = 0;
+  m.np = 1;
+  m.nvalid = 0;
+  const int i = i0 + lane;
+  int b = cb, cu = ccu;
+  if (i < n) {
+    const long long r = wr0 + i;
+    int np = pages_of(p, b);
+    while (r >= (long long)(cu + np) * p.hkv) {
+      cu += np;
+      ++b;
+      np = pages_of(p, b);
+    }
+    const int local = (int)(r - (long long)cu * p.hkv);
+    const int h = local / np;
+    const int page = local - h * np;
+    const int L = clamp_len(p, b);
+    m.pair = b * p.hkv + h;
+    m.page = page;
+    m.np = np;
+    m.nvalid = min(kPage, L - page * kPage);
+    const int pid = __ldg(p.page_table + (long long)b * p.max_pages + page);
+    if (pid >= 0 && pid < p.num_pages) {
+      m.row = pid * p.hkv + h;
+    } else {
+      flag_error(p.status, NVFP4KV_DEVERR_PAGE);
+    }
+  }
+  const int last = min(31, n - 1 - i0);
+  cb = __shfl_sync(0xFFFFFFFFu, b, last);
+  ccu = __shfl_sync(0xFFFFFFFFu, cu, last);
+  return m;
+}
+
+__device__ __forceinline__ ItemMap shfl_map(const ItemMap& m, int src) {
+  ItemMap r;
+  r.row = __shfl_sync(0xFFFFFFFFu, m.row, src);
+  r.pair = __shfl_sync(0xFFFFFFFFu, m.pair, src);
+  r.page = __shfl_sync(0xFFFFFFFFu, m.page, src);
+  r.np = __shfl_sync(0xFFFFFFFFu, m.np, src);
+  r.nvalid = __shfl_sync(0xFFFFFFFFu, m.nvalid, src);
+  return r;
+}
+
+// Lane 0 starts the copies of one page-head (K/V data and scales) into a ring
+// stage; an invalid page (row < 0) only arrives on the barrier.
+__device__ __forceinline__ void issue_page(const DecodeParams& p, int row, uint8_t* st, uint32_t bar, int lane) {
+  if (lane != 0) return;
+  if (row >= 0) {
+    const long long off = (long long)row * kPage;
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    tma_load_1d(smem_u32(st + kOffKD), p.k_data + off * kRowBytes, kPageDataBytes, bar);
+    tma_load_1d(smem_u32(st + kOffVD), p.v_data + off * kRowBytes, kPageDataBytes, bar);
+    tma_load_1d(smem_u32(st + kOffKS), p.k_scale + off * kRowScales, kPageScaleBytes, bar);
+    tma_load_1d(smem_u32(st + kOffVS), p.v_scale + off * kRowScales, kPageScaleBytes, bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+// Per-warp attention state of the current pair.
+struct WarpState {
+  float o[8][4];    // O^T tiles: tile i rows d = 16g+2i (c0,c1) and 16g+2i+1 (c2,c3), cols heads 2t,2t+1
+  uint32_t qf[8][2];  // q B-fragments: tile i holds q[head g][32t+4i .. 32t+4i+3]
+  float m0, m1;     // running max (base 2) of heads 2t, 2t+1
+  float l0, l1;     // this lane's partial sums of P over its tokens
+  float c0, c1;     // score multipliers of heads 2t, 2t+1
+};
+
+// Load q for pair (b, h) into B-fragments with a per-head power-of-two prescale.
+__device__ __forceinline__ void load_q(const DecodeParams& p, int pair, WarpState& s, int g, int t) {
+  const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
+  float qv[32];
+  if (g < p.group) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + ((long long)b * p.hq + (long long)h * p.group + g) * kHeadDim + 32 * t);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = __ldg(src + j);
+      qv[8 * j + 0] = bf16_to_f32(w.x & 0xFFFFu); qv[8 * j + 1] = bf16_to_f32(w.x >> 16);
+      qv[8 * j + 2] = bf16_to_f32(w.y & 0xFFFFu); qv[8 * j + 3] = bf16_to_f32(w.y >> 16);
+      qv[8 * j + 4] = bf16_to_f32(w.z & 0xFFFFu); qv[8 * j + 5] = bf16_to_f32(w.z >> 16);
+      qv[8 * j + 6] = bf16_to_f32(w.w & 0xFFFFu); qv[8 * j + 7] = bf16_to_f32(w.w >> 16);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) qv[j] = 0.0f;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  // prescale 2^e so that amax * 2^e lies in [2^14, 2^15); e clamped to +-100
+  int e = 0;
+  if (amax > 0.0f) {
+    const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;  // floor(log2 amax) for normals
+    e = 14 - ex;
+    e = e > 100 ? 100 : (e < -100 ? -100 : e);
+  }
+  const float pre = __uint_as_float((uint32_t)(e + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    s.qf[i][0] = pack_f16x2(qv[4 * i] * pre, qv[4 * i + 1] * pre);
+    s.qf[i][1] = pack_f16x2(qv[4 * i + 2] * pre, qv[4 * i + 3] * pre);
+  }
+  const float c = p.score_scale * inv;  // score multiplier of head g
+  s.c0 = __shfl_sync(0xFFFFFFFFu, c, (2 * t) * 4);
+  s.c1 = __shfl_sync(0xFFFFFFFFu, c, (2 * t + 1) * 4);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s.o[i][j] = 0.0f;
+  s.m0 = s.m1 = -INFINITY;
+  s.l0 = s.l1 = 0.0f;
+}
+
+// One page of one KV head (16 tokens, nvalid of them valid) from a ring stage.
+__device__ __forceinline__ void process_page(const uint8_t* stage, int nvalid, WarpState& s, int g, int t) {
+  // ---- S^T = Khat q^T --------------------------------------------------------
+  const uint8_t* kd = stage + kOffKD;
+  const uint8_t* ks = stage + kOffKS;
+  const uint4 ka = *reinterpret_cast<const uint4*>(kd + g * kRowBytes + 16 * t);
+  const uint4 kb = *reinterpret_cast<const uint4*>(kd + (g + 8) * kRowBytes + 16 * t);
+  const uint32_t ska = *reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t);
+  const uint32_t skb = *reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t);
+  const uint32_t sa = e4m3x2_to_f16x2(ska);  // (block 2t, block 2t+1) of token g
+  const uint32_t sb = e4m3x2_to_f16x2(skb);  // same for token g + 8
+  const uint32_t sa0 = dup_lo(sa), sa1 = dup_hi(sa), sb0 = dup_lo(sb), sb1 = dup_hi(sb);
+  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t wa = word_of(ka, i >> 1), wb = word_of(kb, i >> 1);
+    uint32_t a0, a1, a2, a3;
+    if (i & 1) {
+      a0 = cvt_sel<2>(wa); a1 = cvt_sel<2>(wb); a2 = cvt_sel<3>(wa); a3 = cvt_sel<3>(wb);
+    } else {
+      a0 = cvt_sel<0>(wa); a1 = cvt_sel<0>(wb); a2 = cvt_sel<1>(wa); a3 = cvt_sel<1>(wb);
+    }
+    const uint32_t s_g = i < 4 ? sa0 : sa1, s_g8 = i < 4 ? sb0 : sb1;
+    a0 = hmul2(a0, s_g); a2 = hmul2(a2, s_g); a1 = hmul2(a1, s_g8); a3 = hmul2(a3, s_g8);
+    mma16816(sc, a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
+  }
+
+  // ---- online softmax (base 2) ----------------------------------------------
+  float x0 = sc[0] * s.c0, x1 = sc[1] * s.c1, x2 = sc[2] * s.c0, x3 = sc[3] * s.c1;
+  if (nvalid < kPage) {
+    if (g >= nvalid) x0 = x1 = -INFINITY;
+    if (g + 8 >= nvalid) x2 = x3 = -INFINITY;
+  }
+  float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+  const bool need = (mx0 > s.m0 + kLazy) || (mx1 > s.m1 + kLazy);
+  if (__any_sync(0xFFFFFFFFu, need)) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+    }
+    const float n0 = fmaxf(s.m0, mx0), n1 = fmaxf(s.m1, mx1);
+    const float f0 = ex2(s.m0 - n0), f1 = ex2(s.m1 - n1);
+    s.l0 *= f0;
+    s.l1 *= f1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s.o[i][0] *= f0; s.o[i][1] *= f1; s.o[i][2] *= f0; s.o[i][3] *= f1;
+    }
+    s.m0 = n0;
+    s.m1 = n1;
+  }
+  const float p0 = ex2(x0 - s.m0), p1 = ex2(x1 - s.m1), p2 = ex2(x2 - s.m0), p3 = ex2(x3 - s.m1);
+  s.l0 += p0 + p2;
+  s.l1 += p1 + p3;
+  // P^T (tokens x heads) in the accumulator layout -> B fragments (k = tokens, n = heads)
+  const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+  const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+
+  // ---- O^T += Vhat^T P^T -----------------------------------------------------
+  const uint8_t* vd = stage + kOffVD;
+  const uint8_t* vs = stage + kOffVS;
+  const int t0 = 2 * t, t1 = 2 * t + 1, t8 = 2 * t + 8, t9 = 2 * t + 9;
+  uint32_t s0 = vs[t0 * kRowScales + g], s1 = vs[t1 * kRowScales + g];
+  uint32_t s8 = vs[t8 * kRowScales + g], s9 = vs[t9 * kRowScales + g];
+  if (nvalid < kPage) {  // tokens past the end: scale 0 keeps unwritten bytes out of the sum
+    if (t0 >= nvalid) s0 = 0;
+    if (t1 >= nvalid) s1 = 0;
+    if (t8 >= nvalid) s8 = 0;
+    if (t9 >= nvalid) s9 = 0;
+  }
+  const uint32_t sv01 = e4m3x2_to_f16x2(s0 | (s1 << 8));  // (token 2t, token 2t+1)
+  const uint32_t sv89 = e4m3x2_to_f16x2(s8 | (s9 << 8));
+  const uint2 d0 = *reinterpret_cast<const uint2*>(vd + t0 * kRowBytes + 8 * g);
+  const uint2 d1 = *reinterpret_cast<const uint2*>(vd + t1 * kRowBytes + 8 * g);
+  const uint2 d8 = *reinterpret_cast<const uint2*>(vd + t8 * kRowBytes + 8 * g);
+  const uint2 d9 = *reinterpret_cast<const uint2*>(vd + t9 * kRowBytes + 8 * g);
+  // interleave nibbles of two tokens: byte j of lo = (even d of token a, even d of token b)
+  const uint32_t lo01a = (d0.x & 0x0F0F0F0Fu) | ((d1.x << 4) & 0xF0F0F0F0u);
+  const uint32_t hi01a = ((d0.x >> 4) & 0x0F0F0F0Fu) | (d1.x & 0xF0F0F0F0u);
+  const uint32_t lo01b = (d0.y & 0x0F0F0F0Fu) | ((d1.y << 4) & 0xF0F0F0F0u);
+  const uint32_t hi01b = ((d0.y >> 4) & 0x0F0F0F0Fu) | (d1.y & 0xF0F0F0F0u);
+  const uint32_t lo89a = (d8.x & 0x0F0F0F0Fu) | ((d9.x << 4) & 0xF0F0F0F0u);
+  const uint32_t hi89a = ((d8.x >> 4) & 0x0F0F0F0Fu) | (d9.x & 0xF0F0F0F0u);
+  const uint32_t lo89b = (d8.y & 0x0F0F0F0Fu) | ((d9.y << 4) & 0xF0F0F0F0u);
+  const uint32_t hi89b = ((d8.y >> 4) & 0x0F0F0F0Fu) | (d9.y & 0xF0F0F0F0u);
+#define NVFP4KV_PV_TILE(I, LO01, HI01, LO89, HI89, K)                                   \
+  {                                                                                     \
+    const uint32_t a0 = hmul2(cvt_sel<K>(LO01), sv01);                                  \
+    const uint32_t a1 = hmul2(cvt_sel<K>(HI01), sv01);                                  \
+    const uint32_t a2 = hmul2(cvt_sel<K>(LO89), sv89);                                  \
+    const uint32_t a3 = hmul2(cvt_sel<K>(HI89), sv89);                                  \
+    mma16816(s.o[I], a0, a1, a2, a3, pb0, pb1);                                         \
+  }
+  NVFP4KV_PV_TILE(0, lo01a, hi01a, lo89a, hi89a, 0)
+  NVFP4KV_PV_TILE(1, lo01a, hi01a, lo89a, hi89a, 1)
+  NVFP4KV_PV_TILE(2, lo01a, hi01a, lo89a, hi89a, 2)
+  NVFP4KV_PV_TILE(3, lo01a, hi01a, lo89a, hi89a, 3)
+  NVFP4KV_PV_TILE(4, lo01b, hi01b, lo89b, hi89b, 0)
+  NVFP4KV_PV_TILE(5, lo01b, hi01b, lo89b, hi89b, 1)
+  NVFP4KV_PV_TILE(6, lo01b, hi01b, lo89b, hi89b, 2)
+  NVFP4KV_PV_TILE(7, lo01b, hi01b, lo89b, hi89b, 3)
+#undef NVFP4KV_PV_TILE
+}
+
+// Finish a warp's piece of a pair: total l over the lanes, then either write
+// the final output (complete pair) or store a record into `slot` (shared).
+__device__ __forceinline__ void finish_piece(const DecodeParams& p, WarpState& s, int pair, bool complete,
+                                             float* slot, int g, int t) {
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    s.l0 += __shfl_xor_sync(0xFFFFFFFFu, s.l0, off);
+    s.l1 += __shfl_xor_sync(0xFFFFFFFFu, s.l1, off);
+  }
+  const int h0 = 2 * t, h1 = 2 * t + 1;
+  if (complete) {
+    const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
+    float* base = p.out + ((long long)b * p.hq + (long long)h * p.group) * kHeadDim;
+    const float r0 = s.l0 > 0.0f ? p.v_gscale / s.l0 : 0.0f;
+    const float r1 = s.l1 > 0.0f ? p.v_gscale / s.l1 : 0.0f;
+    if (h0 < p.group) {
+      float4* dst = reinterpret_cast<float4*>(base + h0 * kHeadDim + 16 * g);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[j] = make_float4(s.o[2 * j][0] * r0, s.o[2 * j][2] * r0, s.o[2 * j + 1][0] * r0, s.o[2 * j + 1][2] * r0);
+    }
+    if (h1 < p.group) {
+      float4* dst = reinterpret_cast<float4*>(base + h1 * kHeadDim + 16 * g);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[j] = make_float4(s.o[2 * j][1] * r1, s.o[2 * j][3] * r1, s.o[2 * j + 1][1] * r1, s.o[2 * j + 1][3] * r1);
+    }
+  } else {
+    float4* d0 = reinterpret_cast<float4*>(slot + h0 * kHeadDim + 16 * g);
+    float4* d1 = reinterpret_cast<float4*>(slot + h1 * kHeadDim + 16 * g);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      d0[j] = make_float4(s.o[2 * j][0], s.o[2 * j][2], s.o[2 * j + 1][0], s.o[2 * j + 1][2]);
+      d1[j] = make_float4(s.o[2 * j][1], s.o[2 * j][3], s.o[2 * j + 1][1], s.o[2 * j + 1][3]);
+    }
+    if (g == 0) {
+      slot[kOffM + h0] = s.m0;
+      slot[kOffM + h1] = s.m1;
+      slot[kOffL + h0] = s.l0;
+      slot[kOffL + h1] = s.l1;
+    }
+  }
+}
+
+__device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int warp, int lane) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  long long total = 0;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) total += red[w];
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
+  float* slot0 = reinterpret_cast<float*>(smem + kRingBytes + kBarBytes);
+  __shared__ SlotInfo sinfo[kNW][2];
+  __shared__ long long red[kNW];
+  __shared__ int wstart_b[kNW], wstart_cu[kNW];
+  __shared__ int run_first[2 * kNW], run_count[2 * kNW], slot_order[2 * kNW];
+  __shared__ int s_nruns, s_last;
+  __shared__ long long s_cfirst, s_clast;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  // ---- prologue: total work, zero outputs of empty sequences -------------------
+  long long pages_local = 0;
+  for (int b = tid; b < p.batch; b += kNW * 32) {
+    const int L = clamp_len(p, b);
+    pages_local += (L + kPage - 1) / kPage;
+    if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
+      float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
+      for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  const long long W = block_sum_ll(pages_local, red, warp, lane) * p.hkv;
+  if (W == 0) return;
+  const long long N = gridDim.x;
+  const long long r0 = cta_start(blockIdx.x, W, N);
+  const long long r1 = cta_start((long long)blockIdx.x + 1, W, N);
+
+  // ---- locate the sequence holding each warp's first page-head ----------------
+  if (tid < kNW) wstart_b[tid] = -1;
+  __syncthreads();
+  {
+    int carry = 0;
+    for (int base = 0; base < p.batch; base += kNW * 32) {
+      const int b = base + tid;
+      const int np = b < p.batch ? pages_of(p, b) : 0;
+      int incl = np;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (lane == 31) red[warp] = incl;
+      __syncthreads();
+      int before = carry, chunk = 0;
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) {
+        if (w < warp) before += (int)red[w];
+        chunk += (int)red[w];
+      }
+      const int excl = before + incl - np;
+      if (np > 0) {
+        for (int w2 = 0; w2 < kNW; ++w2) {
+          const long long ws = r0 + (r1 - r0) * w2 / kNW, we = r0 + (r1 - r0) * (w2 + 1) / kNW;
+          if (ws < we && ws >= (long long)excl * p.hkv && ws < (long long)(excl + np) * p.hkv) {
+            wstart_b[w2] = b;
+            wstart_cu[w2] = excl;
+          }
+        }
+      }
+      carry += chunk;
+      __syncthreads();
+    }
+  }
+
+  // ---- per-warp streaming over its page-heads ----------------------------------
+  const long long wr0 = r0 + (r1 - r0) * warp / kNW;
+  const long long wr1 = r0 + (r1 - r0) * (warp + 1) / kNW;
+  const int n = (int)(wr1 - wr0);
+  uint8_t* wring = ring + warp * kStages * kStageBytes;
+  const uint32_t wbar = smem_u32(bars + warp * kStages);
+  float* wslot0 = slot0 + warp * kRecFloats;
+  float* wslot1 = reinterpret_cast<float*>(wring);  // the ring is free once the warp is done
+  if (lane == 0) {
+    sinfo[warp][0].pair = -1;
+    sinfo[warp][1].pair = -1;
+  }
+
+  if (n > 0) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) mbar_init(wbar + 8 * s, 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    int cb = wstart_b[warp], ccu = wstart_cu[warp];
+    ItemMap cur = map_chunk(p, wr0, 0, n, cb, ccu, lane);
+    ItemMap nxt;
+    nxt.row = -1;
+    nxt.pair = -1; nxt.page = 0; nxt.np = 1; nxt.nvalid = 0;
+    if (n > 32) nxt = map_chunk(p, wr0, 32, n, cb, ccu, lane);
+
+    bool ok = true;  // false after a wait gave up: stop issuing and computing
+    // producer: prefill the ring
+    const int pre = n < kStages ? n : kStages;
+    for (int j = 0; j < pre; ++j)
+      issue_page(p, __shfl_sync(0xFFFFFFFFu, cur.row, j), wring + j * kStageBytes, wbar + 8 * j, lane);
+    int issued = pre;
+
+    WarpState s;
+    int seg_pair = -1, seg_first = 0, seg_last = 0, seg_np = 1, nseg = 0;
+    long long seg_r = 0;
+    for (int i = 0; i < n; ++i) {
+      if (i > 0 && (i & 31) == 0) {
+        cur = nxt;
+        if (i + 32 < n) nxt = map_chunk(p, wr0, i + 32, n, cb, ccu, lane);
+      }
+      const ItemMap it = shfl_map(cur, i & 31);
+      if (it.pair != seg_pair) {
+        if (seg_pair >= 0) {
+          // a piece that ends before the warp range does: complete unless it is the first
+          const bool complete = seg_first == 0 && seg_last == seg_np - 1;
+          finish_piece(p, s, seg_pair, complete, wslot0, g, t);
+          if (!complete && lane == 0) {
+            sinfo[warp][0] = SlotInfo{seg_pair, seg_first, seg_last, seg_np, seg_r};
+          }
+        }
+        seg_pair = it.pair;
+        seg_first = it.page;
+        seg_np = it.np;
+        seg_r = wr0 + i;
+        ++nseg;
+        load_q(p, seg_pair, s, g, t);
+      }
+      seg_last = it.page;
+      const int stage = i % kStages;
+      if (ok) {
+        // every lane waits; the outcome is made warp-uniform before it is used
+        const bool done = mbar_wait(wbar + 8 * stage, (uint32_t)((i / kStages) & 1));
+        if (!__all_sync(0xFFFFFFFFu, done)) {
+          ok = false;
+          if (lane == 0) flag_error(p.status, kDevErrTimeout);
+        }
+      }
+      if (ok && it.row >= 0) process_page(wring + stage * kStageBytes, it.nvalid, s, g, t);
+      __syncwarp();
+      // refill this stage with item i + kStages
+      const int j = i + kStages;
+      if (ok && j < n) {
+        const int src = j & 31;
+        const int row = ((j >> 5) == (i >> 5)) ? __shfl_sync(0xFFFFFFFFu, cur.row, src)
+                                               : __shfl_sync(0xFFFFFFFFu, nxt.row, src);
+        issue_page(p, row, wring + stage * kStageBytes, wbar + 8 * stage, lane);
+        issued = j + 1;
+      }
+    }
+    if (!ok) {
+      // drain: wait (bounded) for every copy still in flight before the ring is reused
+      for (int j = issued - kStages; j < issued; ++j) {
+        if (j < 0) continue;
+        mbar_wait(wbar + 8 * (j % kStages), (uint32_t)((j / kStages) & 1));
+      }
+    }
+    __syncwarp();
+    // the last piece of the warp range
+    const bool complete = seg_first == 0 && seg_last == seg_np - 1;
+    float* slot = nseg == 1 ? wslot0 : wslot1;
+    finish_piece(p, s, seg_pair, complete, slot, g, t);
+    if (!complete && lane == 0) sinfo[warp][nseg == 1 ? 0 : 1] = SlotInfo{seg_pair, seg_first, seg_last, seg_np, seg_r};
+  }
+  __syncthreads();
+
+  // ---- merge pieces cut by warp boundaries; hand pieces cut by CTA boundaries on
+  if (tid == 0) {
+    int nr = 0, ns = 0;
+    int prev = -2;
+    for (int w = 0; w < kNW; ++w)
+      for (int k = 0; k < 2; ++k) {
+        if (sinfo[w][k].pair < 0) continue;
+        slot_order[ns] = w * 2 + k;
+        if (sinfo[w][k].pair != prev) {
+          run_first[nr] = ns;
+          run_count[nr] = 0;
+          ++nr;
+          prev = sinfo[w][k].pair;
+        }
+        ++run_count[nr - 1];
+        ++ns;
+      }
+    s_nruns = nr;
+  }
+  __syncthreads();
+  const int nruns = s_nruns;
+  for (int rk = 0; rk < nruns; ++rk) {
+    const int f = run_first[rk], cnt = run_count[rk];
+    const SlotInfo& a = sinfo[slot_order[f] >> 1][slot_order[f] & 1];
+    const SlotInfo& z = sinfo[slot_order[f + cnt - 1] >> 1][slot_order[f + cnt - 1] & 1];
+    const int pair = a.pair;
+    const bool complete = a.first_page == 0 && z.last_page == a.np - 1;
+    const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
+    float* rec = p.part + ((long long)blockIdx.x + pair) * kRecFloats;
+    for (int e = tid; e < p.group * kHeadDim; e += kNW * 32) {
+      const int head = e >> 7, d = e & (kHeadDim - 1);
+      float M = -INFINITY;
+      for (int k = 0; k < cnt; ++k) {
+        const int so = slot_order[f + k];
+        const float* sl = (so & 1) ? reinterpret_cast<float*>(ring + (so >> 1) * kStages * kStageBytes)
+                                   : slot0 + (so >> 1) * kRecFloats;
+        M = fmaxf(M, sl[kOffM + head]);
+      }
+      float Ls = 0.0f, Os = 0.0f;
+      for (int k = 0; k < cnt; ++k) {
+        const int so = slot_order[f + k];
+        const float* sl = (so & 1) ? reinterpret_cast<float*>(ring + (so >> 1) * kStages * kStageBytes)
+                                   : slot0 + (so >> 1) * kRecFloats;
+        const float w = sl[kOffM + head] == -INFINITY ? 0.0f : ex2(sl[kOffM + head] - M);
+        Ls += sl[kOffL + head] * w;
+        Os += sl[head * kHeadDim + d] * w;
+      }
+      if (complete) {
+        p.out[((long long)b * p.hq + (long long)h * p.group + head) * kHeadDim + d] =
+            Ls > 0.0f ? Os * (p.v_gscale / Ls) : 0.0f;
+      } else {
+        rec[head * kHeadDim + d] = Os;
+        if (d == 0) {
+          rec[kOffM + head] = M;
+          rec[kOffL + head] = Ls;
+        }
+      }
+    }
+    if (!complete) {
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const long long pair_start = a.r_first - a.first_page;
+        const long long cf = cta_of(pair_start, W, N), cl = cta_of(pair_start + a.np - 1, W, N);
+        const int old = atomicAdd(p.counters + pair, 1);
+        s_last = (old == (int)(cl - cf)) ? 1 : 0;
+        s_cfirst = cf;
+        s_clast = cl;
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        const long long cf = s_cfirst, cl = s_clast;
+        for (int e = tid; e < p.group * kHeadDim; e += kNW * 32) {
+          const int head = e >> 7, d = e & (kHeadDim - 1);
+          float M = -INFINITY;
+          for (long long c = cf; c <= cl; ++c) {
+            const float* r = p.part + (c + pair) * kRecFloats;
+            M = fmaxf(M, __ldcg(r + kOffM + head));
+          }
+          float Ls = 0.0f, Os = 0.0f;
+          for (long long c = cf; c <= cl; ++c) {
+            const float* r = p.part + (c + pair) * kRecFloats;
+            const float mc = __ldcg(r + kOffM + head);
+            const float w = mc == -INFINITY ? 0.0f : ex2(mc - M);
+            Ls += __ldcg(r + kOffL + head) * w;
+            Os += __ldcg(r + head * kHeadDim + d) * w;
+          }
+          p.out[((long long)b * p.hq + (long long)h * p.group + head) * kHeadDim + d] =
+              Ls > 0.0f ? Os * (p.v_gscale / Ls) : 0.0f;
+        }
+        if (tid == 0) p.counters[pair] = 0;  // ready for the next call
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+int decode_num_ctas(int num_sms) { return num_sms * kCtasPerSm; }
+
+size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads) {
+  const size_t pairs = (size_t)batch * (size_t)num_kv_heads;
+  size_t rec = ((size_t)num_ctas + pairs) * kRecFloats * sizeof(float);
+  rec = (rec + 255) / 256 * 256;
+  return rec + pairs * sizeof(int32_t);
+}
+
+cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
+                          int32_t max_pages, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                          float softmax_scale, void* workspace, int32_t* device_status, int num_sms,
+                          cudaStream_t stream) {
+  static bool attr_set = false;  // the attribute is per function, for every device
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int num_ctas = decode_num_ctas(num_sms);
+  DecodeParams p;
+  p.k_data = c.k_data;
+  p.v_data = c.v_data;
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  p.num_pages = (int32_t)c.num_pages;
+  p.hkv = c.num_kv_heads;
+  p.q = q;
+  p.out = out;
+  p.page_table = page_table;
+  p.max_pages = max_pages;
+  p.seq_lens = seq_lens;
+  p.batch = batch;
+  p.hq = num_q_heads;
+  p.group = num_q_heads / c.num_kv_heads;
+  p.score_scale = softmax_scale * 1.4426950408889634f * c.k_global_scale;
+  p.v_gscale = c.v_global_scale;
+  const size_t pairs = (size_t)batch * (size_t)c.num_kv_heads;
+  size_t rec = ((size_t)num_ctas + pairs) * kRecFloats * sizeof(float);
+  rec = (rec + 255) / 256 * 256;
+  p.part = static_cast<float*>(workspace);
+  p.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + rec);
+  p.status = device_status;
+  decode_kernel<<<num_ctas, kNW * 32, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4kv

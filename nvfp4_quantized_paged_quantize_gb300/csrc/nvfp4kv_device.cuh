@@ -1,0 +1,162 @@
+// nvfp4kv_device.cuh -- device-side building blocks of the NVFP4 paged KV cache
+// (sm_103a): format conversions through the hardware cvt instructions, TMA bulk
+// copies with mbarrier completion, and bounded waits.
+//
+// Format ("nvfp4-kv-cache-memory-wall", section 2; "NVFP4: breaking the memory
+// wall", technical breakdown): E2M1 data (+-{0,0.5,1,1.5,2,3,4,6}), one E4M3
+// scale per 16 consecutive values, one FP32 global scale per tensor.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "nvfp4kv.h"
+
+namespace nvfp4kv {
+
+constexpr int kHeadDim = 128;                          // supported head_dim
+constexpr int kPage = 16;                              // tokens per page
+constexpr int kBlock = 16;                             // values per E4M3 block scale
+constexpr int kRowBytes = kHeadDim / 2;                // 64: packed E2M1 of one (token, head)
+constexpr int kRowScales = kHeadDim / kBlock;          // 8: E4M3 scales of one (token, head)
+constexpr int kPageDataBytes = kPage * kRowBytes;      // 1024: one head's page of data
+constexpr int kPageScaleBytes = kPage * kRowScales;    // 128: one head's page of scales
+constexpr int kDevErrTimeout = 8;                      // a bounded wait gave up
+
+// ---------------------------------------------------------------------------
+// E2M1 / E4M3 conversions (round to nearest even, saturating, as the
+// satfinite cvt forms do).
+// ---------------------------------------------------------------------------
+
+// Two fp32 -> one byte of two E2M1 codes; `lo` goes to the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One non-negative fp32 -> E4M3 byte.
+__device__ __forceinline__ uint32_t e4m3_from_f32(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2.  Exact: every E4M3 value is
+// an f16 normal number.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  asm("{ .reg .b16 h; cvt.u16.u32 h, %1; cvt.rn.f16x2.e4m3x2 %0, h; }" : "=r"(r) : "r"(two_bytes));
+  return r;
+}
+
+// One E4M3 byte -> fp32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  uint32_t h2 = e4m3x2_to_f16x2(byte & 0xFFu);
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// Byte K of w (two E2M1 codes, element 2i in the low nibble) -> f16x2 with the
+// low nibble in the low half.  Exact: every E2M1 value is an f16 number.
+template <int K>
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
+  uint32_t r;
+  if constexpr (K == 0)
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, a; }" : "=r"(r) : "r"(w));
+  else if constexpr (K == 1)
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(r) : "r"(w));
+  else if constexpr (K == 2)
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, c; }" : "=r"(r) : "r"(w));
+  else
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, d; }" : "=r"(r) : "r"(w));
+  return r;
+}
+
+// f16x2 (low half first) -> two E4M3 bytes (low half -> low byte).
+__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+
+// Two fp32 -> two E4M3 bytes; `lo` goes to the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// ---------------------------------------------------------------------------
+// shared memory, mbarrier and TMA bulk copy (global -> shared, 1-D)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until the mbarrier phase with the given parity has completed.  Gives up
+// after about `limit_ns` of wall time and returns false (the caller records a
+// device error and stops using the stage).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 1000000000ull) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  if (done) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    if (done) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void flag_error(int32_t* status, int bit) {
+  if (status != nullptr) atomicOr(status, bit);
+}
+
+}  // namespace nvfp4kv

@@ -69,6 +69,9 @@ def lib():
         L.nvfp4_oracle_decode_attention.argtypes = [ctypes.POINTER(_CCache), vp, vp, i32, vp,
                                                     i32, i32, f64, vp]
         L.nvfp4_oracle_decode_attention.restype = ctypes.c_int
+        L.nvfp4_oracle_decode_attention_heads.argtypes = [ctypes.POINTER(_CCache), vp, vp, i32, vp,
+                                                          i32, i32, f64, i32, i32, vp]
+        L.nvfp4_oracle_decode_attention_heads.restype = ctypes.c_int
         L.nvfp4_oracle_dequant_to_fp8_workspace.argtypes = [ctypes.POINTER(_CCache), vp, i32, vp,
                                                             vp, i32, f32, f32, vp, vp]
         L.nvfp4_oracle_dequant_to_fp8_workspace.restype = ctypes.c_int
@@ -172,8 +175,10 @@ def quantize_append(cache: Cache, k_bf16, v_bf16, slot_mapping) -> int:
     return lib().nvfp4_oracle_quantize_append(ctypes.byref(c), _ptr(k), _ptr(v), _ptr(s), n)
 
 
-def decode_attention(cache: Cache, q_bf16, page_table, seq_lens, softmax_scale):
-    """fp64 decode attention; returns (out[B, Hq, d] float64, status)."""
+def decode_attention(cache: Cache, q_bf16, page_table, seq_lens, softmax_scale, heads=None):
+    """fp64 decode attention; returns (out[B, Hq, d] float64, status).
+
+    heads=(begin, end) computes only those query heads (other rows stay 0)."""
     q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
     pt = np.ascontiguousarray(page_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -181,8 +186,10 @@ def decode_attention(cache: Cache, q_bf16, page_table, seq_lens, softmax_scale):
     assert d == cache.head_dim and pt.shape[0] == B and sl.shape == (B,)
     out = np.zeros((B, Hq, d), np.float64)
     c = cache._c()
-    st = lib().nvfp4_oracle_decode_attention(ctypes.byref(c), _ptr(q), _ptr(pt), pt.shape[1],
-                                             _ptr(sl), B, Hq, float(softmax_scale), _ptr(out))
+    hb, he = (0, Hq) if heads is None else heads
+    st = lib().nvfp4_oracle_decode_attention_heads(ctypes.byref(c), _ptr(q), _ptr(pt), pt.shape[1],
+                                                   _ptr(sl), B, Hq, float(softmax_scale), hb, he,
+                                                   _ptr(out))
     return out, st
 
 

@@ -75,18 +75,31 @@ double nvfp4_oracle_e4m3_value(uint8_t code) {
   return s ? -mag : mag;
 }
 
+/* Non-negative values of each format by code, filled once from the decoders
+ * above so that the searches below are table lookups. */
+static double e2m1_mag[8];
+static double e4m3_mag[0x7F];
+static int tables_ready = 0;
+
+static void init_tables(void) {
+  if (tables_ready) return;
+  for (int c = 0; c < 8; ++c) e2m1_mag[c] = nvfp4_oracle_e2m1_value((uint8_t)c);
+  for (int c = 0; c < 0x7F; ++c) e4m3_mag[c] = nvfp4_oracle_e4m3_value((uint8_t)c);
+  tables_ready = 1;
+}
+
 /* Nearest-value search over the non-negative codes 0..max_code of a format
- * whose values increase with the code.  Ties pick the even code (the one whose
- * mantissa LSB, which is the code LSB, is zero).  Saturating: anything beyond
- * the largest finite value maps to it. */
-static uint8_t nearest_code(double mag, int max_code, double (*value)(uint8_t)) {
+ * whose values increase with the code (value[c] for code c).  Ties pick the
+ * even code (the one whose mantissa LSB, which is the code LSB, is zero).
+ * Saturating: anything at or beyond the largest finite value maps to it. */
+static uint8_t nearest_code(double mag, int max_code, const double* value) {
   /* at or beyond the largest finite value: saturate (distances to the
    * candidates would also lose their differences for huge inputs) */
-  if (mag >= value((uint8_t)max_code)) return (uint8_t)max_code;
+  if (mag >= value[max_code]) return (uint8_t)max_code;
   int best = 0;
-  double best_d = fabs(mag - value(0));
+  double best_d = fabs(mag - value[0]);
   for (int c = 1; c <= max_code; ++c) {
-    double d = fabs(mag - value((uint8_t)c));
+    double d = fabs(mag - value[c]);
     if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
       best = c;
       best_d = d;
@@ -96,12 +109,14 @@ static uint8_t nearest_code(double mag, int max_code, double (*value)(uint8_t)) 
 }
 
 uint8_t nvfp4_oracle_e2m1_encode(float y) {
-  uint8_t mag = nearest_code(fabs((double)y), 7, nvfp4_oracle_e2m1_value);
+  init_tables();
+  uint8_t mag = nearest_code(fabs((double)y), 7, e2m1_mag);
   return (uint8_t)(mag | (signbit(y) ? 0x8 : 0x0));
 }
 
 uint8_t nvfp4_oracle_e4m3_encode(float z) {
-  uint8_t mag = nearest_code(fabs((double)z), 0x7E, nvfp4_oracle_e4m3_value);
+  init_tables();
+  uint8_t mag = nearest_code(fabs((double)z), 0x7E, e4m3_mag);
   return (uint8_t)(mag | (signbit(z) ? 0x80 : 0x00));
 }
 
@@ -219,36 +234,56 @@ int nvfp4_oracle_quantize_append(const nvfp4_oracle_cache* c, const uint16_t* k_
   return bad;
 }
 
-/* Dequantised element d of the cached row for (page, kv head, row-in-page). */
-static double cached_value(const nvfp4_oracle_cache* c, int which, int64_t page, int h, int off,
-                           int dd) {
+/* Value tables built once per call from the format definitions above (the
+ * same numbers nvfp4_oracle_e2m1_value / nvfp4_oracle_e4m3_value return). */
+typedef struct {
+  double e2m1[16];
+  double e4m3[256];
+} value_tables;
+
+static void build_tables(value_tables* vt) {
+  for (int c = 0; c < 16; ++c) vt->e2m1[c] = nvfp4_oracle_e2m1_value((uint8_t)c);
+  for (int c = 0; c < 256; ++c) vt->e4m3[c] = nvfp4_oracle_e4m3_value((uint8_t)c);
+}
+
+/* Dequantised row (all head_dim elements) of the cached (page, kv head, row). */
+static void cached_row(const nvfp4_oracle_cache* c, const value_tables* vt, int which, int64_t page,
+                       int h, int off, double* dst) {
   const int d = c->head_dim;
   int64_t r = row_index(page, h, off, c->num_kv_heads, c->page_size);
   const uint8_t* data = (which == 0 ? c->k_data : c->v_data) + r * nvfp4_oracle_row_bytes(d);
   const uint8_t* scl = (which == 0 ? c->k_scale : c->v_scale) + r * nvfp4_oracle_row_scale_bytes(d);
-  uint8_t byte = data[dd / 2];
-  uint8_t code = (dd & 1) ? (byte >> 4) : (byte & 0xF);
-  float g = which == 0 ? c->k_global_scale : c->v_global_scale;
-  return nvfp4_oracle_dequant_value(code, scl[dd / NVFP4_ORACLE_BLOCK], g);
+  double g = (double)(which == 0 ? c->k_global_scale : c->v_global_scale);
+  for (int dd = 0; dd < d; ++dd) {
+    uint8_t byte = data[dd / 2];
+    uint8_t code = (dd & 1) ? (byte >> 4) : (byte & 0xF);
+    dst[dd] = vt->e2m1[code] * vt->e4m3[scl[dd / NVFP4_ORACLE_BLOCK]] * g;
+  }
 }
 
 /* ------------------------------------------------------------------------- */
 /* Decode attention: one query token per sequence, softmax over all cached   */
-/* tokens of that sequence, GQA (query head h reads KV head h / G).          */
+/* tokens of that sequence, GQA (query head h reads KV head h / G).  Query   */
+/* heads [head_begin, head_end) are computed; other rows of out are left as  */
+/* they are.                                                                 */
 /* ------------------------------------------------------------------------- */
 
-int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q_bf16,
-                                  const int32_t* page_table, int32_t max_pages,
-                                  const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
-                                  double softmax_scale, double* out) {
+int nvfp4_oracle_decode_attention_heads(const nvfp4_oracle_cache* c, const uint16_t* q_bf16,
+                                        const int32_t* page_table, int32_t max_pages,
+                                        const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                        double softmax_scale, int32_t head_begin, int32_t head_end,
+                                        double* out) {
   const int d = c->head_dim, H = c->num_kv_heads, P = c->page_size;
-  const int G = num_q_heads / H;
   int bad = 0;
   if (d > 512 || d % NVFP4_ORACLE_BLOCK != 0 || H <= 0 || num_q_heads % H != 0) return -1;
+  const int G = num_q_heads / H;
+  value_tables vt;
+  build_tables(&vt);
+  double row[512];
   for (int32_t b = 0; b < batch; ++b) {
     int64_t L = seq_lens[b];
     if (L < 0 || L > (int64_t)max_pages * P) { bad = 1; L = L < 0 ? 0 : (int64_t)max_pages * P; }
-    for (int hq = 0; hq < num_q_heads; ++hq) {
+    for (int hq = head_begin; hq < head_end; ++hq) {
       double* o = out + ((int64_t)b * num_q_heads + hq) * d;
       for (int dd = 0; dd < d; ++dd) o[dd] = 0.0;
       if (L == 0) continue;
@@ -263,8 +298,9 @@ int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q
         int32_t page = page_table[(int64_t)b * max_pages + t / P];
         valid[t] = page >= 0 && page < c->num_pages;
         if (!valid[t]) { bad = 1; continue; }
+        cached_row(c, &vt, 0, page, hk, (int)(t % P), row);
         double acc = 0.0;
-        for (int dd = 0; dd < d; ++dd) acc += q[dd] * cached_value(c, 0, page, hk, (int)(t % P), dd);
+        for (int dd = 0; dd < d; ++dd) acc += q[dd] * row[dd];
         s[t] = softmax_scale * acc;
         if (s[t] > m) m = s[t];
       }
@@ -274,7 +310,8 @@ int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q
         double w = exp(s[t] - m);
         l += w;
         int32_t page = page_table[(int64_t)b * max_pages + t / P];
-        for (int dd = 0; dd < d; ++dd) o[dd] += w * cached_value(c, 1, page, hk, (int)(t % P), dd);
+        cached_row(c, &vt, 1, page, hk, (int)(t % P), row);
+        for (int dd = 0; dd < d; ++dd) o[dd] += w * row[dd];
       }
       if (l > 0.0)
         for (int dd = 0; dd < d; ++dd) o[dd] /= l;
@@ -283,6 +320,14 @@ int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q
     }
   }
   return bad;
+}
+
+int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q_bf16,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                  double softmax_scale, double* out) {
+  return nvfp4_oracle_decode_attention_heads(c, q_bf16, page_table, max_pages, seq_lens, batch,
+                                             num_q_heads, softmax_scale, 0, num_q_heads, out);
 }
 
 /* ------------------------------------------------------------------------- */

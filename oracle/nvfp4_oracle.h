@@ -52,6 +52,11 @@ int nvfp4_oracle_decode_attention(const nvfp4_oracle_cache* c, const uint16_t* q
                                   const int32_t* page_table, int32_t max_pages,
                                   const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                                   double softmax_scale, double* out);
+int nvfp4_oracle_decode_attention_heads(const nvfp4_oracle_cache* c, const uint16_t* q_bf16,
+                                        const int32_t* page_table, int32_t max_pages,
+                                        const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                        double softmax_scale, int32_t head_begin, int32_t head_end,
+                                        double* out);
 int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int32_t* page_table,
                                           int32_t max_pages, const int32_t* prefix_lens,
                                           const int64_t* cu_prefix, int32_t batch,

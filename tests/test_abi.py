@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads and exports every symbol the header declares.
+
+No compute call is made here (these run without a GPU): only size queries and
+the host-side argument checks that return before anything touches CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_quantized_paged_quantize_gb300 as kv
+from nvfp4_quantized_paged_quantize_gb300 import build as kvbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "nvfp4kv.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4kv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+    return kv.load()
+
+
+def test_library_builds_in_tree():
+    path = kvbuild.build()
+    assert os.path.exists(path)
+    assert os.path.dirname(path).startswith(os.path.dirname(kv.__file__))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert set(names) >= {"nvfp4kv_quantize_append", "nvfp4kv_decode_attention",
+                          "nvfp4kv_dequant_to_fp8_workspace", "nvfp4kv_decode_workspace_size",
+                          "nvfp4kv_cache_bytes", "nvfp4kv_status_string"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, 12345):
+        assert kv.nvfp4kv_status_string(code)
+    assert kv.nvfp4kv_status_string(-4).startswith("workspace")
+
+
+def test_cache_bytes_nine_sixteenths(lib):
+    d, s = kv.nvfp4kv_cache_bytes(10, 8)
+    values = 10 * 8 * 16 * 128
+    assert d == values // 2 and s == values // 16
+    assert (d + s) / values == 9 / 16
+    with pytest.raises(kv.Nvfp4kvError):
+        kv.nvfp4kv_cache_bytes(0, 8)
+
+
+def _fake_cache(**kw):
+    # aligned fake addresses: these calls are rejected before any device access
+    c = kv.Cache(0x10000, 0x20000, 0x30000, 0x40000, 4, 2)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _raw(lib, fn, *args):
+    return getattr(lib, fn)(*args)
+
+
+def test_host_validation_codes(lib):
+    c = _fake_cache()
+    cs = c.c_struct()
+    P = ctypes.byref
+    # null cache
+    assert lib.nvfp4kv_quantize_append(None, 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    # unsupported head_dim / page size
+    bad = _fake_cache(head_dim=64).c_struct()
+    assert lib.nvfp4kv_quantize_append(P(bad), 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_UNSUPPORTED
+    bad = _fake_cache(page_size=32).c_struct()
+    assert lib.nvfp4kv_decode_attention(P(bad), 16, 16, 4, 1, 4, 1, 2, 0.1, 256, 1 << 20, None,
+                                        None) == kv.NVFP4KV_ERR_UNSUPPORTED
+    # misaligned pool, bad global scale
+    bad = _fake_cache(k_data=0x10001).c_struct()
+    assert lib.nvfp4kv_quantize_append(P(bad), 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    bad = _fake_cache(k_global_scale=float("nan")).c_struct()
+    assert lib.nvfp4kv_quantize_append(P(bad), 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    bad = _fake_cache(v_global_scale=0.0).c_struct()
+    assert lib.nvfp4kv_quantize_append(P(bad), 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    # zero tokens is a no-op; negative is an error
+    assert lib.nvfp4kv_quantize_append(P(cs), None, None, None, 0, None, None) == kv.NVFP4KV_OK
+    assert lib.nvfp4kv_quantize_append(P(cs), 16, 16, 8, -1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    # misaligned k
+    assert lib.nvfp4kv_quantize_append(P(cs), 18, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    # decode: group not dividing, group > 8, bad softmax scale, empty batch
+    assert lib.nvfp4kv_decode_attention(P(cs), 16, 16, 4, 1, 4, 1, 3, 0.1, 256, 1 << 20, None,
+                                        None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4kv_decode_attention(P(cs), 16, 16, 4, 1, 4, 1, 18, 0.1, 256, 1 << 20, None,
+                                        None) == kv.NVFP4KV_ERR_UNSUPPORTED
+    assert lib.nvfp4kv_decode_attention(P(cs), 16, 16, 4, 1, 4, 1, 8, -1.0, 256, 1 << 20, None,
+                                        None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4kv_decode_attention(P(cs), 16, 16, 4, 1, 4, 0, 8, 0.1, 256, 1 << 20, None,
+                                        None) == kv.NVFP4KV_OK
+    # dequant: bad workspace scale, misaligned workspace, nothing to do
+    assert lib.nvfp4kv_dequant_to_fp8_workspace(P(cs), 4, 1, 4, 8, 1, 16, 0.0, 1.0, 16, 16, None,
+                                                None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4kv_dequant_to_fp8_workspace(P(cs), 4, 1, 4, 8, 1, 16, 1.0, 1.0, 17, 16, None,
+                                                None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4kv_dequant_to_fp8_workspace(P(cs), 4, 1, 4, 8, 1, 0, 1.0, 1.0, 16, 16, None,
+                                                None) == kv.NVFP4KV_OK

@@ -1,0 +1,146 @@
+"""GPU paged decode attention (fused NVFP4 dequant) vs the oracle's fp64 attention.
+
+Decode dequantises inside the attention kernel ("nvfp4-kv-cache-memory-wall",
+section 3, item 3).  Bar: per (sequence, query head) row,
+max_d |out - ref| <= 2e-3 * ||ref||_2 (gpu_util.ATTN_TOL).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import nvfp4_quantized_paged_quantize_gb300 as kv
+from nvfp4_quantized_paged_quantize_gb300 import inputs
+from gpu_util import (ATTN_TOL, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle,
+                      oracle_pair, pool_host, status_word)
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_compare(wl):
+    prompts = wl.all_prompt_kv()
+    new = wl.new_kv() if wl.append else None
+    q = wl.q()
+    g = fill_workload_gpu(wl, prompts, new)
+    st = status_word()
+    out, ws = decode_gpu(wl, g, q, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o = fill_workload_oracle(wl, prompts, new)
+    ref, rs = oracle.decode_attention(o, q, wl.page_table, wl.seq_lens, wl.softmax_scale)
+    assert rs == 0
+    worst = check_rows(out.cpu().numpy(), ref)
+    # the workspace counters are back to zero: a second call gives the same bits
+    out2, _ = decode_gpu(wl, g, q, workspace=ws)
+    assert torch.equal(out, out2)
+    assert not ws[-wl.batch * wl.num_kv_heads * 4:].any()
+    return worst
+
+
+def test_tiny_workload(cuda_lib):
+    _full_compare(inputs.decode_config(1))
+
+
+@pytest.mark.parametrize("index,scale", [(2, 1 / 32), (3, 1 / 256), (4, 1 / 32)])
+def test_scaled_workloads(cuda_lib, index, scale):
+    _full_compare(inputs.decode_config(index, scale))
+
+
+def _custom(lens, hq, hkv, seed=0, dist=None, pool_factor=1.0, append=False):
+    dist = dist or inputs.KVDist("normal", 1.0)
+    return inputs.DecodeWorkload("custom", seed, np.array(lens, np.int64), append, hq, hkv, dist,
+                                 pool_factor=pool_factor)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (4, 2), (16, 4), (64, 8), (24, 8)])
+def test_group_sizes(cuda_lib, hq, hkv):
+    _full_compare(_custom([1, 15, 16, 17, 33, 200], hq, hkv, seed=hq))
+
+
+def test_ragged_tails_empty_and_many_tiny_sequences(cuda_lib):
+    rng = np.random.default_rng(9)
+    lens = list(rng.integers(0, 40, 300)) + [0, 1, 2, 16, 4096]
+    _full_compare(_custom(lens, 32, 8, seed=5, pool_factor=1.3))
+
+
+def test_long_single_sequence_across_many_ctas(cuda_lib):
+    _full_compare(_custom([65536 + 7], 8, 1, seed=11, append=True,
+                          dist=inputs.KVDist("normal", 0.02, outlier=6.0, per_chunk=8)))
+
+
+def test_large_scores_and_calibrated_scales(cuda_lib):
+    wl = _custom([300, 1000], 16, 2, seed=12, dist=inputs.KVDist("channel", lo=0.1, hi=10.0))
+    wl.q_sigma = 30.0           # sharp softmax: exercises the running-max rescale
+    wl.calibrated = True
+    _full_compare(wl)
+
+
+def test_bad_page_ids_and_lengths_are_flagged_and_skipped(cuda_lib):
+    wl = _custom([40, 70], 8, 2, seed=13)
+    prompts = wl.all_prompt_kv()
+    q = wl.q()
+    g = fill_workload_gpu(wl, prompts)
+    o = fill_workload_oracle(wl, prompts)
+    pt = wl.page_table.copy()
+    pt[1, 2] = wl.num_pages + 100          # sequence 1, tokens 32..47 -> skipped
+    st = status_word()
+    B, Hq = wl.batch, wl.num_q_heads
+    ws = torch.zeros(kv.nvfp4kv_decode_workspace_size(g, B, Hq), dtype=torch.uint8, device="cuda")
+    out = torch.zeros((B, Hq, 128), dtype=torch.float32, device="cuda")
+    from gpu_util import bf16_dev
+    kv.nvfp4kv_decode_attention(g, bf16_dev(q), out, dev(pt), dev(wl.seq_lens), wl.softmax_scale, ws,
+                                device_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kv.NVFP4KV_DEVERR_PAGE
+    ref, rs = oracle.decode_attention(o, q, pt, wl.seq_lens, wl.softmax_scale)
+    assert rs == 1
+    check_rows(out.cpu().numpy(), ref)
+    # a length past the page table is clamped and flagged
+    lens = wl.seq_lens.copy()
+    lens[0] = wl.max_pages * 16 + 5
+    st.zero_()
+    kv.nvfp4kv_decode_attention(g, bf16_dev(q), out, dev(wl.page_table), dev(lens), wl.softmax_scale, ws,
+                                device_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kv.NVFP4KV_DEVERR_LENGTH
+
+
+def _full_size_sampled(index, samples):
+    """Full-size workload through the launch configuration the benchmark times;
+    oracle on sampled (sequence, KV head) pairs, filled from the same inputs."""
+    wl = inputs.decode_config(index)
+    prompts = wl.all_prompt_kv(threads=16)
+    new = wl.new_kv() if wl.append else None
+    q = wl.q()
+    gk, gv = wl.global_scales(prompts, new)
+    g = fill_workload_gpu(wl, prompts, new)
+    out, _ = decode_gpu(wl, g, q)
+    out = out.cpu().numpy()
+    kd, vd, ks, vs = pool_host(g)
+    G = wl.num_q_heads // wl.num_kv_heads
+    worst = 0.0
+    for b, h in samples:
+        k_seq, v_seq = prompts[b]
+        if wl.append:
+            k_seq = np.concatenate([k_seq, new[0][b:b + 1]])
+            v_seq = np.concatenate([v_seq, new[1][b:b + 1]])
+        ref, oc, npg = oracle_pair(wl, b, h, k_seq, v_seq, q, gk, gv)
+        worst = max(worst, check_rows(out[b, h * G:(h + 1) * G], ref))
+        # the pool rows of this pair are bit-exact too
+        pages = wl.page_table[b, :npg].astype(np.int64)
+        rows = ((pages[:, None] * wl.num_kv_heads + h) * 16 + np.arange(16)[None, :]).reshape(-1)
+        L = k_seq.shape[0]
+        rows = rows[:L]
+        np.testing.assert_array_equal(kd[rows], oc.k_data[:L])
+        np.testing.assert_array_equal(vd[rows], oc.v_data[:L])
+        np.testing.assert_array_equal(ks[rows], oc.k_scale[:L])
+        np.testing.assert_array_equal(vs[rows], oc.v_scale[:L])
+    return worst
+
+
+def test_full_size_decode_b32_ctx8k(cuda_lib):
+    _full_size_sampled(2, [(0, 0), (13, 5), (31, 7)])
+
+
+def test_full_size_decode_b4_ctx128k(cuda_lib):
+    _full_size_sampled(3, [(2, 3)])

@@ -1,0 +1,141 @@
+"""GPU quantize-append vs the oracle: packed nibbles and scale bytes bit-exact.
+
+Two-level scaling ("nvfp4-kv-cache-memory-wall", section 2) applied on the way
+into the paged cache (same page, section 3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import nvfp4_quantized_paged_quantize_gb300 as kv
+from nvfp4_quantized_paged_quantize_gb300 import inputs
+from gpu_util import (bf16_dev, dev, fill_workload_gpu, fill_workload_oracle, gpu_append, gpu_cache,
+                      pool_host, status_word)
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert_pool_equal(gpu_cache_, orc):
+    kd, vd, ks, vs = pool_host(gpu_cache_)
+    np.testing.assert_array_equal(ks, orc.k_scale)
+    np.testing.assert_array_equal(vs, orc.v_scale)
+    np.testing.assert_array_equal(kd, orc.k_data)
+    np.testing.assert_array_equal(vd, orc.v_data)
+
+
+def test_tiny_workload_pool_bit_exact(cuda_lib):
+    wl = inputs.decode_config(1)
+    prompts = wl.all_prompt_kv()
+    new = wl.new_kv()
+    st = status_word()
+    g = fill_workload_gpu(wl, prompts, new, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _assert_pool_equal(g, fill_workload_oracle(wl, prompts, new))
+
+
+@pytest.mark.parametrize("index", [2, 3, 4])
+def test_scaled_workloads_pool_bit_exact(cuda_lib, index):
+    wl = inputs.decode_config(index, scale=1 / 64)
+    prompts = wl.all_prompt_kv()
+    new = wl.new_kv() if wl.append else None
+    g = fill_workload_gpu(wl, prompts, new)
+    _assert_pool_equal(g, fill_workload_oracle(wl, prompts, new))
+
+
+def _edge_blocks():
+    """Blocks that walk every E4M3 scale rounding boundary and every E2M1 midpoint."""
+    rng = np.random.default_rng(7)
+    blocks = []
+    e4 = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+    mids = (e4[:-1] + e4[1:]) / 2
+    for m in mids:  # amax / 6 lands on, just below and just above each scale midpoint
+        for f in (1.0, 1.0 - 2 ** -7, 1.0 + 2 ** -7):
+            x = rng.normal(0, 1, 16) * m
+            x[3] = 6 * m * f
+            blocks.append(x)
+    for s in e4[1:]:  # E2M1 midpoints at an exact scale (amax = 6 * scale)
+        x = np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5, 0.1])
+        blocks.append(x * s)
+    blocks.append(np.zeros(16))
+    blocks.append(-np.zeros(16))
+    blocks.append(np.full(16, 1e-6))                         # scale rounds to 0 -> signed zeros
+    blocks.append(np.array([3e38] + [1.0] * 15))            # saturated scale
+    blocks.append(rng.normal(0, 1e-30, 16))                 # bf16 subnormal range
+    return np.stack(blocks).astype(np.float32)
+
+
+@pytest.mark.parametrize("gk,gv", [(1.0, 1.0), (0.37, 5.5), (1.0 / 2688, 3e-3), (1e3, 1e-5)])
+def test_edge_blocks_bit_exact(cuda_lib, gk, gv):
+    blocks = _edge_blocks()
+    n = (blocks.shape[0] + 7) // 8
+    flat = np.zeros((n * 8, 16), np.float32)
+    flat[:blocks.shape[0]] = blocks
+    x = flat.reshape(n, 1, 128)
+    kb = inputs.bf16_bits(x)
+    vb = inputs.bf16_bits(-x[::-1].copy())
+    slots = np.random.default_rng(1).permutation(n + 5)[:n].astype(np.int64)
+    pages = (n + 5 + 15) // 16
+    g = gpu_cache(pages, 1, gk, gv)
+    gpu_append(g, kb, vb, slots)
+    o = oracle.Cache(pages, 1, 128, 16, gk, gv)
+    oracle.quantize_append(o, kb, vb, slots)
+    _assert_pool_equal(g, o)
+
+
+def test_every_bf16_value_at_every_scale_bit_exact(cuda_lib):
+    # g = 1: for each non-zero E4M3 scale s, blocks whose amax is exactly 6 s
+    # followed by 15 bf16 values swept over every bf16 magnitude below 6 s
+    allbits = np.arange(0x8000, dtype=np.uint16)                    # non-negative bf16 patterns
+    vals = inputs.bf16_bits_to_f32(allbits)
+    vals = vals[np.isfinite(vals)]
+    rows = []
+    for sb in range(1, 0x7F):
+        s = oracle.e4m3_value(sb)
+        v = vals[vals <= 6 * s]
+        v = np.concatenate([v, -v])
+        pad = (-v.size) % 15
+        v = np.concatenate([v, np.zeros(pad, np.float32)]).reshape(-1, 15)
+        blk = np.concatenate([np.full((v.shape[0], 1), 6 * s, np.float32), v], axis=1)
+        rows.append(blk)
+    blocks = np.concatenate(rows).astype(np.float32)
+    n = (blocks.shape[0] + 7) // 8
+    flat = np.zeros((n * 8, 16), np.float32)
+    flat[:blocks.shape[0]] = blocks
+    x = inputs.bf16_bits(flat.reshape(n, 1, 128))
+    slots = np.arange(n, dtype=np.int64)
+    pages = (n + 15) // 16
+    g = gpu_cache(pages, 1)
+    gpu_append(g, x, x, slots)
+    o = oracle.Cache(pages, 1)
+    oracle.quantize_append(o, x, x, slots)
+    _assert_pool_equal(g, o)
+
+
+def test_padding_and_out_of_range_slots(cuda_lib):
+    rng = np.random.default_rng(3)
+    x = inputs.bf16_bits(rng.normal(0, 1, (6, 2, 128)).astype(np.float32))
+    slots = np.array([5, -1, 40, 63, 64, 1 << 40], np.int64)   # pool holds 64 slots
+    g = gpu_cache(4, 2)
+    st = status_word()
+    gpu_append(g, x, x, slots, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kv.NVFP4KV_DEVERR_SLOT
+    o = oracle.Cache(4, 2)
+    assert oracle.quantize_append(o, x, x, slots) == 1
+    _assert_pool_equal(g, o)
+
+
+def test_extend_chunk_full_size_bit_exact(cuda_lib):
+    # one layer of the extend workload: 16 sequences x 2048 new tokens x 8 KV heads
+    wl = inputs.extend_config()
+    ks, vs = zip(*[wl.chunk_kv(0, b) for b in range(wl.batch)])
+    k = np.concatenate(ks)
+    v = np.concatenate(vs)
+    slots = wl.chunk_slots()
+    g = gpu_cache(wl.num_pages, wl.num_kv_heads)
+    kv.nvfp4kv_quantize_append(g, bf16_dev(k), bf16_dev(v), dev(slots))
+    o = oracle.Cache(wl.num_pages, wl.num_kv_heads)
+    assert oracle.quantize_append(o, k, v, slots) == 0
+    _assert_pool_equal(g, o)
