@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 paged KV cache hot path on GB300.
+
+Headline: NVFP4 paged decode attention KV-tokens/s (and HBM GB/s, % of 8 TB/s)
+on the decode workload at the pages' shape: 32 sequences x 8192 cached tokens
+(+1 appended), 64 query heads / 8 KV heads, head_dim 128, 16-token pages.
+One step = quantize-append of the 32 new tokens + decode attention (with its
+split combine), both through the C ABI.  Secondary lines of the same run: the
+128K-token decode workload and one layer of the extend workload (FP8
+workspace dequant and 2048-token quantize-write).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+`--impl reference` times the CPU oracle on the host cores instead (same
+metric, bounded samples).  With torchrun (N > 1) every rank runs a replica.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_quantized_paged_quantize_gb300 import inputs  # noqa: E402
+
+METRIC = "NVFP4 paged decode attention KV-tokens/s and HBM GB/s (% of 8 TB/s) on 1 GB300"
+UNIT = "KV-tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nvfp4kv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lines = [[p.strip() for p in ln.split(",")] for ln in open(self.path)]
+        lines = [p for p in lines if len(p) >= 9]
+        if len({p[0] for p in lines}) > 1:          # several GPUs visible: keep ours
+            lines = [p for p in lines if p[0] == str(self.gpu)]
+        for parts in lines:
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _dev(torch, a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return (t.view(dtype) if dtype is not None else t).cuda()
+
+
+def _bf16(torch, bits):
+    return _dev(torch, np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16), torch.bfloat16)
+
+
+def _fill_cache(torch, kv, wl, prompts, new):
+    gk, gv = wl.global_scales(prompts, new)
+    cache = kv.Cache.empty(wl.num_pages, wl.num_kv_heads, k_global_scale=gk, v_global_scale=gv, zero=True)
+    for b in range(wl.batch):
+        k, v = prompts[b]
+        kv.nvfp4kv_quantize_append(cache, _bf16(torch, k), _bf16(torch, v),
+                                   _dev(torch, wl.slots(b, 0, k.shape[0])))
+    torch.cuda.synchronize()
+    return cache
+
+
+class DecodeBench:
+    """Device state and one step (append + decode) of a decode workload."""
+
+    def __init__(self, torch, kv, wl):
+        self.torch, self.kv, self.wl = torch, kv, wl
+        prompts = wl.all_prompt_kv(threads=16)
+        self.new = wl.new_kv() if wl.append else None
+        self.q_bits = wl.q()
+        self.cache = _fill_cache(torch, kv, wl, prompts, self.new)
+        del prompts
+        self.q = _bf16(torch, self.q_bits)
+        self.pt = _dev(torch, wl.page_table)
+        self.lens = _dev(torch, wl.seq_lens.astype(np.int32))
+        if wl.append:
+            self.k_new = _bf16(torch, self.new[0])
+            self.v_new = _bf16(torch, self.new[1])
+            self.slots = _dev(torch, wl.append_slots())
+        self.out = torch.empty((wl.batch, wl.num_q_heads, 128), dtype=torch.float32, device="cuda")
+        n = kv.nvfp4kv_decode_workspace_size(self.cache, wl.batch, wl.num_q_heads)
+        self.ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+    def append(self):
+        if self.wl.append:
+            self.kv.nvfp4kv_quantize_append(self.cache, self.k_new, self.v_new, self.slots)
+
+    def decode(self):
+        self.kv.nvfp4kv_decode_attention(self.cache, self.q, self.out, self.pt, self.lens,
+                                         self.wl.softmax_scale, self.ws)
+
+    def launches_per_step(self):
+        return 2 if self.wl.append else 1
+
+
+def time_steps(torch, steps, warmup, body, flush, split=None):
+    """Run `warmup` untimed then `steps` timed iterations of body(); each timed
+    iteration is bracketed by CUDA events on the current stream, with an L2
+    flush (outside the events) before it.  split() may record an inner event
+    pair around the dominant kernel.  Returns per-step ms and inner ms."""
+    for _ in range(warmup):
+        flush()
+        body()
+    torch.cuda.synchronize()
+    E = torch.cuda.Event
+    starts = [E(enable_timing=True) for _ in range(steps)]
+    ends = [E(enable_timing=True) for _ in range(steps)]
+    inner = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)] if split else None
+    torch.cuda.nvtx.range_push("timed")
+    for i in range(steps):
+        flush()
+        starts[i].record()
+        body(inner[i] if inner else None)
+        ends[i].record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ims = [a.elapsed_time(b) for a, b in inner] if inner else None
+    return ms, ims
+
+
+def gpu_arm(args):
+    import torch
+
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    import nvfp4_quantized_paged_quantize_gb300 as kv
+
+    kv.load()
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.zero_()
+
+    wl = inputs.decode_config(2)
+    bench = DecodeBench(torch, kv, wl)
+    kv_tokens = wl.kv_tokens()
+    alg_bytes = wl.algorithmic_bytes()
+
+    def step(ev=None):
+        bench.append()
+        if ev is not None:
+            ev[0].record()
+        bench.decode()
+        if ev is not None:
+            ev[1].record()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        step_ms, dec_ms = time_steps(torch, args.steps, args.warmup, step, flush, split=True)
+    torch.cuda.synchronize()
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * kv_tokens * args.steps / (total_ms / 1e3)
+    dec_avg_ms = float(np.mean(dec_ms))
+    achieved = alg_bytes / (dec_avg_ms / 1e3) / 1e9
+
+    # e2e through the public API with host buffers: per step H2D of the step's
+    # inputs (q, new K/V, slots, page table, lengths) from pinned memory, the
+    # two calls, and D2H of the output into pinned memory
+    host_in = {
+        "q": torch.from_numpy(bench.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "k": torch.from_numpy(bench.new[0].view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "v": torch.from_numpy(bench.new[1].view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "slots": torch.from_numpy(wl.append_slots()).pin_memory(),
+        "pt": torch.from_numpy(wl.page_table).pin_memory(),
+        "lens": torch.from_numpy(wl.seq_lens.astype(np.int32)).pin_memory(),
+    }
+    dev_in = {"q": bench.q, "k": bench.k_new, "v": bench.v_new, "slots": bench.slots, "pt": bench.pt,
+              "lens": bench.lens}
+    host_out = torch.empty(bench.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step(ev=None):
+        for k_, t in host_in.items():
+            dev_in[k_].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(bench.out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ms, _ = time_steps(torch, e2e_steps, args.warmup, e2e_step, flush)
+    e2e_total = float(sum(e2e_ms))
+    if world > 1:
+        t = torch.tensor([e2e_total], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * kv_tokens * e2e_steps / (e2e_total / 1e3)
+    del bench
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 storage; f16 mma operands, f32 accumulate",
+        "data": "synthetic (seeded numpy: K/V N(0,0.02) with 8 of every 4096 values = 6.0, q N(0,1))",
+        "config": {
+            "workload": wl.name, "batch": wl.batch, "ctx": int(wl.seq_lens[0]), "q_heads": wl.num_q_heads,
+            "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16,
+            "step": "quantize-append of 32 new tokens + decode attention (split combine fused)",
+            "l2": "flushed before every timed step (256 MiB memset, outside the step's events)",
+            "parallelism": f"replicas x{world}",
+        },
+        "decode": {
+            "kernel_ms": dec_avg_ms,
+            "kv_tokens_per_s": kv_tokens / (dec_avg_ms / 1e3),
+            "hbm_gbs": achieved,
+            "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
+            "algorithmic_bytes": alg_bytes,
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": None,
+            "kernel": "decode_kernel", "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks.summary(),
+    }
+    if not args.skip_secondary:
+        line["secondary"] = secondary(torch, kv, args, flush, hbm_peak)
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def secondary(torch, kv, args, flush, hbm_peak):
+    out = {}
+    steps = max(3, min(args.steps, 50))
+    # long-context decode: 4 sequences x 131072 tokens, calibrated global scales
+    wl = inputs.decode_config(3)
+    b = DecodeBench(torch, kv, wl)
+    ms, _ = time_steps(torch, steps, args.warmup, lambda ev=None: b.decode(), flush)
+    t = float(np.mean(ms))
+    gbs = wl.algorithmic_bytes() / (t / 1e3) / 1e9
+    out["decode_b4_ctx128k"] = {"kernel_ms": t, "kv_tokens_per_s": wl.kv_tokens() / (t / 1e3), "hbm_gbs": gbs,
+                                "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS, "frac_of_measured_peak": gbs / hbm_peak}
+    del b
+    torch.cuda.empty_cache()
+    # extend: one layer (16 x 16384-token prefix -> FP8 workspace; 16 x 2048 new tokens quantized)
+    ew = inputs.extend_config(num_layers=1)
+    cache = kv.Cache.empty(ew.num_pages, ew.num_kv_heads, zero=True)
+    for s in range(ew.batch):
+        k, v = ew.prefix_kv(0, s)
+        kv.nvfp4kv_quantize_append(cache, _bf16(torch, k), _bf16(torch, v), _dev(torch, ew.slots(s, 0, ew.prefix_len)))
+    ks, vs = zip(*[ew.chunk_kv(0, s) for s in range(ew.batch)])
+    kc, vc = _bf16(torch, np.concatenate(ks)), _bf16(torch, np.concatenate(vs))
+    slots = _dev(torch, ew.chunk_slots())
+    pt, pl, cu = _dev(torch, ew.page_table), _dev(torch, ew.prefix_lens), _dev(torch, ew.cu_prefix)
+    wk = torch.empty((ew.total_rows, ew.num_kv_heads, 128), dtype=torch.uint8, device="cuda")
+    wv = torch.empty_like(wk)
+    ms, _ = time_steps(torch, steps, args.warmup,
+                       lambda ev=None: kv.nvfp4kv_dequant_to_fp8_workspace(cache, pt, pl, cu, wk, wv), flush)
+    t = float(np.mean(ms))
+    gbs = ew.dequant_bytes_per_layer() / (t / 1e3) / 1e9
+    out["extend_dequant_fp8_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak,
+                                           "x80_layers_ms": 80 * t}
+    ms, _ = time_steps(torch, steps, args.warmup,
+                       lambda ev=None: kv.nvfp4kv_quantize_append(cache, kc, vc, slots), flush)
+    t = float(np.mean(ms))
+    gbs = ew.quantize_bytes_per_layer() / (t / 1e3) / 1e9
+    out["extend_quantize_2048x16_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak,
+                                                "x80_layers_ms": 80 * t}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings (the baseline, not the target)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """One (sequence, KV head) pair of a decode workload, prepared for the oracle:
+    its cached prompt quantized by the oracle (setup), then per step the append
+    of the new token and the fp64 decode over the first n tokens."""
+
+    def __init__(self, wl, b, h):
+        import oracle
+
+        self.oracle, self.wl, self.b, self.h = oracle, wl, b, h
+        k, v = wl.prompt_kv(b)
+        new = wl.new_kv() if wl.append else None
+        if wl.append:
+            k = np.concatenate([k, new[0][b:b + 1]])
+            v = np.concatenate([v, new[1][b:b + 1]])
+        self.k = np.ascontiguousarray(k[:, h:h + 1])
+        self.v = np.ascontiguousarray(v[:, h:h + 1])
+        L = self.k.shape[0]
+        self.L = L
+        npg = (L + 15) // 16
+        self.cache = oracle.Cache(npg, 1)
+        oracle.quantize_append(self.cache, self.k[:L - 1], self.v[:L - 1], np.arange(L - 1, dtype=np.int64))
+        G = wl.num_q_heads // wl.num_kv_heads
+        self.q = np.ascontiguousarray(wl.q()[b:b + 1, h * G:(h + 1) * G])
+        self.pt = np.arange(npg, dtype=np.int32)[None]
+
+    def step(self, n):
+        """Append the last token, then decode over the first n tokens; returns KV-tokens done."""
+        self.oracle.quantize_append(self.cache, self.k[-1:], self.v[-1:], np.array([self.L - 1], np.int64))
+        self.oracle.decode_attention(self.cache, self.q, self.pt, np.array([n], np.int32), self.wl.softmax_scale)
+        return n / self.wl.num_kv_heads
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The oracle on a bounded sample: whole (sequence, KV head) pairs, repeated
+    until about budget_s of CPU time; KV-tokens counted per layer over all KV
+    heads (a pair of L tokens is L / Hkv KV-tokens)."""
+    samples = [OracleSample(wl, b, b % wl.num_kv_heads) for b in range(4)]
+    t0 = time.perf_counter()
+    done = 0.0
+    pairs = 0
+    while time.perf_counter() - t0 < budget_s:
+        s = samples[pairs % len(samples)]
+        done += s.step(s.L)
+        pairs += 1
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{pairs} (sequence, KV head) pairs of {wl.name}: append 1 token + fp64 decode over "
+                      f"{samples[0].L} tokens x {wl.num_q_heads // wl.num_kv_heads} query heads; "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def reference_arm(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    wl = inputs.decode_config(2)
+    sample = OracleSample(wl, 0, 0)
+    # size each step so that warmup + steps finish in about args.cpu_total_s
+    t0 = time.perf_counter()
+    sample.step(sample.L)
+    t_full = time.perf_counter() - t0
+    per_step = args.cpu_total_s / max(1, args.steps + args.warmup)
+    n = int(min(sample.L, max(16, sample.L * per_step / max(t_full, 1e-6))))
+    for _ in range(args.warmup):
+        sample.step(n)
+    t0 = time.perf_counter()
+    done = 0.0
+    for _ in range(args.steps):
+        done += sample.step(n)
+    dt = time.perf_counter() - t0
+    value = done / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": wl.name, "batch": wl.batch, "ctx": int(wl.seq_lens[0]), "q_heads": wl.num_q_heads,
+                   "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16,
+                   "step": f"oracle: append 1 token + fp64 decode over {n} tokens of one (sequence, KV head)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"one (sequence, KV head) pair, {n} of {sample.L} tokens per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--skip-secondary", action="store_true", help="only the headline workload")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-total-s", type=float, default=90.0, help="reference arm: total oracle seconds")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

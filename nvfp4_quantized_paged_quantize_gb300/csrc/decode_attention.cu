@@ -15,6 +15,7 @@
 //   1. converts K's E2M1 pairs to f16x2 with cvt.rn.f16x2.e2m1x2, multiplies
 //      by the E4M3 block scale (exact in f16), and computes S^T = Khat q^T for
 //      the 16 tokens x G query heads with mma.sync m16n8k16 (f16 in, f32 acc);
+//      two pages of the same pair are taken per step (32 tokens);
 //   2. runs the online softmax in base 2 (scores scaled by softmax_scale *
 //      log2(e) * g_K); the running max is only raised when a score exceeds it
 //      by more than 8, so the rescale of the accumulators is rare;
@@ -38,9 +39,21 @@
 namespace nvfp4kv {
 namespace {
 
-constexpr int kNW = 4;          // warps per CTA (each streams its own pages)
-constexpr int kStages = 4;      // pages in flight per warp
-constexpr int kCtasPerSm = 4;   // resident CTAs per SM the launch is sized for
+#ifndef NVFP4KV_DECODE_WARPS
+#define NVFP4KV_DECODE_WARPS 4
+#endif
+#ifndef NVFP4KV_DECODE_STAGES
+#define NVFP4KV_DECODE_STAGES 6
+#endif
+#ifndef NVFP4KV_DECODE_CTAS_PER_SM
+#define NVFP4KV_DECODE_CTAS_PER_SM 3
+#endif
+#ifndef NVFP4KV_DECODE_STAGING
+#define NVFP4KV_DECODE_STAGING 1  // 0: 1-D TMA bulk copies issued by lane 0; 1: cp.async by all lanes
+#endif
+constexpr int kNW = NVFP4KV_DECODE_WARPS;              // warps per CTA (each streams its own pages)
+constexpr int kStages = NVFP4KV_DECODE_STAGES;         // ring stages per warp (2 pages in compute)
+constexpr int kCtasPerSm = NVFP4KV_DECODE_CTAS_PER_SM; // resident CTAs per SM the launch is sized for
 constexpr int kGMax = 8;        // query heads per KV head (one MMA n-tile)
 constexpr float kLazy = 8.0f;   // running-max slack (log2 units): P <= 2^8 in f16
 
@@ -167,65 +180,74 @@ struct ItemMap {
   int pair;    // b * hkv + h, -1 past the warp's range
   int page;    // page index within the sequence
   int np;      // pages of the pair
-  int nvalid;  // valid tokens in the page (1..16)
+  int info;    // valid tokens (0..16; 0 for an invalid page) | kNewSeg | kSameNext
 };
+constexpr int kNvMask = 31;
+constexpr int kNewSeg = 32;    // the item's pair differs from the previous item's
+constexpr int kSameNext = 64;  // the next item is in this chunk and has the same pair
 
 // Map items [i0, i0 + 32) of the warp range starting at wr0 (n items) to pages.
 // (cb, ccu) is a sequence whose first page-head is <= the chunk's first item;
-// on return it is the sequence of the chunk's last valid item.
+// on return it is the sequence of the chunk's last valid item.  prev_pair is
+// the pair of the item before the chunk (-1 at the start), updated likewise.
 __device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr0, int i0, int n, int& cb,
-                                             int& ccu, int lane) {
+                                             int& ccu, int& prev_pair, int lane) {
   ItemMap m;
   m.row = -1;
   m.pair = -1;
   m.page = 0;
   m.np = 1;
-  m.nvalid = 0;
+  int nv = 0;
   const int i = i0 + lane;
   int b = cb, cu = ccu;
   if (i < n) {
     const long long r = wr0 + i;
-    int np = pages_of(p, b);
+    int L = clamp_len(p, b);
+    int np = (L + kPage - 1) / kPage;
     while (r >= (long long)(cu + np) * p.hkv) {
       cu += np;
       ++b;
-      np = pages_of(p, b);
+      L = clamp_len(p, b);
+      np = (L + kPage - 1) / kPage;
     }
     const int local = (int)(r - (long long)cu * p.hkv);
     const int h = local / np;
     const int page = local - h * np;
-    const int L = clamp_len(p, b);
     m.pair = b * p.hkv + h;
     m.page = page;
     m.np = np;
-    m.nvalid = min(kPage, L - page * kPage);
     const int pid = __ldg(p.page_table + (long long)b * p.max_pages + page);
     if (pid >= 0 && pid < p.num_pages) {
       m.row = pid * p.hkv + h;
+      nv = min(kPage, L - page * kPage);
     } else {
       flag_error(p.status, NVFP4KV_DEVERR_PAGE);
     }
   }
+  const int up = __shfl_up_sync(0xFFFFFFFFu, m.pair, 1);
+  const int before = lane == 0 ? prev_pair : up;
+  const int next = __shfl_down_sync(0xFFFFFFFFu, m.pair, 1);
+  m.info = nv | (m.pair != before ? kNewSeg : 0) | (lane < 31 && i + 1 < n && next == m.pair ? kSameNext : 0);
   const int last = min(31, n - 1 - i0);
   cb = __shfl_sync(0xFFFFFFFFu, b, last);
   ccu = __shfl_sync(0xFFFFFFFFu, cu, last);
+  prev_pair = __shfl_sync(0xFFFFFFFFu, m.pair, last);
   return m;
 }
 
-__device__ __forceinline__ ItemMap shfl_map(const ItemMap& m, int src) {
-  ItemMap r;
-  r.row = __shfl_sync(0xFFFFFFFFu, m.row, src);
-  r.pair = __shfl_sync(0xFFFFFFFFu, m.pair, src);
-  r.page = __shfl_sync(0xFFFFFFFFu, m.page, src);
-  r.np = __shfl_sync(0xFFFFFFFFu, m.np, src);
-  r.nvalid = __shfl_sync(0xFFFFFFFFu, m.nvalid, src);
+// The row (physical page-head) of item j, from the chunk map that holds it.
+__device__ __forceinline__ int item_row(const ItemMap& cur, const ItemMap& nxt, int j, int i_chunk) {
+  int r;
+  if ((j >> 5) == i_chunk)
+    r = __shfl_sync(0xFFFFFFFFu, cur.row, j & 31);
+  else
+    r = __shfl_sync(0xFFFFFFFFu, nxt.row, j & 31);
   return r;
 }
 
 // Lane 0 starts the copies of one page-head (K/V data and scales) into a ring
 // stage; an invalid page (row < 0) only arrives on the barrier.
-__device__ __forceinline__ void issue_page(const DecodeParams& p, int row, uint8_t* st, uint32_t bar, int lane) {
-  if (lane != 0) return;
+__device__ __forceinline__ void issue_page(const DecodeParams& p, int row, uint8_t* st, uint32_t bar) {
   if (row >= 0) {
     const long long off = (long long)row * kPage;
     mbar_arrive_expect_tx(bar, kStageBytes);
@@ -233,6 +255,48 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, int row, uint8
     tma_load_1d(smem_u32(st + kOffVD), p.v_data + off * kRowBytes, kPageDataBytes, bar);
     tma_load_1d(smem_u32(st + kOffKS), p.k_scale + off * kRowScales, kPageScaleBytes, bar);
     tma_load_1d(smem_u32(st + kOffVS), p.v_scale + off * kRowScales, kPageScaleBytes, bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+// cp.async staging: each lane copies fixed 16-byte chunks of every page-head
+// (two of K's data, two of V's, and lanes 0-15 one scale chunk), then arrives
+// (no-increment) on the stage's mbarrier, which expects 32 arrivals.  The
+// lane's source bases and shared-memory offsets are set up once.
+struct LaneCopy {
+  const uint8_t* kd;  // k_data + 16 * lane
+  const uint8_t* vd;  // v_data + 16 * lane
+  const uint8_t* sc;  // (lanes 0-7: k_scale, 8-15: v_scale) + 16 * (lane % 8)
+  uint32_t off;       // 16 * lane
+  uint32_t sc_off;    // stage offset of the lane's scale chunk
+};
+
+__device__ __forceinline__ LaneCopy lane_copy(const DecodeParams& p, int lane) {
+  LaneCopy c;
+  c.kd = p.k_data + 16 * lane;
+  c.vd = p.v_data + 16 * lane;
+  c.sc = (lane < 8 ? p.k_scale : p.v_scale) + 16 * (lane & 7);
+  c.off = 16u * lane;
+  c.sc_off = (lane < 8 ? kOffKS : kOffVS) + 16u * (lane & 7);
+  return c;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void issue_page_cpasync(const LaneCopy& c, int row, uint32_t st, uint32_t bar,
+                                                   int lane) {
+  if (row >= 0) {
+    const size_t data_off = (size_t)row * kPageDataBytes;
+    const size_t scale_off = (size_t)row * kPageScaleBytes;
+    cp_async16(st + kOffKD + c.off, c.kd + data_off);
+    cp_async16(st + kOffKD + 512 + c.off, c.kd + data_off + 512);
+    cp_async16(st + kOffVD + c.off, c.vd + data_off);
+    cp_async16(st + kOffVD + 512 + c.off, c.vd + data_off + 512);
+    if (lane < 16) cp_async16(st + c.sc_off, c.sc + scale_off);
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
   } else {
     mbar_arrive(bar);
   }
@@ -296,40 +360,61 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, int pair, WarpStat
   s.l0 = s.l1 = 0.0f;
 }
 
-// One page of one KV head (16 tokens, nvalid of them valid) from a ring stage.
-__device__ __forceinline__ void process_page(const uint8_t* stage, int nvalid, WarpState& s, int g, int t) {
-  // ---- S^T = Khat q^T --------------------------------------------------------
-  const uint8_t* kd = stage + kOffKD;
-  const uint8_t* ks = stage + kOffKS;
-  const uint4 ka = *reinterpret_cast<const uint4*>(kd + g * kRowBytes + 16 * t);
-  const uint4 kb = *reinterpret_cast<const uint4*>(kd + (g + 8) * kRowBytes + 16 * t);
-  const uint32_t ska = *reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t);
-  const uint32_t skb = *reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t);
-  const uint32_t sa = e4m3x2_to_f16x2(ska);  // (block 2t, block 2t+1) of token g
-  const uint32_t sb = e4m3x2_to_f16x2(skb);  // same for token g + 8
-  const uint32_t sa0 = dup_lo(sa), sa1 = dup_hi(sa), sb0 = dup_lo(sb), sb1 = dup_hi(sb);
-  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+// Phase 1 of a step: S^T = Khat q^T for NP pages (16 tokens x G heads each),
+// two independent accumulator chains per page (tiles 0-3 and 4-7).
+template <int NP>
+__device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], const WarpState& s,
+                                         float (&sc)[NP][2][4], int g, int t) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t wa = word_of(ka, i >> 1), wb = word_of(kb, i >> 1);
-    uint32_t a0, a1, a2, a3;
-    if (i & 1) {
-      a0 = cvt_sel<2>(wa); a1 = cvt_sel<2>(wb); a2 = cvt_sel<3>(wa); a3 = cvt_sel<3>(wb);
-    } else {
-      a0 = cvt_sel<0>(wa); a1 = cvt_sel<0>(wb); a2 = cvt_sel<1>(wa); a3 = cvt_sel<1>(wb);
+  for (int k = 0; k < NP; ++k) {
+    const uint8_t* kd = stage[k] + kOffKD;
+    const uint8_t* ks = stage[k] + kOffKS;
+    const uint4 ka = *reinterpret_cast<const uint4*>(kd + g * kRowBytes + 16 * t);
+    const uint4 kb = *reinterpret_cast<const uint4*>(kd + (g + 8) * kRowBytes + 16 * t);
+    const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t));
+    const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t));
+    const uint32_t sa0 = dup_lo(sa), sa1 = dup_hi(sa), sb0 = dup_lo(sb), sb1 = dup_hi(sb);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[k][h][j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t wa = word_of(ka, i >> 1), wb = word_of(kb, i >> 1);
+      uint32_t a0, a1, a2, a3;
+      if (i & 1) {
+        a0 = cvt_sel<2>(wa); a1 = cvt_sel<2>(wb); a2 = cvt_sel<3>(wa); a3 = cvt_sel<3>(wb);
+      } else {
+        a0 = cvt_sel<0>(wa); a1 = cvt_sel<0>(wb); a2 = cvt_sel<1>(wa); a3 = cvt_sel<1>(wb);
+      }
+      const uint32_t s_g = i < 4 ? sa0 : sa1, s_g8 = i < 4 ? sb0 : sb1;
+      a0 = hmul2(a0, s_g); a2 = hmul2(a2, s_g); a1 = hmul2(a1, s_g8); a3 = hmul2(a3, s_g8);
+      mma16816(sc[k][i >> 2], a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
     }
-    const uint32_t s_g = i < 4 ? sa0 : sa1, s_g8 = i < 4 ? sb0 : sb1;
-    a0 = hmul2(a0, s_g); a2 = hmul2(a2, s_g); a1 = hmul2(a1, s_g8); a3 = hmul2(a3, s_g8);
-    mma16816(sc, a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
   }
 
-  // ---- online softmax (base 2) ----------------------------------------------
-  float x0 = sc[0] * s.c0, x1 = sc[1] * s.c1, x2 = sc[2] * s.c0, x3 = sc[3] * s.c1;
-  if (nvalid < kPage) {
-    if (g >= nvalid) x0 = x1 = -INFINITY;
-    if (g + 8 >= nvalid) x2 = x3 = -INFINITY;
+}
+
+// Phase 2: online softmax (base 2) over the NP pages' scores, one running-max
+// check for all of them; returns P^T as mma B fragments (k = tokens, n = heads).
+template <int NP, bool kFull>
+__device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const int (&nvalid)[NP], WarpState& s,
+                                              uint32_t (&pb)[NP][2], int g) {
+  float x[NP][4];
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    x[k][0] = (sc[k][0][0] + sc[k][1][0]) * s.c0;
+    x[k][1] = (sc[k][0][1] + sc[k][1][1]) * s.c1;
+    x[k][2] = (sc[k][0][2] + sc[k][1][2]) * s.c0;
+    x[k][3] = (sc[k][0][3] + sc[k][1][3]) * s.c1;
+    if (!kFull && nvalid[k] < kPage) {
+      if (g >= nvalid[k]) x[k][0] = x[k][1] = -INFINITY;
+      if (g + 8 >= nvalid[k]) x[k][2] = x[k][3] = -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(x[k][0], x[k][2]));
+    mx1 = fmaxf(mx1, fmaxf(x[k][1], x[k][3]));
   }
-  float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
   const bool need = (mx0 > s.m0 + kLazy) || (mx1 > s.m1 + kLazy);
   if (__any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
@@ -348,40 +433,52 @@ __device__ __forceinline__ void process_page(const uint8_t* stage, int nvalid, W
     s.m0 = n0;
     s.m1 = n1;
   }
-  const float p0 = ex2(x0 - s.m0), p1 = ex2(x1 - s.m1), p2 = ex2(x2 - s.m0), p3 = ex2(x3 - s.m1);
-  s.l0 += p0 + p2;
-  s.l1 += p1 + p3;
-  // P^T (tokens x heads) in the accumulator layout -> B fragments (k = tokens, n = heads)
-  const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-  const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
-
-  // ---- O^T += Vhat^T P^T -----------------------------------------------------
-  const uint8_t* vd = stage + kOffVD;
-  const uint8_t* vs = stage + kOffVS;
-  const int t0 = 2 * t, t1 = 2 * t + 1, t8 = 2 * t + 8, t9 = 2 * t + 9;
-  uint32_t s0 = vs[t0 * kRowScales + g], s1 = vs[t1 * kRowScales + g];
-  uint32_t s8 = vs[t8 * kRowScales + g], s9 = vs[t9 * kRowScales + g];
-  if (nvalid < kPage) {  // tokens past the end: scale 0 keeps unwritten bytes out of the sum
-    if (t0 >= nvalid) s0 = 0;
-    if (t1 >= nvalid) s1 = 0;
-    if (t8 >= nvalid) s8 = 0;
-    if (t9 >= nvalid) s9 = 0;
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const float p0 = ex2(x[k][0] - s.m0), p1 = ex2(x[k][1] - s.m1);
+    const float p2 = ex2(x[k][2] - s.m0), p3 = ex2(x[k][3] - s.m1);
+    s.l0 += p0 + p2;
+    s.l1 += p1 + p3;
+    // P^T (tokens x heads) in the accumulator layout -> B fragments (k = tokens, n = heads)
+    pb[k][0] = movmatrix_trans(pack_f16x2(p0, p1));
+    pb[k][1] = movmatrix_trans(pack_f16x2(p2, p3));
   }
-  const uint32_t sv01 = e4m3x2_to_f16x2(s0 | (s1 << 8));  // (token 2t, token 2t+1)
-  const uint32_t sv89 = e4m3x2_to_f16x2(s8 | (s9 << 8));
-  const uint2 d0 = *reinterpret_cast<const uint2*>(vd + t0 * kRowBytes + 8 * g);
-  const uint2 d1 = *reinterpret_cast<const uint2*>(vd + t1 * kRowBytes + 8 * g);
-  const uint2 d8 = *reinterpret_cast<const uint2*>(vd + t8 * kRowBytes + 8 * g);
-  const uint2 d9 = *reinterpret_cast<const uint2*>(vd + t9 * kRowBytes + 8 * g);
-  // interleave nibbles of two tokens: byte j of lo = (even d of token a, even d of token b)
-  const uint32_t lo01a = (d0.x & 0x0F0F0F0Fu) | ((d1.x << 4) & 0xF0F0F0F0u);
-  const uint32_t hi01a = ((d0.x >> 4) & 0x0F0F0F0Fu) | (d1.x & 0xF0F0F0F0u);
-  const uint32_t lo01b = (d0.y & 0x0F0F0F0Fu) | ((d1.y << 4) & 0xF0F0F0F0u);
-  const uint32_t hi01b = ((d0.y >> 4) & 0x0F0F0F0Fu) | (d1.y & 0xF0F0F0F0u);
-  const uint32_t lo89a = (d8.x & 0x0F0F0F0Fu) | ((d9.x << 4) & 0xF0F0F0F0u);
-  const uint32_t hi89a = ((d8.x >> 4) & 0x0F0F0F0Fu) | (d9.x & 0xF0F0F0F0u);
-  const uint32_t lo89b = (d8.y & 0x0F0F0F0Fu) | ((d9.y << 4) & 0xF0F0F0F0u);
-  const uint32_t hi89b = ((d8.y >> 4) & 0x0F0F0F0Fu) | (d9.y & 0xF0F0F0F0u);
+
+}
+
+// Phase 3: O^T += Vhat^T P^T for the NP pages.
+template <int NP, bool kFull>
+__device__ __forceinline__ void pv_phase(const uint8_t* const (&stage)[NP], const int (&nvalid)[NP],
+                                         const uint32_t (&pb)[NP][2], WarpState& s, int g, int t) {
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const uint8_t* vd = stage[k] + kOffVD;
+    const uint8_t* vs = stage[k] + kOffVS;
+    const int t0 = 2 * t, t1 = 2 * t + 1, t8 = 2 * t + 8, t9 = 2 * t + 9;
+    uint32_t s0 = vs[t0 * kRowScales + g], s1 = vs[t1 * kRowScales + g];
+    uint32_t s8 = vs[t8 * kRowScales + g], s9 = vs[t9 * kRowScales + g];
+    if (!kFull && nvalid[k] < kPage) {  // tokens past the end: scale 0 keeps unwritten bytes out of the sum
+      if (t0 >= nvalid[k]) s0 = 0;
+      if (t1 >= nvalid[k]) s1 = 0;
+      if (t8 >= nvalid[k]) s8 = 0;
+      if (t9 >= nvalid[k]) s9 = 0;
+    }
+    const uint32_t sv01 = e4m3x2_to_f16x2(s0 | (s1 << 8));  // (token 2t, token 2t+1)
+    const uint32_t sv89 = e4m3x2_to_f16x2(s8 | (s9 << 8));
+    const uint2 d0 = *reinterpret_cast<const uint2*>(vd + t0 * kRowBytes + 8 * g);
+    const uint2 d1 = *reinterpret_cast<const uint2*>(vd + t1 * kRowBytes + 8 * g);
+    const uint2 d8 = *reinterpret_cast<const uint2*>(vd + t8 * kRowBytes + 8 * g);
+    const uint2 d9 = *reinterpret_cast<const uint2*>(vd + t9 * kRowBytes + 8 * g);
+    // interleave nibbles of two tokens: byte j of lo = (even d of token a, even d of token b)
+    const uint32_t lo01a = (d0.x & 0x0F0F0F0Fu) | ((d1.x << 4) & 0xF0F0F0F0u);
+    const uint32_t hi01a = ((d0.x >> 4) & 0x0F0F0F0Fu) | (d1.x & 0xF0F0F0F0u);
+    const uint32_t lo01b = (d0.y & 0x0F0F0F0Fu) | ((d1.y << 4) & 0xF0F0F0F0u);
+    const uint32_t hi01b = ((d0.y >> 4) & 0x0F0F0F0Fu) | (d1.y & 0xF0F0F0F0u);
+    const uint32_t lo89a = (d8.x & 0x0F0F0F0Fu) | ((d9.x << 4) & 0xF0F0F0F0u);
+    const uint32_t hi89a = ((d8.x >> 4) & 0x0F0F0F0Fu) | (d9.x & 0xF0F0F0F0u);
+    const uint32_t lo89b = (d8.y & 0x0F0F0F0Fu) | ((d9.y << 4) & 0xF0F0F0F0u);
+    const uint32_t hi89b = ((d8.y >> 4) & 0x0F0F0F0Fu) | (d9.y & 0xF0F0F0F0u);
+    const uint32_t pb0 = pb[k][0], pb1 = pb[k][1];
 #define NVFP4KV_PV_TILE(I, LO01, HI01, LO89, HI89, K)                                   \
   {                                                                                     \
     const uint32_t a0 = hmul2(cvt_sel<K>(LO01), sv01);                                  \
@@ -390,15 +487,29 @@ __device__ __forceinline__ void process_page(const uint8_t* stage, int nvalid, W
     const uint32_t a3 = hmul2(cvt_sel<K>(HI89), sv89);                                  \
     mma16816(s.o[I], a0, a1, a2, a3, pb0, pb1);                                         \
   }
-  NVFP4KV_PV_TILE(0, lo01a, hi01a, lo89a, hi89a, 0)
-  NVFP4KV_PV_TILE(1, lo01a, hi01a, lo89a, hi89a, 1)
-  NVFP4KV_PV_TILE(2, lo01a, hi01a, lo89a, hi89a, 2)
-  NVFP4KV_PV_TILE(3, lo01a, hi01a, lo89a, hi89a, 3)
-  NVFP4KV_PV_TILE(4, lo01b, hi01b, lo89b, hi89b, 0)
-  NVFP4KV_PV_TILE(5, lo01b, hi01b, lo89b, hi89b, 1)
-  NVFP4KV_PV_TILE(6, lo01b, hi01b, lo89b, hi89b, 2)
-  NVFP4KV_PV_TILE(7, lo01b, hi01b, lo89b, hi89b, 3)
+    NVFP4KV_PV_TILE(0, lo01a, hi01a, lo89a, hi89a, 0)
+    NVFP4KV_PV_TILE(1, lo01a, hi01a, lo89a, hi89a, 1)
+    NVFP4KV_PV_TILE(2, lo01a, hi01a, lo89a, hi89a, 2)
+    NVFP4KV_PV_TILE(3, lo01a, hi01a, lo89a, hi89a, 3)
+    NVFP4KV_PV_TILE(4, lo01b, hi01b, lo89b, hi89b, 0)
+    NVFP4KV_PV_TILE(5, lo01b, hi01b, lo89b, hi89b, 1)
+    NVFP4KV_PV_TILE(6, lo01b, hi01b, lo89b, hi89b, 2)
+    NVFP4KV_PV_TILE(7, lo01b, hi01b, lo89b, hi89b, 3)
 #undef NVFP4KV_PV_TILE
+  }
+}
+
+// NP pages of one KV head (16 tokens each, nvalid[k] of them valid) from ring
+// stages, folded into the warp's running softmax state with one max update.
+// kFull: every page has all 16 tokens (no masking code).
+template <int NP, bool kFull>
+__device__ __forceinline__ void process_pages(const uint8_t* const (&stage)[NP], const int (&nvalid)[NP],
+                                              WarpState& s, int g, int t) {
+  float sc[NP][2][4];
+  uint32_t pb[NP][2];
+  qk_phase<NP>(stage, s, sc, g, t);
+  softmax_phase<NP, kFull>(sc, nvalid, s, pb, g);
+  pv_phase<NP, kFull>(stage, nvalid, pb, s, g, t);
 }
 
 // Finish a warp's piece of a pair: total l over the lanes, then either write
@@ -445,6 +556,13 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, WarpState& s
   }
 }
 
+// A piece record in shared memory: slot 0 of warp w in the slot area, slot 1
+// at the start of warp w's ring (free once the warp has finished streaming).
+__device__ __forceinline__ float* slot_ptr(uint8_t* ring, float* slot0, int so) {
+  return (so & 1) ? reinterpret_cast<float*>(ring + (so >> 1) * kStages * kStageBytes)
+                  : slot0 + (so >> 1) * kRecFloats;
+}
+
 __device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int warp, int lane) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
@@ -466,8 +584,10 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   __shared__ long long red[kNW];
   __shared__ int wstart_b[kNW], wstart_cu[kNW];
   __shared__ int run_first[2 * kNW], run_count[2 * kNW], slot_order[2 * kNW];
-  __shared__ int s_nruns, s_last;
-  __shared__ long long s_cfirst, s_clast;
+  __shared__ int s_nruns, s_npend;
+  __shared__ float s_w[2 * kNW][kGMax], s_M[kGMax], s_L[kGMax];
+  __shared__ int s_pend_pair[2], s_pend_last[2];
+  __shared__ long long s_pend_cf[2], s_pend_cl[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -540,69 +660,113 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
 
   if (n > 0) {
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) mbar_init(wbar + 8 * s, 1);
+      for (int s = 0; s < kStages; ++s) mbar_init(wbar + 8 * s, NVFP4KV_DECODE_STAGING == 1 ? 32 : 1);
       fence_mbar_init();
     }
     __syncwarp();
-    int cb = wstart_b[warp], ccu = wstart_cu[warp];
-    ItemMap cur = map_chunk(p, wr0, 0, n, cb, ccu, lane);
-    ItemMap nxt;
-    nxt.row = -1;
-    nxt.pair = -1; nxt.page = 0; nxt.np = 1; nxt.nvalid = 0;
-    if (n > 32) nxt = map_chunk(p, wr0, 32, n, cb, ccu, lane);
+    int cb = wstart_b[warp], ccu = wstart_cu[warp], prev_pair = -1;
+    ItemMap cur = map_chunk(p, wr0, 0, n, cb, ccu, prev_pair, lane);
+    ItemMap nxt = cur;
+    if (n > 32) nxt = map_chunk(p, wr0, 32, n, cb, ccu, prev_pair, lane);
 
     bool ok = true;  // false after a wait gave up: stop issuing and computing
-    // producer: prefill the ring
+    // producer: prefill the ring (all within the first chunk: kStages < 32)
     const int pre = n < kStages ? n : kStages;
-    for (int j = 0; j < pre; ++j)
-      issue_page(p, __shfl_sync(0xFFFFFFFFu, cur.row, j), wring + j * kStageBytes, wbar + 8 * j, lane);
+    const LaneCopy lc = lane_copy(p, lane);
+    const uint32_t wring_u32 = smem_u32(wring);
+    for (int j = 0; j < pre; ++j) {
+      const int row = __shfl_sync(0xFFFFFFFFu, cur.row, j);
+      if (NVFP4KV_DECODE_STAGING == 1)
+        issue_page_cpasync(lc, row, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
+      else if (lane == 0)
+        issue_page(p, row, wring + j * kStageBytes, wbar + 8 * j);
+    }
     int issued = pre;
 
     WarpState s;
     int seg_pair = -1, seg_first = 0, seg_last = 0, seg_np = 1, nseg = 0;
     long long seg_r = 0;
-    for (int i = 0; i < n; ++i) {
-      if (i > 0 && (i & 31) == 0) {
+    int chunk = 0;   // the chunk `cur` maps
+    int st = 0;      // ring stage of item i
+    uint32_t ph = 0; // its mbarrier phase parity
+    int i = 0;
+    while (i < n) {
+      if ((i >> 5) != chunk) {
         cur = nxt;
-        if (i + 32 < n) nxt = map_chunk(p, wr0, i + 32, n, cb, ccu, lane);
+        chunk = i >> 5;
+        if ((chunk + 1) * 32 < n) nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, cb, ccu, prev_pair, lane);
       }
-      const ItemMap it = shfl_map(cur, i & 31);
-      if (it.pair != seg_pair) {
+      const int li = i & 31;
+      const int info0 = __shfl_sync(0xFFFFFFFFu, cur.info, li);
+      const int row0 = __shfl_sync(0xFFFFFFFFu, cur.row, li);
+      const int li1 = li + 1 < 32 ? li + 1 : 31;
+      const int info1 = __shfl_sync(0xFFFFFFFFu, cur.info, li1);
+      if (info0 & kNewSeg) {
         if (seg_pair >= 0) {
           // a piece that ends before the warp range does: complete unless it is the first
           const bool complete = seg_first == 0 && seg_last == seg_np - 1;
           finish_piece(p, s, seg_pair, complete, wslot0, g, t);
-          if (!complete && lane == 0) {
-            sinfo[warp][0] = SlotInfo{seg_pair, seg_first, seg_last, seg_np, seg_r};
-          }
+          if (!complete && lane == 0) sinfo[warp][0] = SlotInfo{seg_pair, seg_first, seg_last, seg_np, seg_r};
         }
-        seg_pair = it.pair;
-        seg_first = it.page;
-        seg_np = it.np;
+        seg_pair = __shfl_sync(0xFFFFFFFFu, cur.pair, li);
+        seg_first = __shfl_sync(0xFFFFFFFFu, cur.page, li);
+        seg_np = __shfl_sync(0xFFFFFFFFu, cur.np, li);
+        seg_last = seg_first - 1;
         seg_r = wr0 + i;
         ++nseg;
         load_q(p, seg_pair, s, g, t);
       }
-      seg_last = it.page;
-      const int stage = i % kStages;
-      if (ok) {
+      // a second page of the same pair in the same chunk: take both in one step
+      const bool two = (info0 & kSameNext) != 0;
+      seg_last += two ? 2 : 1;
+      const int st1 = st + 1 == kStages ? 0 : st + 1;
+      const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
+      {
         // every lane waits; the outcome is made warp-uniform before it is used
-        const bool done = mbar_wait(wbar + 8 * stage, (uint32_t)((i / kStages) & 1));
+        bool done = mbar_wait(wbar + 8 * st, ph);
+        if (two) done = mbar_wait(wbar + 8 * st1, ph1) && done;
         if (!__all_sync(0xFFFFFFFFu, done)) {
           ok = false;
           if (lane == 0) flag_error(p.status, kDevErrTimeout);
+          break;
         }
       }
-      if (ok && it.row >= 0) process_page(wring + stage * kStageBytes, it.nvalid, s, g, t);
+      // a missing or invalid page takes part with no valid tokens
+      const int nv0 = info0 & kNvMask;
+      const int nv1 = two ? (info1 & kNvMask) : 0;
+      {
+        const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + (two ? st1 : st) * kStageBytes};
+        const int nvs[2] = {nv0, nv1};
+        if ((nv0 & nv1) == kPage)
+          process_pages<2, true>(stg, nvs, s, g, t);
+        else if (nv0 | nv1)
+          process_pages<2, false>(stg, nvs, s, g, t);
+      }
       __syncwarp();
-      // refill this stage with item i + kStages
-      const int j = i + kStages;
-      if (ok && j < n) {
-        const int src = j & 31;
-        const int row = ((j >> 5) == (i >> 5)) ? __shfl_sync(0xFFFFFFFFu, cur.row, src)
-                                               : __shfl_sync(0xFFFFFFFFu, nxt.row, src);
-        issue_page(p, row, wring + stage * kStageBytes, wbar + 8 * stage, lane);
-        issued = j + 1;
+      // refill the freed stages with items i + kStages (and i + 1 + kStages)
+      {
+        const int ja = i + kStages, jb = i + 1 + kStages;
+        const int ra = ja < n ? item_row(cur, nxt, ja, chunk) : -1;
+        const int rb = (two && jb < n) ? item_row(cur, nxt, jb, chunk) : -1;
+        if (NVFP4KV_DECODE_STAGING == 1) {
+          if (ja < n) issue_page_cpasync(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+          if (two && jb < n) issue_page_cpasync(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
+        } else if (lane == 0) {
+          if (ja < n) issue_page(p, ra, wring + st * kStageBytes, wbar + 8 * st);
+          if (two && jb < n) issue_page(p, rb, wring + st1 * kStageBytes, wbar + 8 * st1);
+        }
+        if (ja < n) issued = ja + 1;
+        if (two && jb < n) issued = jb + 1;
+      }
+      // advance to item i + 1 (+ 1)
+      if (two) {
+        st = st1 + 1 == kStages ? 0 : st1 + 1;
+        ph = st1 + 1 == kStages ? ph1 ^ 1u : ph1;
+        i += 2;
+      } else {
+        st = st1;
+        ph = ph1;
+        i += 1;
       }
     }
     if (!ok) {
@@ -639,89 +803,138 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         ++ns;
       }
     s_nruns = nr;
+    s_npend = 0;
   }
   __syncthreads();
   const int nruns = s_nruns;
+  // phase 1: merge each run of shared-memory pieces; complete pairs go to out,
+  // pairs cut by the CTA range become a record in the workspace (at most two:
+  // the range's first and last pair)
   for (int rk = 0; rk < nruns; ++rk) {
     const int f = run_first[rk], cnt = run_count[rk];
     const SlotInfo& a = sinfo[slot_order[f] >> 1][slot_order[f] & 1];
     const SlotInfo& z = sinfo[slot_order[f + cnt - 1] >> 1][slot_order[f + cnt - 1] & 1];
     const int pair = a.pair;
     const bool complete = a.first_page == 0 && z.last_page == a.np - 1;
+    if (tid < p.group) {
+      const int head = tid;
+      float M = -INFINITY;
+      for (int k = 0; k < cnt; ++k) M = fmaxf(M, slot_ptr(ring, slot0, slot_order[f + k])[kOffM + head]);
+      float L = 0.0f;
+      for (int k = 0; k < cnt; ++k) {
+        const float* sl = slot_ptr(ring, slot0, slot_order[f + k]);
+        const float w = sl[kOffM + head] == -INFINITY ? 0.0f : ex2(sl[kOffM + head] - M);
+        s_w[k][head] = w;
+        L += sl[kOffL + head] * w;
+      }
+      s_M[head] = M;
+      s_L[head] = L;
+    }
+    __syncthreads();
     const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
     float* rec = p.part + ((long long)blockIdx.x + pair) * kRecFloats;
-    for (int e = tid; e < p.group * kHeadDim; e += kNW * 32) {
-      const int head = e >> 7, d = e & (kHeadDim - 1);
-      float M = -INFINITY;
+    float* dst = p.out + ((long long)b * p.hq + (long long)h * p.group) * kHeadDim;
+    for (int e4 = tid; e4 < p.group * (kHeadDim / 4); e4 += kNW * 32) {
+      const int head = e4 / (kHeadDim / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int k = 0; k < cnt; ++k) {
-        const int so = slot_order[f + k];
-        const float* sl = (so & 1) ? reinterpret_cast<float*>(ring + (so >> 1) * kStages * kStageBytes)
-                                   : slot0 + (so >> 1) * kRecFloats;
-        M = fmaxf(M, sl[kOffM + head]);
-      }
-      float Ls = 0.0f, Os = 0.0f;
-      for (int k = 0; k < cnt; ++k) {
-        const int so = slot_order[f + k];
-        const float* sl = (so & 1) ? reinterpret_cast<float*>(ring + (so >> 1) * kStages * kStageBytes)
-                                   : slot0 + (so >> 1) * kRecFloats;
-        const float w = sl[kOffM + head] == -INFINITY ? 0.0f : ex2(sl[kOffM + head] - M);
-        Ls += sl[kOffL + head] * w;
-        Os += sl[head * kHeadDim + d] * w;
+        const float w = s_w[k][head];
+        const float4 v = reinterpret_cast<const float4*>(slot_ptr(ring, slot0, slot_order[f + k]))[e4];
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
       }
       if (complete) {
-        p.out[((long long)b * p.hq + (long long)h * p.group + head) * kHeadDim + d] =
-            Ls > 0.0f ? Os * (p.v_gscale / Ls) : 0.0f;
+        const float r = s_L[head] > 0.0f ? p.v_gscale / s_L[head] : 0.0f;
+        reinterpret_cast<float4*>(dst)[e4] = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
       } else {
-        rec[head * kHeadDim + d] = Os;
-        if (d == 0) {
-          rec[kOffM + head] = M;
-          rec[kOffL + head] = Ls;
-        }
+        reinterpret_cast<float4*>(rec)[e4] = acc;
       }
     }
-    if (!complete) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        const long long pair_start = a.r_first - a.first_page;
-        const long long cf = cta_of(pair_start, W, N), cl = cta_of(pair_start + a.np - 1, W, N);
-        const int old = atomicAdd(p.counters + pair, 1);
-        s_last = (old == (int)(cl - cf)) ? 1 : 0;
-        s_cfirst = cf;
-        s_clast = cl;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        const long long cf = s_cfirst, cl = s_clast;
-        for (int e = tid; e < p.group * kHeadDim; e += kNW * 32) {
-          const int head = e >> 7, d = e & (kHeadDim - 1);
-          float M = -INFINITY;
-          for (long long c = cf; c <= cl; ++c) {
-            const float* r = p.part + (c + pair) * kRecFloats;
-            M = fmaxf(M, __ldcg(r + kOffM + head));
-          }
-          float Ls = 0.0f, Os = 0.0f;
-          for (long long c = cf; c <= cl; ++c) {
-            const float* r = p.part + (c + pair) * kRecFloats;
-            const float mc = __ldcg(r + kOffM + head);
-            const float w = mc == -INFINITY ? 0.0f : ex2(mc - M);
-            Ls += __ldcg(r + kOffL + head) * w;
-            Os += __ldcg(r + head * kHeadDim + d) * w;
-          }
-          p.out[((long long)b * p.hq + (long long)h * p.group + head) * kHeadDim + d] =
-              Ls > 0.0f ? Os * (p.v_gscale / Ls) : 0.0f;
-        }
-        if (tid == 0) p.counters[pair] = 0;  // ready for the next call
-      }
+    if (!complete && tid < p.group) {
+      rec[kOffM + tid] = s_M[tid];
+      rec[kOffL + tid] = s_L[tid];
     }
+    if (!complete && tid == 0) {
+      const long long pair_start = a.r_first - a.first_page;
+      const int k = s_npend++;
+      s_pend_pair[k] = pair;
+      s_pend_cf[k] = cta_of(pair_start, W, N);
+      s_pend_cl[k] = cta_of(pair_start + a.np - 1, W, N);
+    }
+    __syncthreads();
+  }
+  const int npend = s_npend;
+  if (npend == 0) return;
+  // phase 2: publish the records, then take a ticket per cut pair; the last
+  // CTA to arrive merges all of the pair's records (nobody waits)
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    for (int k = 0; k < npend; ++k) {
+      const int old = atomicAdd(p.counters + s_pend_pair[k], 1);
+      s_pend_last[k] = old == (int)(s_pend_cl[k] - s_pend_cf[k]);
+    }
+  }
+  __syncthreads();
+  // phase 3: merge records c = cf..cl of each pair this CTA closes; the ring is
+  // free now and holds the records' m and l, then their weights
+  float* wbuf = reinterpret_cast<float*>(ring);
+  for (int k = 0; k < npend; ++k) {
+    if (!s_pend_last[k]) continue;
+    __threadfence();
+    const int pair = s_pend_pair[k];
+    const long long cf = s_pend_cf[k];
+    const int cnt = (int)(s_pend_cl[k] - cf + 1);
+    float* lbuf = wbuf + cnt * kGMax;
+    for (int i = tid; i < cnt * p.group; i += kNW * 32) {
+      const int c = i / p.group, head = i - c * p.group;
+      const float* r = p.part + (cf + c + pair) * kRecFloats;
+      wbuf[c * kGMax + head] = __ldcg(r + kOffM + head);
+      lbuf[c * kGMax + head] = __ldcg(r + kOffL + head);
+    }
+    __syncthreads();
+    if (tid < p.group) {
+      const int head = tid;
+      float M = -INFINITY;
+      for (int c = 0; c < cnt; ++c) M = fmaxf(M, wbuf[c * kGMax + head]);
+      float L = 0.0f;
+      for (int c = 0; c < cnt; ++c) {
+        const float m = wbuf[c * kGMax + head];
+        const float w = m == -INFINITY ? 0.0f : ex2(m - M);
+        wbuf[c * kGMax + head] = w;
+        L += lbuf[c * kGMax + head] * w;
+      }
+      s_L[head] = L;
+    }
+    __syncthreads();
+    const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
+    float* dst = p.out + ((long long)b * p.hq + (long long)h * p.group) * kHeadDim;
+    for (int e4 = tid; e4 < p.group * (kHeadDim / 4); e4 += kNW * 32) {
+      const int head = e4 / (kHeadDim / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int c = 0; c < cnt; ++c) {
+        const float w = wbuf[c * kGMax + head];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part + (cf + c + pair) * kRecFloats) + e4);
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      }
+      const float r = s_L[head] > 0.0f ? p.v_gscale / s_L[head] : 0.0f;
+      reinterpret_cast<float4*>(dst)[e4] = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
+    }
+    if (tid == 0) p.counters[pair] = 0;  // ready for the next call
     __syncthreads();
   }
 }
 
 }  // namespace
 
-int decode_num_ctas(int num_sms) { return num_sms * kCtasPerSm; }
+// The final merge keeps m, l (then weights) of up to one record per CTA in the
+// ring: cap the grid so they always fit.
+constexpr int kMaxCtas = kRingBytes / (2 * kGMax * (int)sizeof(float));
+
+int decode_num_ctas(int num_sms) {
+  const int n = num_sms * kCtasPerSm;
+  return n < kMaxCtas ? n : kMaxCtas;
+}
 
 size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads) {
   const size_t pairs = (size_t)batch * (size_t)num_kv_heads;

@@ -139,17 +139,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Wait until the mbarrier phase with the given parity has completed.  Gives up
 // after about `limit_ns` of wall time and returns false (the caller records a
 // device error and stops using the stage).
+// Each try_wait may suspend the thread (up to the hinted 1 ms) until the phase
+// completes, so a warp waiting for data sleeps instead of spinning.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 1000000000ull) {
   uint32_t done;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
   if (done) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
     if (done) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }

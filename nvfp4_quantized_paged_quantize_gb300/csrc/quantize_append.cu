@@ -8,7 +8,7 @@
 //   amax = max |x|                       (exact; inputs are bf16)
 //   sb   = E4M3(amax / (6 g))            (IEEE division, RNE, saturating)
 //   den  = E4M3val(sb) * g
-//   code = E2M1(x / den)                 (IEEE division, RNE, saturating)
+//   code = E2M1(x / den)                 (x / den rounded to nearest, RNE, saturating)
 // A block with den == 0 stores signed zeros.  The row's 64 data bytes and 8
 // scale bytes go to slot slot_mapping[token].  HBM-bound: 2 B read and 9/16 B
 // written per value.
@@ -86,19 +86,32 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
       amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
       const uint32_t sb = e4m3_from_f32(__fdiv_rn(amax, t6));
       const float den = __fmul_rn(e4m3_to_f32(sb), g);
+      // x / den rounded to nearest: one correctly rounded reciprocal per block,
+      // then per value q0 = x*r and Markstein's correction q0 + r*(x - den*q0)
+      // (two FMAs), which gives the correctly rounded quotient while den, 1/den
+      // and every quotient of the block stay well inside the normal range (a
+      // saturated block scale can push quotients towards overflow); otherwise
+      // IEEE division.
+      const float rcp = __frcp_rn(den);
+      const bool fast = den >= 0x1p-100f && den <= 0x1p+100f && __fmul_rn(amax, rcp) < 0x1p+64f;
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (den == 0.0f) {
+          y[i] = copysignf(0.0f, f[i]);
+        } else if (fast) {
+          const float q0 = __fmul_rn(f[i], rcp);
+          const float rem = __fmaf_rn(-q0, den, f[i]);
+          // a quotient that rounds to zero can come out as +0 for negative x;
+          // the sign of x / den is the sign of x (den > 0)
+          y[i] = copysignf(__fmaf_rn(rem, rcp, q0), f[i]);
+        } else {
+          y[i] = __fdiv_rn(f[i], den);
+        }
+      }
       uint32_t packed = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float y0, y1;
-        if (den == 0.0f) {
-          y0 = copysignf(0.0f, f[2 * k]);
-          y1 = copysignf(0.0f, f[2 * k + 1]);
-        } else {
-          y0 = __fdiv_rn(f[2 * k], den);
-          y1 = __fdiv_rn(f[2 * k + 1], den);
-        }
-        packed |= e2m1x2_from_f32(y0, y1) << (8 * k);
-      }
+      for (int k = 0; k < 4; ++k) packed |= e2m1x2_from_f32(y[2 * k], y[2 * k + 1]) << (8 * k);
       reinterpret_cast<uint32_t*>(data + row * kRowBytes)[sub] = packed;
       if ((sub & 1) == 0) scale[row * kRowScales + (sub >> 1)] = (uint8_t)sb;
     }

@@ -139,3 +139,24 @@ def test_extend_chunk_full_size_bit_exact(cuda_lib):
     o = oracle.Cache(wl.num_pages, wl.num_kv_heads)
     assert oracle.quantize_append(o, k, v, slots) == 0
     _assert_pool_equal(g, o)
+
+
+def test_random_blocks_wide_scale_range_bit_exact(cuda_lib):
+    # 2^20 blocks: magnitudes over 60 binades, global scales over 40 binades
+    rng = np.random.default_rng(21)
+    for trial, (lo, hi) in enumerate([(-30, 30), (-6, 6)]):
+        n = 1 << 13                                          # tokens of one head: 8 blocks each
+        mag = 2.0 ** rng.uniform(lo, hi, (n, 1, 8, 1))
+        x = (rng.standard_normal((n, 1, 8, 16)) * mag).astype(np.float32).reshape(n, 1, 128)
+        x[rng.random(x.shape) < 0.01] *= -1e3
+        kb = inputs.bf16_bits(x)
+        vb = inputs.bf16_bits(rng.standard_t(3, x.shape).astype(np.float32) * np.float32(2.0 ** rng.uniform(-8, 8)))
+        for gk, gv in [(float(2.0 ** rng.uniform(-20, 20)), float(2.0 ** rng.uniform(-20, 20))) for _ in range(3)]:
+            gk, gv = float(np.float32(gk)), float(np.float32(gv))
+            pages = n // 16
+            slots = rng.permutation(n).astype(np.int64)
+            g = gpu_cache(pages, 1, gk, gv)
+            gpu_append(g, kb, vb, slots)
+            o = oracle.Cache(pages, 1, 128, 16, gk, gv)
+            assert oracle.quantize_append(o, kb, vb, slots) == 0
+            _assert_pool_equal(g, o)
