@@ -153,6 +153,39 @@ int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* o
                              float softmax_scale, void* workspace, size_t workspace_bytes,
                              int32_t* device_status, nvfp4kv_stream_t stream);
 
+/* Bytes of the fixed device scratch used by nvfp4kv_decode_attention_static. */
+#define NVFP4KV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * nvfp4kv_decode_attention without a caller-provided workspace, for callers
+ * that cannot allocate device memory (for example code running inside an
+ * allocator hook, or a plug-in whose host runtime owns all device memory).
+ * The source pages have no counterpart to this call; it only changes where
+ * the decode's split-K scratch lives.
+ *
+ * The scratch is a fixed NVFP4KV_STATIC_SCRATCH_BYTES (16 MiB) array in the
+ * library's device image: every GPU that loads the library holds it until the
+ * process exits.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Each call clears the arrival counters it
+ * needs (cudaMemsetAsync on its stream) and then runs exactly what
+ * nvfp4kv_decode_attention runs.  Nothing is allocated or freed.
+ *
+ * All calls share the one array, which keeps the last call's contents: calls
+ * that overlap on the GPU (different streams, or different host threads
+ * without ordering) race and give wrong results; serialise them.
+ *
+ * Arguments, layout and errors are those of nvfp4kv_decode_attention without
+ * `workspace` / `workspace_bytes`.  A batch whose workspace would exceed the
+ * fixed scratch (see nvfp4kv_decode_workspace_size) returns
+ * NVFP4KV_ERR_WORKSPACE before anything is enqueued.
+ */
+int nvfp4kv_decode_attention_static(const nvfp4kv_cache* cache, const void* q, float* out,
+                                    const int32_t* page_table, int32_t max_pages_per_seq,
+                                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                    float softmax_scale, int32_t* device_status,
+                                    nvfp4kv_stream_t stream);
+
 /*
  * Dequantise cached prefixes into an FP8 E4M3 workspace for chunked prefill /
  * extend ("nvfp4-kv-cache-memory-wall", section 3, item 2: the NVFP4 prefix is
