@@ -44,6 +44,32 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def decode_source_hash():
+    """sha256 of the decode kernel's sources (a committed ncu traffic figure is
+    reported only while it still describes this code)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("decode_attention.cu", "nvfp4kv_device.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_quantized_paged_quantize_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def committed_traffic(workload):
+    """DRAM bytes per decode launch from profiles/decode_traffic.json (written
+    from an ncu capture), or None if absent or taken on other code."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != decode_source_hash():
+        return None
+    return rec.get("traffic_bytes_per_launch", {}).get(workload)
+
+
 def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -300,7 +326,7 @@ def gpu_arm(args):
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": None,
+            "frac": achieved / hbm_peak, "traffic": committed_traffic(wl.name),
             "kernel": "decode_kernel", "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -447,6 +473,38 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def only_arm(args):
+    """Run one workload's kernels a few times (for profiler command lines)."""
+    import torch
+
+    import nvfp4_quantized_paged_quantize_gb300 as kv
+
+    kv.load()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.zero_()
+    if args.only in ("decode8k", "decode128k"):
+        b = DecodeBench(torch, kv, inputs.decode_config(2 if args.only == "decode8k" else 3))
+        time_steps(torch, args.steps, args.warmup, lambda ev=None: (b.append(), b.decode()), flush)
+    else:
+        ew = inputs.extend_config(num_layers=1)
+        cache = kv.Cache.empty(ew.num_pages, ew.num_kv_heads, zero=True)
+        for s_ in range(ew.batch):
+            k, v = ew.prefix_kv(0, s_)
+            kv.nvfp4kv_quantize_append(cache, _bf16(torch, k), _bf16(torch, v),
+                                       _dev(torch, ew.slots(s_, 0, ew.prefix_len)))
+        ks, vs = zip(*[ew.chunk_kv(0, s_) for s_ in range(ew.batch)])
+        kc, vc = _bf16(torch, np.concatenate(ks)), _bf16(torch, np.concatenate(vs))
+        slots = _dev(torch, ew.chunk_slots())
+        pt, pl, cu = _dev(torch, ew.page_table), _dev(torch, ew.prefix_lens), _dev(torch, ew.cu_prefix)
+        wk = torch.empty((ew.total_rows, ew.num_kv_heads, 128), dtype=torch.uint8, device="cuda")
+        wv = torch.empty_like(wk)
+        time_steps(torch, args.steps, args.warmup,
+                   lambda ev=None: (kv.nvfp4kv_dequant_to_fp8_workspace(cache, pt, pl, cu, wk, wv),
+                                    kv.nvfp4kv_quantize_append(cache, kc, vc, slots)), flush)
+    torch.cuda.synchronize()
+    print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,10 +515,14 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--cpu-total-s", type=float, default=90.0, help="reference arm: total oracle seconds")
+    ap.add_argument("--only", choices=["decode8k", "decode128k", "extend"],
+                    help="run just one workload's kernels (profiler command lines); no JSON metric line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.only:
+        only_arm(args)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_arm(args)

@@ -17,8 +17,9 @@
 //      the 16 tokens x G query heads with mma.sync m16n8k16 (f16 in, f32 acc);
 //      two pages of the same pair are taken per step (32 tokens);
 //   2. runs the online softmax in base 2 (scores scaled by softmax_scale *
-//      log2(e) * g_K); the running max is only raised when a score exceeds it
-//      by more than 8, so the rescale of the accumulators is rare;
+//      log2(e) * g_K, folded into one FMA per score); the running max is only
+//      raised when a score exceeds it by more than 8, so the rescale of the
+//      accumulators is rare;
 //   3. transposes P (f16) with movmatrix and accumulates O^T += Vhat^T P^T,
 //      Vhat^T built from nibble-interleaved V bytes and scaled per token.
 // A (sequence, KV head) pair that lies inside one warp range is finished by
@@ -47,6 +48,9 @@ namespace {
 #endif
 #ifndef NVFP4KV_DECODE_CTAS_PER_SM
 #define NVFP4KV_DECODE_CTAS_PER_SM 3
+#endif
+#ifndef NVFP4KV_DECODE_QK_CHAINS
+#define NVFP4KV_DECODE_QK_CHAINS 2  // independent QK accumulator chains per page (1 or 2)
 #endif
 #ifndef NVFP4KV_DECODE_STAGING
 #define NVFP4KV_DECODE_STAGING 1  // 0: 1-D TMA bulk copies issued by lane 0; 1: cp.async by all lanes
@@ -180,24 +184,20 @@ struct ItemMap {
   int pair;    // b * hkv + h, -1 past the warp's range
   int page;    // page index within the sequence
   int np;      // pages of the pair
-  int info;    // valid tokens (0..16; 0 for an invalid page) | kNewSeg | kSameNext
+  int lastnv;  // valid tokens in the pair's last page (1..16)
 };
-constexpr int kNvMask = 31;
-constexpr int kNewSeg = 32;    // the item's pair differs from the previous item's
-constexpr int kSameNext = 64;  // the next item is in this chunk and has the same pair
 
 // Map items [i0, i0 + 32) of the warp range starting at wr0 (n items) to pages.
 // (cb, ccu) is a sequence whose first page-head is <= the chunk's first item;
-// on return it is the sequence of the chunk's last valid item.  prev_pair is
-// the pair of the item before the chunk (-1 at the start), updated likewise.
+// on return it is the sequence of the chunk's last valid item.
 __device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr0, int i0, int n, int& cb,
-                                             int& ccu, int& prev_pair, int lane) {
+                                             int& ccu, int lane) {
   ItemMap m;
   m.row = -1;
   m.pair = -1;
   m.page = 0;
   m.np = 1;
-  int nv = 0;
+  m.lastnv = kPage;
   const int i = i0 + lane;
   int b = cb, cu = ccu;
   if (i < n) {
@@ -216,22 +216,17 @@ __device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr
     m.pair = b * p.hkv + h;
     m.page = page;
     m.np = np;
+    m.lastnv = L - (np - 1) * kPage;
     const int pid = __ldg(p.page_table + (long long)b * p.max_pages + page);
     if (pid >= 0 && pid < p.num_pages) {
       m.row = pid * p.hkv + h;
-      nv = min(kPage, L - page * kPage);
     } else {
       flag_error(p.status, NVFP4KV_DEVERR_PAGE);
     }
   }
-  const int up = __shfl_up_sync(0xFFFFFFFFu, m.pair, 1);
-  const int before = lane == 0 ? prev_pair : up;
-  const int next = __shfl_down_sync(0xFFFFFFFFu, m.pair, 1);
-  m.info = nv | (m.pair != before ? kNewSeg : 0) | (lane < 31 && i + 1 < n && next == m.pair ? kSameNext : 0);
   const int last = min(31, n - 1 - i0);
   cb = __shfl_sync(0xFFFFFFFFu, b, last);
   ccu = __shfl_sync(0xFFFFFFFFu, cu, last);
-  prev_pair = __shfl_sync(0xFFFFFFFFu, m.pair, last);
   return m;
 }
 
@@ -389,7 +384,7 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
       }
       const uint32_t s_g = i < 4 ? sa0 : sa1, s_g8 = i < 4 ? sb0 : sb1;
       a0 = hmul2(a0, s_g); a2 = hmul2(a2, s_g); a1 = hmul2(a1, s_g8); a3 = hmul2(a3, s_g8);
-      mma16816(sc[k][i >> 2], a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
+      mma16816(sc[k][NVFP4KV_DECODE_QK_CHAINS == 2 ? (i >> 2) : 0], a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
     }
   }
 
@@ -400,21 +395,21 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
 template <int NP, bool kFull>
 __device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const int (&nvalid)[NP], WarpState& s,
                                               uint32_t (&pb)[NP][2], int g) {
-  float x[NP][4];
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  // raw scores; the running max is kept in scaled (base-2) units: max(S c) = c max(S), c > 0
+  float S[NP][4];
+  float ms0 = -INFINITY, ms1 = -INFINITY;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
-    x[k][0] = (sc[k][0][0] + sc[k][1][0]) * s.c0;
-    x[k][1] = (sc[k][0][1] + sc[k][1][1]) * s.c1;
-    x[k][2] = (sc[k][0][2] + sc[k][1][2]) * s.c0;
-    x[k][3] = (sc[k][0][3] + sc[k][1][3]) * s.c1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) S[k][j] = NVFP4KV_DECODE_QK_CHAINS == 2 ? sc[k][0][j] + sc[k][1][j] : sc[k][0][j];
     if (!kFull && nvalid[k] < kPage) {
-      if (g >= nvalid[k]) x[k][0] = x[k][1] = -INFINITY;
-      if (g + 8 >= nvalid[k]) x[k][2] = x[k][3] = -INFINITY;
+      if (g >= nvalid[k]) S[k][0] = S[k][1] = -INFINITY;
+      if (g + 8 >= nvalid[k]) S[k][2] = S[k][3] = -INFINITY;
     }
-    mx0 = fmaxf(mx0, fmaxf(x[k][0], x[k][2]));
-    mx1 = fmaxf(mx1, fmaxf(x[k][1], x[k][3]));
+    ms0 = fmaxf(ms0, fmaxf(S[k][0], S[k][2]));
+    ms1 = fmaxf(ms1, fmaxf(S[k][1], S[k][3]));
   }
+  float mx0 = ms0 * s.c0, mx1 = ms1 * s.c1;
   const bool need = (mx0 > s.m0 + kLazy) || (mx1 > s.m1 + kLazy);
   if (__any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
@@ -433,17 +428,17 @@ __device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const
     s.m0 = n0;
     s.m1 = n1;
   }
+  const float nm0 = -s.m0, nm1 = -s.m1;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
-    const float p0 = ex2(x[k][0] - s.m0), p1 = ex2(x[k][1] - s.m1);
-    const float p2 = ex2(x[k][2] - s.m0), p3 = ex2(x[k][3] - s.m1);
+    const float p0 = ex2(fmaf(S[k][0], s.c0, nm0)), p1 = ex2(fmaf(S[k][1], s.c1, nm1));
+    const float p2 = ex2(fmaf(S[k][2], s.c0, nm0)), p3 = ex2(fmaf(S[k][3], s.c1, nm1));
     s.l0 += p0 + p2;
     s.l1 += p1 + p3;
     // P^T (tokens x heads) in the accumulator layout -> B fragments (k = tokens, n = heads)
     pb[k][0] = movmatrix_trans(pack_f16x2(p0, p1));
     pb[k][1] = movmatrix_trans(pack_f16x2(p2, p3));
   }
-
 }
 
 // Phase 3: O^T += Vhat^T P^T for the NP pages.
@@ -664,12 +659,12 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       fence_mbar_init();
     }
     __syncwarp();
-    int cb = wstart_b[warp], ccu = wstart_cu[warp], prev_pair = -1;
-    ItemMap cur = map_chunk(p, wr0, 0, n, cb, ccu, prev_pair, lane);
+    int cb = wstart_b[warp], ccu = wstart_cu[warp];
+    ItemMap cur = map_chunk(p, wr0, 0, n, cb, ccu, lane);
     ItemMap nxt = cur;
-    if (n > 32) nxt = map_chunk(p, wr0, 32, n, cb, ccu, prev_pair, lane);
+    if (n > 32) nxt = map_chunk(p, wr0, 32, n, cb, ccu, lane);
 
-    bool ok = true;  // false after a wait gave up: stop issuing and computing
+    bool ok = true;  // false after a wait gave up: stop waiting, computing and issuing
     // producer: prefill the ring (all within the first chunk: kStages < 32)
     const int pre = n < kStages ? n : kStages;
     const LaneCopy lc = lane_copy(p, lane);
@@ -682,106 +677,116 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         issue_page(p, row, wring + j * kStageBytes, wbar + 8 * j);
     }
     int issued = pre;
-
-    WarpState s;
-    int seg_pair = -1, seg_first = 0, seg_last = 0, seg_np = 1, nseg = 0;
-    long long seg_r = 0;
+    // valid-page bits of the two chunk maps (bit l: item 32 chunk + l has a valid page)
+    uint32_t vcur = __ballot_sync(0xFFFFFFFFu, cur.row >= 0);
+    uint32_t vnxt = __ballot_sync(0xFFFFFFFFu, nxt.row >= 0);
     int chunk = 0;   // the chunk `cur` maps
-    int st = 0;      // ring stage of item i
+    int st = 0;      // ring stage of the next item
     uint32_t ph = 0; // its mbarrier phase parity
+    WarpState s;
+    int nseg = 0;
     int i = 0;
     while (i < n) {
-      if ((i >> 5) != chunk) {
+      // ---- one piece: items [i, iend) of one (sequence, KV head) pair -------------
+      while ((i >> 5) != chunk) {
         cur = nxt;
-        chunk = i >> 5;
-        if ((chunk + 1) * 32 < n) nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, cb, ccu, prev_pair, lane);
+        vcur = vnxt;
+        ++chunk;
+        if ((chunk + 1) * 32 < n) {
+          nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, cb, ccu, lane);
+          vnxt = __ballot_sync(0xFFFFFFFFu, nxt.row >= 0);
+        }
       }
       const int li = i & 31;
-      const int info0 = __shfl_sync(0xFFFFFFFFu, cur.info, li);
-      const int row0 = __shfl_sync(0xFFFFFFFFu, cur.row, li);
-      const int li1 = li + 1 < 32 ? li + 1 : 31;
-      const int info1 = __shfl_sync(0xFFFFFFFFu, cur.info, li1);
-      if (info0 & kNewSeg) {
-        if (seg_pair >= 0) {
-          // a piece that ends before the warp range does: complete unless it is the first
-          const bool complete = seg_first == 0 && seg_last == seg_np - 1;
-          finish_piece(p, s, seg_pair, complete, wslot0, g, t);
-          if (!complete && lane == 0) sinfo[warp][0] = SlotInfo{seg_pair, seg_first, seg_last, seg_np, seg_r};
+      const int pair = __shfl_sync(0xFFFFFFFFu, cur.pair, li);
+      const int page0 = __shfl_sync(0xFFFFFFFFu, cur.page, li);
+      const int np = __shfl_sync(0xFFFFFFFFu, cur.np, li);
+      const int lastnv = __shfl_sync(0xFFFFFFFFu, cur.lastnv, li);
+      const int iend = min(n, i + (np - page0));
+      const long long piece_r = wr0 + i;
+      ++nseg;
+      load_q(p, pair, s, g, t);
+      for (int j = i; j < iend;) {
+        if ((j >> 5) != chunk) {
+          cur = nxt;
+          vcur = vnxt;
+          ++chunk;
+          if ((chunk + 1) * 32 < n) {
+            nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, cb, ccu, lane);
+            vnxt = __ballot_sync(0xFFFFFFFFu, nxt.row >= 0);
+          }
         }
-        seg_pair = __shfl_sync(0xFFFFFFFFu, cur.pair, li);
-        seg_first = __shfl_sync(0xFFFFFFFFu, cur.page, li);
-        seg_np = __shfl_sync(0xFFFFFFFFu, cur.np, li);
-        seg_last = seg_first - 1;
-        seg_r = wr0 + i;
-        ++nseg;
-        load_q(p, seg_pair, s, g, t);
-      }
-      // a second page of the same pair in the same chunk: take both in one step
-      const bool two = (info0 & kSameNext) != 0;
-      seg_last += two ? 2 : 1;
-      const int st1 = st + 1 == kStages ? 0 : st + 1;
-      const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
-      {
-        // every lane waits; the outcome is made warp-uniform before it is used
-        bool done = mbar_wait(wbar + 8 * st, ph);
-        if (two) done = mbar_wait(wbar + 8 * st1, ph1) && done;
-        if (!__all_sync(0xFFFFFFFFu, done)) {
-          ok = false;
-          if (lane == 0) flag_error(p.status, kDevErrTimeout);
-          break;
+        const bool two = j + 1 < iend;
+        const int st1 = st + 1 == kStages ? 0 : st + 1;
+        const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
+        if (ok) {
+          // every lane waits; the outcome is made warp-uniform before it is used
+          bool done = mbar_wait(wbar + 8 * st, ph);
+          if (two) done = mbar_wait(wbar + 8 * st1, ph1) && done;
+          if (!__all_sync(0xFFFFFFFFu, done)) {
+            ok = false;
+            if (lane == 0) flag_error(p.status, kDevErrTimeout);
+          }
+        }
+        if (ok) {
+          // a page with an invalid id, or a missing second page, has no valid tokens
+          const int pg = page0 + (j - i);
+          const uint32_t vm0 = vcur, vm1 = ((j + 1) >> 5) == chunk ? vcur : vnxt;
+          const int nv0 = ((vm0 >> (j & 31)) & 1u) ? (pg == np - 1 ? lastnv : kPage) : 0;
+          const int nv1 = (two && ((vm1 >> ((j + 1) & 31)) & 1u)) ? (pg + 1 == np - 1 ? lastnv : kPage) : 0;
+          const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + (two ? st1 : st) * kStageBytes};
+          const int nvs[2] = {nv0, nv1};
+          if ((nv0 & nv1) == kPage)
+            process_pages<2, true>(stg, nvs, s, g, t);
+          else if (nv0 | nv1)
+            process_pages<2, false>(stg, nvs, s, g, t);
+          __syncwarp();
+          // refill the freed stages with items j + kStages (and j + 1 + kStages)
+          const int ja = j + kStages, jb = j + 1 + kStages;
+          if (ja < n) {
+            const int ra = item_row(cur, nxt, ja, chunk);
+            if (NVFP4KV_DECODE_STAGING == 1)
+              issue_page_cpasync(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            else if (lane == 0)
+              issue_page(p, ra, wring + st * kStageBytes, wbar + 8 * st);
+            issued = ja + 1;
+          }
+          if (two && jb < n) {
+            const int rb = item_row(cur, nxt, jb, chunk);
+            if (NVFP4KV_DECODE_STAGING == 1)
+              issue_page_cpasync(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
+            else if (lane == 0)
+              issue_page(p, rb, wring + st1 * kStageBytes, wbar + 8 * st1);
+            issued = jb + 1;
+          }
+        }
+        if (two) {
+          st = st1 + 1 == kStages ? 0 : st1 + 1;
+          ph = st1 + 1 == kStages ? ph1 ^ 1u : ph1;
+          j += 2;
+        } else {
+          st = st1;
+          ph = ph1;
+          j += 1;
         }
       }
-      // a missing or invalid page takes part with no valid tokens
-      const int nv0 = info0 & kNvMask;
-      const int nv1 = two ? (info1 & kNvMask) : 0;
-      {
-        const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + (two ? st1 : st) * kStageBytes};
-        const int nvs[2] = {nv0, nv1};
-        if ((nv0 & nv1) == kPage)
-          process_pages<2, true>(stg, nvs, s, g, t);
-        else if (nv0 | nv1)
-          process_pages<2, false>(stg, nvs, s, g, t);
+      if (iend == n && !ok) {
+        // drain: wait (bounded) for every copy still in flight before the ring is reused
+        for (int j = issued - kStages; j < issued; ++j) {
+          if (j < 0) continue;
+          mbar_wait(wbar + 8 * (j % kStages), (uint32_t)((j / kStages) & 1));
+        }
       }
       __syncwarp();
-      // refill the freed stages with items i + kStages (and i + 1 + kStages)
-      {
-        const int ja = i + kStages, jb = i + 1 + kStages;
-        const int ra = ja < n ? item_row(cur, nxt, ja, chunk) : -1;
-        const int rb = (two && jb < n) ? item_row(cur, nxt, jb, chunk) : -1;
-        if (NVFP4KV_DECODE_STAGING == 1) {
-          if (ja < n) issue_page_cpasync(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
-          if (two && jb < n) issue_page_cpasync(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
-        } else if (lane == 0) {
-          if (ja < n) issue_page(p, ra, wring + st * kStageBytes, wbar + 8 * st);
-          if (two && jb < n) issue_page(p, rb, wring + st1 * kStageBytes, wbar + 8 * st1);
-        }
-        if (ja < n) issued = ja + 1;
-        if (two && jb < n) issued = jb + 1;
-      }
-      // advance to item i + 1 (+ 1)
-      if (two) {
-        st = st1 + 1 == kStages ? 0 : st1 + 1;
-        ph = st1 + 1 == kStages ? ph1 ^ 1u : ph1;
-        i += 2;
-      } else {
-        st = st1;
-        ph = ph1;
-        i += 1;
-      }
+      // a piece that ends before the warp range does is complete unless it is the
+      // first; the last piece goes to slot 1 (the idle ring) unless it is also the first
+      const int last_page = page0 + (iend - i) - 1;
+      const bool complete = page0 == 0 && last_page == np - 1;
+      const int slot = (iend == n && nseg > 1) ? 1 : 0;
+      finish_piece(p, s, pair, complete, slot ? wslot1 : wslot0, g, t);
+      if (!complete && lane == 0) sinfo[warp][slot] = SlotInfo{pair, page0, last_page, np, piece_r};
+      i = iend;
     }
-    if (!ok) {
-      // drain: wait (bounded) for every copy still in flight before the ring is reused
-      for (int j = issued - kStages; j < issued; ++j) {
-        if (j < 0) continue;
-        mbar_wait(wbar + 8 * (j % kStages), (uint32_t)((j / kStages) & 1));
-      }
-    }
-    __syncwarp();
-    // the last piece of the warp range
-    const bool complete = seg_first == 0 && seg_last == seg_np - 1;
-    float* slot = nseg == 1 ? wslot0 : wslot1;
-    finish_piece(p, s, seg_pair, complete, slot, g, t);
-    if (!complete && lane == 0) sinfo[warp][nseg == 1 ? 0 : 1] = SlotInfo{seg_pair, seg_first, seg_last, seg_np, seg_r};
   }
   __syncthreads();
 
