@@ -9,9 +9,9 @@
 // whose sizes differ by at most one, one per CTA, and each CTA range into kNW
 // such ranges, one per warp.
 // A warp streams its pages through a private ring of kStages shared-memory
-// stages filled by 1-D TMA bulk copies (K data 1 KiB, V data 1 KiB, K and V
-// scales 128 B each per page and head), completion counted on one mbarrier
-// per stage.  For each page it
+// stages (K data 1 KiB, V data 1 KiB, K and V scales 128 B each per page and
+// head) that all 32 lanes fill with 16-byte cp.async copies, completion
+// counted on one mbarrier per stage.  For each page it
 //   1. converts K's E2M1 pairs to f16x2 with cvt.rn.f16x2.e2m1x2, multiplies
 //      by the E4M3 block scale (exact in f16), and computes S^T = Khat q^T for
 //      the 16 tokens x G query heads with mma.sync m16n8k16 (f16 in, f32 acc);
@@ -51,9 +51,6 @@ namespace {
 #endif
 #ifndef NVFP4KV_DECODE_QK_CHAINS
 #define NVFP4KV_DECODE_QK_CHAINS 2  // independent QK accumulator chains per page (1 or 2)
-#endif
-#ifndef NVFP4KV_DECODE_STAGING
-#define NVFP4KV_DECODE_STAGING 1  // 0: 1-D TMA bulk copies issued by lane 0; 1: cp.async by all lanes
 #endif
 constexpr int kNW = NVFP4KV_DECODE_WARPS;              // warps per CTA (each streams its own pages)
 constexpr int kStages = NVFP4KV_DECODE_STAGES;         // ring stages per warp (2 pages in compute)
@@ -180,29 +177,40 @@ __device__ __forceinline__ long long cta_of(long long r, long long W, long long 
 
 // Where each item of a 32-item chunk of a warp's range lives (one per lane).
 struct ItemMap {
-  int row;     // physical row pid * hkv + h of the page-head, -1 if the page id is invalid
+  int row;     // the page id as loaded; after resolve_chunk the physical row pid * hkv + h, or -1
+  int h;       // KV head
   int pair;    // b * hkv + h, -1 past the warp's range
   int page;    // page index within the sequence
   int np;      // pages of the pair
   int lastnv;  // valid tokens in the pair's last page (1..16)
 };
 
-// Map items [i0, i0 + 32) of the warp range starting at wr0 (n items) to pages.
-// (cb, ccu) is a sequence whose first page-head is <= the chunk's first item;
-// on return it is the sequence of the chunk's last valid item.
-__device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr0, int i0, int n, int& cb,
-                                             int& ccu, int lane) {
+// The sequence a chunk walk starts from: its index, its first page (in units
+// of pages of all earlier sequences) and its clamped length.
+struct SeqCursor {
+  int b;
+  int cu;
+  int L;
+};
+
+// Map items [i0, i0 + 32) of the warp range starting at wr0 (n items) to pages
+// and start the page-table loads; resolve_chunk turns the loaded ids into rows
+// later, so the load latency is hidden behind the pages already staged.
+// `sc` is a sequence whose first page-head is <= the chunk's first item; on
+// return it is the sequence of the chunk's last valid item.
+__device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr0, int i0, int n, SeqCursor& sc,
+                                             int lane) {
   ItemMap m;
   m.row = -1;
+  m.h = 0;
   m.pair = -1;
   m.page = 0;
   m.np = 1;
   m.lastnv = kPage;
   const int i = i0 + lane;
-  int b = cb, cu = ccu;
+  int b = sc.b, cu = sc.cu, L = sc.L;
   if (i < n) {
     const long long r = wr0 + i;
-    int L = clamp_len(p, b);
     int np = (L + kPage - 1) / kPage;
     while (r >= (long long)(cu + np) * p.hkv) {
       cu += np;
@@ -213,21 +221,28 @@ __device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr
     const int local = (int)(r - (long long)cu * p.hkv);
     const int h = local / np;
     const int page = local - h * np;
+    m.h = h;
     m.pair = b * p.hkv + h;
     m.page = page;
     m.np = np;
     m.lastnv = L - (np - 1) * kPage;
-    const int pid = __ldg(p.page_table + (long long)b * p.max_pages + page);
-    if (pid >= 0 && pid < p.num_pages) {
-      m.row = pid * p.hkv + h;
-    } else {
-      flag_error(p.status, NVFP4KV_DEVERR_PAGE);
-    }
+    m.row = __ldg(p.page_table + (long long)b * p.max_pages + page);
   }
   const int last = min(31, n - 1 - i0);
-  cb = __shfl_sync(0xFFFFFFFFu, b, last);
-  ccu = __shfl_sync(0xFFFFFFFFu, cu, last);
+  sc.b = __shfl_sync(0xFFFFFFFFu, b, last);
+  sc.cu = __shfl_sync(0xFFFFFFFFu, cu, last);
+  sc.L = __shfl_sync(0xFFFFFFFFu, L, last);
   return m;
+}
+
+// Turn the loaded page ids of a chunk map into physical rows (-1 for an id out
+// of range, which is flagged); returns the valid-page bits (bit l: lane l).
+__device__ __forceinline__ uint32_t resolve_chunk(const DecodeParams& p, ItemMap& m) {
+  const bool real = m.pair >= 0;
+  const bool valid = real && m.row >= 0 && m.row < p.num_pages;
+  if (real && !valid) flag_error(p.status, NVFP4KV_DEVERR_PAGE);
+  m.row = valid ? m.row * p.hkv + m.h : -1;
+  return __ballot_sync(0xFFFFFFFFu, valid);
 }
 
 // The row (physical page-head) of item j, from the chunk map that holds it.
@@ -238,21 +253,6 @@ __device__ __forceinline__ int item_row(const ItemMap& cur, const ItemMap& nxt, 
   else
     r = __shfl_sync(0xFFFFFFFFu, nxt.row, j & 31);
   return r;
-}
-
-// Lane 0 starts the copies of one page-head (K/V data and scales) into a ring
-// stage; an invalid page (row < 0) only arrives on the barrier.
-__device__ __forceinline__ void issue_page(const DecodeParams& p, int row, uint8_t* st, uint32_t bar) {
-  if (row >= 0) {
-    const long long off = (long long)row * kPage;
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    tma_load_1d(smem_u32(st + kOffKD), p.k_data + off * kRowBytes, kPageDataBytes, bar);
-    tma_load_1d(smem_u32(st + kOffVD), p.v_data + off * kRowBytes, kPageDataBytes, bar);
-    tma_load_1d(smem_u32(st + kOffKS), p.k_scale + off * kRowScales, kPageScaleBytes, bar);
-    tma_load_1d(smem_u32(st + kOffVS), p.v_scale + off * kRowScales, kPageScaleBytes, bar);
-  } else {
-    mbar_arrive(bar);
-  }
 }
 
 // cp.async staging: each lane copies fixed 16-byte chunks of every page-head
@@ -291,10 +291,11 @@ __device__ __forceinline__ void issue_page_cpasync(const LaneCopy& c, int row, u
     cp_async16(st + kOffVD + c.off, c.vd + data_off);
     cp_async16(st + kOffVD + 512 + c.off, c.vd + data_off + 512);
     if (lane < 16) cp_async16(st + c.sc_off, c.sc + scale_off);
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-  } else {
-    mbar_arrive(bar);
   }
+  // fires once all of this lane's earlier copies have landed (also for an
+  // invalid page, which copies nothing): a stage's barrier therefore covers
+  // every stage issued before it as well
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Per-warp attention state of the current pair.
@@ -306,24 +307,37 @@ struct WarpState {
   float c0, c1;     // score multipliers of heads 2t, 2t+1
 };
 
-// Load q for pair (b, h) into B-fragments with a per-head power-of-two prescale.
-__device__ __forceinline__ void load_q(const DecodeParams& p, int pair, WarpState& s, int g, int t) {
-  const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
-  float qv[32];
+// The bf16 q elements lane (g, t) needs for pair b * hkv + h: head h * G + g,
+// elements 32t .. 32t + 31 (zeros for g >= G).  Query heads of pair P start at
+// row P * G of q, since hq = hkv * G.
+struct QRaw {
+  uint4 w[4];
+};
+
+__device__ __forceinline__ QRaw fetch_q(const DecodeParams& p, int pair, int g, int t) {
+  QRaw r;
   if (g < p.group) {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + ((long long)b * p.hq + (long long)h * p.group + g) * kHeadDim + 32 * t);
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((long long)pair * p.group + g) * kHeadDim + 32 * t);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 w = __ldg(src + j);
-      qv[8 * j + 0] = bf16_to_f32(w.x & 0xFFFFu); qv[8 * j + 1] = bf16_to_f32(w.x >> 16);
-      qv[8 * j + 2] = bf16_to_f32(w.y & 0xFFFFu); qv[8 * j + 3] = bf16_to_f32(w.y >> 16);
-      qv[8 * j + 4] = bf16_to_f32(w.z & 0xFFFFu); qv[8 * j + 5] = bf16_to_f32(w.z >> 16);
-      qv[8 * j + 6] = bf16_to_f32(w.w & 0xFFFFu); qv[8 * j + 7] = bf16_to_f32(w.w >> 16);
-    }
+    for (int j = 0; j < 4; ++j) r.w[j] = __ldg(src + j);
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) qv[j] = 0.0f;
+    for (int j = 0; j < 4; ++j) r.w[j] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  return r;
+}
+
+// Turn fetched q into B-fragments with a per-head power-of-two prescale and
+// reset the pair's softmax state.
+__device__ __forceinline__ void load_q(const DecodeParams& p, const QRaw& raw, WarpState& s, int g, int t) {
+  float qv[32];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 w = raw.w[j];
+    qv[8 * j + 0] = bf16_to_f32(w.x & 0xFFFFu); qv[8 * j + 1] = bf16_to_f32(w.x >> 16);
+    qv[8 * j + 2] = bf16_to_f32(w.y & 0xFFFFu); qv[8 * j + 3] = bf16_to_f32(w.y >> 16);
+    qv[8 * j + 4] = bf16_to_f32(w.z & 0xFFFFu); qv[8 * j + 5] = bf16_to_f32(w.z >> 16);
+    qv[8 * j + 6] = bf16_to_f32(w.w & 0xFFFFu); qv[8 * j + 7] = bf16_to_f32(w.w >> 16);
   }
   float amax = 0.0f;
 #pragma unroll
@@ -588,6 +602,13 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   const int g = lane >> 2, t = lane & 3;
 
   // ---- prologue: total work, zero outputs of empty sequences -------------------
+  {
+    // bring q into L2 early (each CTA a slice, 128-byte lines): later pieces then
+    // find their q rows there instead of queueing behind the KV stream
+    const long long lines = ((long long)p.batch * p.hq * kHeadDim * 2 + 127) / 128;
+    for (long long l = (long long)blockIdx.x * blockDim.x + tid; l < lines; l += (long long)gridDim.x * blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(p.q) + 128 * l));
+  }
   long long pages_local = 0;
   for (int b = tid; b < p.batch; b += kNW * 32) {
     const int L = clamp_len(p, b);
@@ -655,14 +676,27 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
 
   if (n > 0) {
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) mbar_init(wbar + 8 * s, NVFP4KV_DECODE_STAGING == 1 ? 32 : 1);
+      for (int s = 0; s < kStages; ++s) mbar_init(wbar + 8 * s, 32);
       fence_mbar_init();
     }
     __syncwarp();
-    int cb = wstart_b[warp], ccu = wstart_cu[warp];
-    ItemMap cur = map_chunk(p, wr0, 0, n, cb, ccu, lane);
+    SeqCursor seq;
+    seq.b = wstart_b[warp];
+    seq.cu = wstart_cu[warp];
+    seq.L = clamp_len(p, seq.b);
+    ItemMap cur = map_chunk(p, wr0, 0, n, seq, lane);
+    // the first piece's q goes out before the ring prefill, so it does not
+    // queue behind the pages
+    const QRaw q_first = fetch_q(p, __shfl_sync(0xFFFFFFFFu, cur.pair, 0), g, t);
     ItemMap nxt = cur;
-    if (n > 32) nxt = map_chunk(p, wr0, 32, n, cb, ccu, lane);
+    bool nres = true;  // nxt has been resolved (or is not used)
+    if (n > 32) {
+      nxt = map_chunk(p, wr0, 32, n, seq, lane);
+      nres = false;
+    }
+    // valid-page bits of the two chunk maps (bit l: item 32 chunk + l has a valid page)
+    uint32_t vcur = resolve_chunk(p, cur);
+    uint32_t vnxt = 0;
 
     bool ok = true;  // false after a wait gave up: stop waiting, computing and issuing
     // producer: prefill the ring (all within the first chunk: kStages < 32)
@@ -671,30 +705,27 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     const uint32_t wring_u32 = smem_u32(wring);
     for (int j = 0; j < pre; ++j) {
       const int row = __shfl_sync(0xFFFFFFFFu, cur.row, j);
-      if (NVFP4KV_DECODE_STAGING == 1)
-        issue_page_cpasync(lc, row, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
-      else if (lane == 0)
-        issue_page(p, row, wring + j * kStageBytes, wbar + 8 * j);
+      issue_page_cpasync(lc, row, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
     }
     int issued = pre;
-    // valid-page bits of the two chunk maps (bit l: item 32 chunk + l has a valid page)
-    uint32_t vcur = __ballot_sync(0xFFFFFFFFu, cur.row >= 0);
-    uint32_t vnxt = __ballot_sync(0xFFFFFFFFu, nxt.row >= 0);
     int chunk = 0;   // the chunk `cur` maps
     int st = 0;      // ring stage of the next item
     uint32_t ph = 0; // its mbarrier phase parity
     WarpState s;
+    load_q(p, q_first, s, g, t);  // the first piece's q, fetched before the prefill
     int nseg = 0;
     int i = 0;
     while (i < n) {
       // ---- one piece: items [i, iend) of one (sequence, KV head) pair -------------
       while ((i >> 5) != chunk) {
+        if (!nres) vnxt = resolve_chunk(p, nxt);
         cur = nxt;
         vcur = vnxt;
         ++chunk;
+        nres = true;
         if ((chunk + 1) * 32 < n) {
-          nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, cb, ccu, lane);
-          vnxt = __ballot_sync(0xFFFFFFFFu, nxt.row >= 0);
+          nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, seq, lane);
+          nres = false;
         }
       }
       const int li = i & 31;
@@ -705,24 +736,33 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       const int iend = min(n, i + (np - page0));
       const long long piece_r = wr0 + i;
       ++nseg;
-      load_q(p, pair, s, g, t);
+      if (nseg > 1) load_q(p, fetch_q(p, pair, g, t), s, g, t);
       for (int j = i; j < iend;) {
         if ((j >> 5) != chunk) {
+          if (!nres) vnxt = resolve_chunk(p, nxt);
           cur = nxt;
           vcur = vnxt;
           ++chunk;
+          nres = true;
           if ((chunk + 1) * 32 < n) {
-            nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, cb, ccu, lane);
-            vnxt = __ballot_sync(0xFFFFFFFFu, nxt.row >= 0);
+            nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, seq, lane);
+            nres = false;
           }
+        }
+        // the next chunk's rows are first needed at item 32 chunk + 32 - kStages - 1;
+        // resolving them half way through the chunk leaves their loads time to land
+        if (!nres && (j & 31) >= 16) {
+          vnxt = resolve_chunk(p, nxt);
+          nres = true;
         }
         const bool two = j + 1 < iend;
         const int st1 = st + 1 == kStages ? 0 : st + 1;
         const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
         if (ok) {
-          // every lane waits; the outcome is made warp-uniform before it is used
-          bool done = mbar_wait(wbar + 8 * st, ph);
-          if (two) done = mbar_wait(wbar + 8 * st1, ph1) && done;
+          // every lane waits; the outcome is made warp-uniform before it is used.
+          // The second stage's barrier fires only after each lane's earlier copies
+          // (those of the first stage) have landed too, so one wait covers both.
+          const bool done = two ? mbar_wait(wbar + 8 * st1, ph1) : mbar_wait(wbar + 8 * st, ph);
           if (!__all_sync(0xFFFFFFFFu, done)) {
             ok = false;
             if (lane == 0) flag_error(p.status, kDevErrTimeout);
@@ -745,18 +785,12 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
           const int ja = j + kStages, jb = j + 1 + kStages;
           if (ja < n) {
             const int ra = item_row(cur, nxt, ja, chunk);
-            if (NVFP4KV_DECODE_STAGING == 1)
-              issue_page_cpasync(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
-            else if (lane == 0)
-              issue_page(p, ra, wring + st * kStageBytes, wbar + 8 * st);
+            issue_page_cpasync(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
             issued = ja + 1;
           }
           if (two && jb < n) {
             const int rb = item_row(cur, nxt, jb, chunk);
-            if (NVFP4KV_DECODE_STAGING == 1)
-              issue_page_cpasync(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
-            else if (lane == 0)
-              issue_page(p, rb, wring + st1 * kStageBytes, wbar + 8 * st1);
+            issue_page_cpasync(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
             issued = jb + 1;
           }
         }
