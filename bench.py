@@ -313,7 +313,7 @@ def gpu_arm(args):
         "config": {
             "workload": wl.name, "batch": wl.batch, "ctx": int(wl.seq_lens[0]), "q_heads": wl.num_q_heads,
             "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16,
-            "step": "quantize-append of 32 new tokens + decode attention (split combine fused)",
+            "step": "quantize-append of 32 new tokens + decode attention (split-K decode + combine)",
             "l2": "flushed before every timed step (256 MiB memset, outside the step's events)",
             "parallelism": f"replicas x{world}",
         },
@@ -330,7 +330,7 @@ def gpu_arm(args):
             "kernel": "decode_kernel", "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * 2,
+        "gpu_launches": args.steps * 3,  # quantize-append, decode, split combine
         "clocks": clocks.summary(),
     }
     if not args.skip_secondary:

@@ -116,7 +116,7 @@ int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const voi
 /*
  * Bytes of device workspace nvfp4kv_decode_attention needs for this batch
  * shape on the current CUDA device (split-K partial results and per-(sequence,
- * KV head) arrival counters).  Host only; query it with the device current
+ * KV head) merge headers).  Host only; query it with the device current
  * that will run the decode.
  */
 int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
@@ -140,12 +140,15 @@ int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int
  *   seq_lens        device int32 [batch]
  *   softmax_scale   finite, > 0 (usually 1/sqrt(head_dim))
  *   workspace       device, >= nvfp4kv_decode_workspace_size() bytes, 256-byte
- *                   aligned, ZEROED before its first use; every call leaves it
- *                   zeroed again, so it can be reused without clearing.  Calls
- *                   that overlap on the GPU must not share a workspace.
+ *                   aligned; scratch that needs no initialisation (each call
+ *                   writes every byte of it that it reads).  Calls that
+ *                   overlap on the GPU must not share a workspace.
  * Requires 1 <= G <= 8.  A page id out of range is skipped (its tokens do
  * not take part) with NVFP4KV_DEVERR_PAGE; a length out of range is clamped
  * with NVFP4KV_DEVERR_LENGTH.
+ * Enqueues two kernels on `stream`: the split-K decode, then (batch > 0) a
+ * combine of the partial results of pairs the split cut, launched as a
+ * programmatic dependent of the decode.
  */
 int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* out,
                              const int32_t* page_table, int32_t max_pages_per_seq,
@@ -167,9 +170,9 @@ int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* o
  * library's device image: every GPU that loads the library holds it until the
  * process exits.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Each call clears the arrival counters it
- * needs (cudaMemsetAsync on its stream) and then runs exactly what
- * nvfp4kv_decode_attention runs.  Nothing is allocated or freed.
+ * call before any stream capture.  Each call then runs exactly what
+ * nvfp4kv_decode_attention runs, whose scratch needs no clearing between
+ * calls.  Nothing is allocated or freed.
  *
  * All calls share the one array, which keeps the last call's contents: calls
  * that overlap on the GPU (different streams, or different host threads

@@ -23,10 +23,12 @@
 //   3. transposes P (f16) with movmatrix and accumulates O^T += Vhat^T P^T,
 //      Vhat^T built from nibble-interleaved V bytes and scaled per token.
 // A (sequence, KV head) pair that lies inside one warp range is finished by
-// that warp.  Pieces of pairs cut by warp boundaries are merged in shared
-// memory; pieces cut by CTA boundaries are written to the workspace, and the
-// last CTA to arrive on the pair's counter (atomicAdd, no spinning) merges
-// them and resets the counter to 0.
+// that warp.  A piece of a pair cut by a warp boundary is written to the
+// workspace as a record (unnormalised O, running max m, sum l) and the warp
+// is done: no CTA-wide barrier or merge sits at the end of the decode, where
+// it would wait on the slowest warp and run cold code under full memory load.
+// combine_kernel, launched right behind the decode as a programmatic
+// dependent, merges each cut pair's records (the flash-decoding combine).
 //
 // Exactness: e2m1 * E4M3 has at most 6 significant bits in [2^-10, 2688], so
 // Khat and Vhat are exact in f16.  q is bf16; it is multiplied by a power of
@@ -72,9 +74,7 @@ constexpr int kOffL = kGMax * kHeadDim + kGMax;
 
 constexpr int kRingBytes = kNW * kStages * kStageBytes;
 constexpr int kBarBytes = kNW * kStages * 8;
-constexpr int kSlot0Bytes = kNW * kRecFloats * 4;
-constexpr int kSmemBytes = kRingBytes + kBarBytes + kSlot0Bytes;
-static_assert(kStages * kStageBytes >= kRecFloats * 4, "a warp's ring must hold one record");
+constexpr int kSmemBytes = kRingBytes + kBarBytes;
 
 struct DecodeParams {
   const uint8_t* k_data;
@@ -93,17 +93,10 @@ struct DecodeParams {
   int32_t group;
   float score_scale;  // softmax_scale * log2(e) * g_K
   float v_gscale;     // g_V
-  float* part;        // [num_ctas + batch * hkv] records
-  int32_t* counters;  // [batch * hkv]
+  float* part;        // [2 * num_ctas * kNW] records: warp w's first (2w) and last (2w + 1) cut piece
+  int2* hdr;          // [batch * hkv], written every call: a pair cut by warp ranges gets (record of its
+                      // first piece, last warp), any other pair (0, 0)
   int32_t* status;
-};
-
-struct SlotInfo {
-  int pair;        // b * hkv + h, or -1 for an empty slot
-  int first_page;  // pages [first_page, last_page] of the pair are merged here
-  int last_page;
-  int np;          // pages of the pair
-  long long r_first;  // global page-head index of first_page
 };
 
 // ---------------------------------------------------------------------------
@@ -162,8 +155,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 }
 
 // Balanced partition of W page-heads over N CTAs: the first W % N CTAs take
-// W / N + 1, the rest W / N, so CTAs with an empty range (W < N) all come last
-// and the CTAs that cover any pair are consecutive.
+// W / N + 1, the rest W / N.  (Weighting CTAs by their launch order on an SM,
+// whose warp scheduler favours older CTAs by about 5%, balanced the CTAs'
+// finish times but did not shorten the launch: the slowest warps are spread
+// over all SMs.)
 __device__ __forceinline__ long long cta_start(long long c, long long W, long long N) {
   const long long q = W / N, rem = W % N;
   return c * q + (c < rem ? c : rem);
@@ -173,6 +168,14 @@ __device__ __forceinline__ long long cta_start(long long c, long long W, long lo
 __device__ __forceinline__ long long cta_of(long long r, long long W, long long N) {
   const long long q = W / N, rem = W % N, big = rem * (q + 1);
   return r < big ? r / (q + 1) : rem + (r - big) / q;
+}
+
+// The global warp (CTA * kNW + warp) whose range holds page-head r: CTA c's
+// range [r0, r0 + len) gives warp w the items [r0 + len w / kNW, r0 + len (w + 1) / kNW).
+__device__ __forceinline__ int warp_of_item(long long r, long long W, long long N) {
+  const long long c = cta_of(r, W, N);
+  const long long r0 = cta_start(c, W, N), len = cta_start(c + 1, W, N) - r0;
+  return (int)(c * kNW + ((r - r0 + 1) * kNW - 1) / len);
 }
 
 // Where each item of a 32-item chunk of a warp's range lives (one per lane).
@@ -522,7 +525,7 @@ __device__ __forceinline__ void process_pages(const uint8_t* const (&stage)[NP],
 }
 
 // Finish a warp's piece of a pair: total l over the lanes, then either write
-// the final output (complete pair) or store a record into `slot` (shared).
+// the final output (complete pair) or store the piece's record at `slot`.
 __device__ __forceinline__ void finish_piece(const DecodeParams& p, WarpState& s, int pair, bool complete,
                                              float* slot, int g, int t) {
 #pragma unroll
@@ -565,13 +568,6 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, WarpState& s
   }
 }
 
-// A piece record in shared memory: slot 0 of warp w in the slot area, slot 1
-// at the start of warp w's ring (free once the warp has finished streaming).
-__device__ __forceinline__ float* slot_ptr(uint8_t* ring, float* slot0, int so) {
-  return (so & 1) ? reinterpret_cast<float*>(ring + (so >> 1) * kStages * kStageBytes)
-                  : slot0 + (so >> 1) * kRecFloats;
-}
-
 __device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int warp, int lane) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
@@ -588,18 +584,15 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
-  float* slot0 = reinterpret_cast<float*>(smem + kRingBytes + kBarBytes);
-  __shared__ SlotInfo sinfo[kNW][2];
   __shared__ long long red[kNW];
+  __shared__ long long s_W;  // total page-heads, reread by the merge
   __shared__ int wstart_b[kNW], wstart_cu[kNW];
-  __shared__ int run_first[2 * kNW], run_count[2 * kNW], slot_order[2 * kNW];
-  __shared__ int s_nruns, s_npend;
-  __shared__ float s_w[2 * kNW][kGMax], s_M[kGMax], s_L[kGMax];
-  __shared__ int s_pend_pair[2], s_pend_last[2];
-  __shared__ long long s_pend_cf[2], s_pend_cl[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
+  // the combine kernel may be scheduled now: its blocks take SMs as decode CTAs
+  // retire and wait (griddepcontrol.wait) for the whole decode grid
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // ---- prologue: total work, zero outputs of empty sequences -------------------
   {
@@ -616,9 +609,11 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
       float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
       for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int h = 0; h < p.hkv; ++h) p.hdr[(long long)b * p.hkv + h] = make_int2(0, 0);  // nothing to combine
     }
   }
   const long long W = block_sum_ll(pages_local, red, warp, lane) * p.hkv;
+  if (tid == 0) s_W = W;
   if (W == 0) return;
   const long long N = gridDim.x;
   const long long r0 = cta_start(blockIdx.x, W, N);
@@ -667,12 +662,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   const int n = (int)(wr1 - wr0);
   uint8_t* wring = ring + warp * kStages * kStageBytes;
   const uint32_t wbar = smem_u32(bars + warp * kStages);
-  float* wslot0 = slot0 + warp * kRecFloats;
-  float* wslot1 = reinterpret_cast<float*>(wring);  // the ring is free once the warp is done
-  if (lane == 0) {
-    sinfo[warp][0].pair = -1;
-    sinfo[warp][1].pair = -1;
-  }
+  const long long gwarp = (long long)blockIdx.x * kNW + warp;  // global warp index
 
   if (n > 0) {
     if (lane == 0) {
@@ -813,173 +803,86 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       }
       __syncwarp();
       // a piece that ends before the warp range does is complete unless it is the
-      // first; the last piece goes to slot 1 (the idle ring) unless it is also the first
+      // first; a cut piece becomes record 2 gwarp (the warp's first piece) or
+      // 2 gwarp + 1 (its last piece), merged later by combine_kernel
       const int last_page = page0 + (iend - i) - 1;
       const bool complete = page0 == 0 && last_page == np - 1;
       const int slot = (iend == n && nseg > 1) ? 1 : 0;
-      finish_piece(p, s, pair, complete, slot ? wslot1 : wslot0, g, t);
-      if (!complete && lane == 0) sinfo[warp][slot] = SlotInfo{pair, page0, last_page, np, piece_r};
+      finish_piece(p, s, pair, complete, p.part + (2 * gwarp + slot) * kRecFloats, g, t);
+      if (page0 == 0 && lane == 0) {
+        // the pair's first piece writes the pair's header on every call: where
+        // its pieces are if it was cut, else the no-op header (0, 0)
+        int2 hd = make_int2(0, 0);
+        if (!complete) {
+          const long long Wt = s_W, Nt = gridDim.x;
+          hd = make_int2((int)(2 * gwarp + slot), warp_of_item(piece_r + np - 1, Wt, Nt));
+        }
+        p.hdr[pair] = hd;
+      }
       i = iend;
     }
   }
-  __syncthreads();
+}
 
-  // ---- merge pieces cut by warp boundaries; hand pieces cut by CTA boundaries on
-  if (tid == 0) {
-    int nr = 0, ns = 0;
-    int prev = -2;
-    for (int w = 0; w < kNW; ++w)
-      for (int k = 0; k < 2; ++k) {
-        if (sinfo[w][k].pair < 0) continue;
-        slot_order[ns] = w * 2 + k;
-        if (sinfo[w][k].pair != prev) {
-          run_first[nr] = ns;
-          run_count[nr] = 0;
-          ++nr;
-          prev = sinfo[w][k].pair;
-        }
-        ++run_count[nr - 1];
-        ++ns;
-      }
-    s_nruns = nr;
-    s_npend = 0;
-  }
-  __syncthreads();
-  const int nruns = s_nruns;
-  // phase 1: merge each run of shared-memory pieces; complete pairs go to out,
-  // pairs cut by the CTA range become a record in the workspace (at most two:
-  // the range's first and last pair)
-  for (int rk = 0; rk < nruns; ++rk) {
-    const int f = run_first[rk], cnt = run_count[rk];
-    const SlotInfo& a = sinfo[slot_order[f] >> 1][slot_order[f] & 1];
-    const SlotInfo& z = sinfo[slot_order[f + cnt - 1] >> 1][slot_order[f + cnt - 1] & 1];
-    const int pair = a.pair;
-    const bool complete = a.first_page == 0 && z.last_page == a.np - 1;
-    if (tid < p.group) {
-      const int head = tid;
-      float M = -INFINITY;
-      for (int k = 0; k < cnt; ++k) M = fmaxf(M, slot_ptr(ring, slot0, slot_order[f + k])[kOffM + head]);
-      float L = 0.0f;
-      for (int k = 0; k < cnt; ++k) {
-        const float* sl = slot_ptr(ring, slot0, slot_order[f + k]);
-        const float w = sl[kOffM + head] == -INFINITY ? 0.0f : ex2(sl[kOffM + head] - M);
-        s_w[k][head] = w;
-        L += sl[kOffL + head] * w;
-      }
-      s_M[head] = M;
-      s_L[head] = L;
-    }
-    __syncthreads();
-    const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
-    float* rec = p.part + ((long long)blockIdx.x + pair) * kRecFloats;
-    float* dst = p.out + ((long long)b * p.hq + (long long)h * p.group) * kHeadDim;
-    for (int e4 = tid; e4 < p.group * (kHeadDim / 4); e4 += kNW * 32) {
-      const int head = e4 / (kHeadDim / 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < cnt; ++k) {
-        const float w = s_w[k][head];
-        const float4 v = reinterpret_cast<const float4*>(slot_ptr(ring, slot0, slot_order[f + k]))[e4];
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-      }
-      if (complete) {
-        const float r = s_L[head] > 0.0f ? p.v_gscale / s_L[head] : 0.0f;
-        reinterpret_cast<float4*>(dst)[e4] = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
-      } else {
-        reinterpret_cast<float4*>(rec)[e4] = acc;
-      }
-    }
-    if (!complete && tid < p.group) {
-      rec[kOffM + tid] = s_M[tid];
-      rec[kOffL + tid] = s_L[tid];
-    }
-    if (!complete && tid == 0) {
-      const long long pair_start = a.r_first - a.first_page;
-      const int k = s_npend++;
-      s_pend_pair[k] = pair;
-      s_pend_cf[k] = cta_of(pair_start, W, N);
-      s_pend_cl[k] = cta_of(pair_start + a.np - 1, W, N);
-    }
-    __syncthreads();
-  }
-  const int npend = s_npend;
-  if (npend == 0) return;
-  // phase 2: publish the records, then take a ticket per cut pair; the last
-  // CTA to arrive merges all of the pair's records (nobody waits)
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    for (int k = 0; k < npend; ++k) {
-      const int old = atomicAdd(p.counters + s_pend_pair[k], 1);
-      s_pend_last[k] = old == (int)(s_pend_cl[k] - s_pend_cf[k]);
-    }
-  }
-  __syncthreads();
-  // phase 3: merge records c = cf..cl of each pair this CTA closes; the ring is
-  // free now and holds the records' m and l, then their weights
-  float* wbuf = reinterpret_cast<float*>(ring);
-  for (int k = 0; k < npend; ++k) {
-    if (!s_pend_last[k]) continue;
-    __threadfence();
-    const int pair = s_pend_pair[k];
-    const long long cf = s_pend_cf[k];
-    const int cnt = (int)(s_pend_cl[k] - cf + 1);
-    float* lbuf = wbuf + cnt * kGMax;
-    for (int i = tid; i < cnt * p.group; i += kNW * 32) {
-      const int c = i / p.group, head = i - c * p.group;
-      const float* r = p.part + (cf + c + pair) * kRecFloats;
-      wbuf[c * kGMax + head] = __ldcg(r + kOffM + head);
-      lbuf[c * kGMax + head] = __ldcg(r + kOffL + head);
-    }
-    __syncthreads();
-    if (tid < p.group) {
-      const int head = tid;
-      float M = -INFINITY;
-      for (int c = 0; c < cnt; ++c) M = fmaxf(M, wbuf[c * kGMax + head]);
-      float L = 0.0f;
-      for (int c = 0; c < cnt; ++c) {
-        const float m = wbuf[c * kGMax + head];
-        const float w = m == -INFINITY ? 0.0f : ex2(m - M);
-        wbuf[c * kGMax + head] = w;
-        L += lbuf[c * kGMax + head] * w;
-      }
-      s_L[head] = L;
-    }
-    __syncthreads();
-    const int b = pair / p.hkv, h = pair - (pair / p.hkv) * p.hkv;
-    float* dst = p.out + ((long long)b * p.hq + (long long)h * p.group) * kHeadDim;
-    for (int e4 = tid; e4 < p.group * (kHeadDim / 4); e4 += kNW * 32) {
-      const int head = e4 / (kHeadDim / 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// Merge the records of every pair the warp ranges cut: block = (pair, query
+// head), thread = (record group, 4-column group).  Group k takes records k,
+// k + groups, ... with an online rescale (the loads of a group are
+// independent), then group 0 merges the groups' partial results.  Launched as
+// a programmatic dependent of decode_kernel: griddepcontrol.wait returns once
+// the decode grid has finished and its writes are visible.
+constexpr int kCombineMaxGroups = 16;
+
+__device__ __forceinline__ void online_merge(float& M, float& L, float4& acc, float m, float l, float4 v) {
+  const float Mn = fmaxf(M, m);
+  const float a = M == -INFINITY ? 0.0f : ex2(M - Mn);
+  const float b = m == -INFINITY ? 0.0f : ex2(m - Mn);
+  L = L * a + l * b;
+  acc.x = acc.x * a + v.x * b;
+  acc.y = acc.y * a + v.y * b;
+  acc.z = acc.z * a + v.z * b;
+  acc.w = acc.w * a + v.w * b;
+  M = Mn;
+}
+
+__global__ void __launch_bounds__(kCombineMaxGroups * 32) combine_kernel(const DecodeParams p) {
+  __shared__ float s_m[kCombineMaxGroups][32], s_l[kCombineMaxGroups][32];
+  __shared__ float4 s_o[kCombineMaxGroups][32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int pair = blockIdx.x, head = blockIdx.y;
+  const int2 h = __ldcg(p.hdr + pair);
+  const int gw_first = h.x >> 1;
+  if (h.y <= gw_first) return;  // the pair was not cut
+  const int groups = blockDim.x >> 5, grp = threadIdx.x >> 5, col = threadIdx.x & 31;
+  const int cnt = h.y - gw_first + 1;  // records: h.x, then 2 (gw_first + c) for c = 1 .. cnt - 1
+  float M = -INFINITY, L = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int c = 0; c < cnt; ++c) {
-        const float w = wbuf[c * kGMax + head];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part + (cf + c + pair) * kRecFloats) + e4);
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-      }
-      const float r = s_L[head] > 0.0f ? p.v_gscale / s_L[head] : 0.0f;
-      reinterpret_cast<float4*>(dst)[e4] = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
-    }
-    if (tid == 0) p.counters[pair] = 0;  // ready for the next call
-    __syncthreads();
+  for (int c = grp; c < cnt; c += groups) {
+    const long long ri = c == 0 ? (long long)h.x : 2LL * (gw_first + c);
+    const float* r = p.part + ri * kRecFloats;
+    const float m = __ldcg(r + kOffM + head), l = __ldcg(r + kOffL + head);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(r + head * kHeadDim) + col);
+    online_merge(M, L, acc, m, l, v);
   }
+  s_m[grp][col] = M;
+  s_l[grp][col] = L;
+  s_o[grp][col] = acc;
+  __syncthreads();
+  if (grp != 0) return;
+  for (int k = 1; k < groups; ++k) online_merge(M, L, acc, s_m[k][col], s_l[k][col], s_o[k][col]);
+  const float sc = L > 0.0f ? p.v_gscale / L : 0.0f;
+  reinterpret_cast<float4*>(p.out + ((long long)pair * p.group + head) * kHeadDim)[col] =
+      make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
 }
 
 }  // namespace
 
-// The final merge keeps m, l (then weights) of up to one record per CTA in the
-// ring: cap the grid so they always fit.
-constexpr int kMaxCtas = kRingBytes / (2 * kGMax * (int)sizeof(float));
-
-int decode_num_ctas(int num_sms) {
-  const int n = num_sms * kCtasPerSm;
-  return n < kMaxCtas ? n : kMaxCtas;
-}
+int decode_num_ctas(int num_sms) { return num_sms * kCtasPerSm; }
 
 size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads) {
-  const size_t pairs = (size_t)batch * (size_t)num_kv_heads;
-  size_t rec = ((size_t)num_ctas + pairs) * kRecFloats * sizeof(float);
+  size_t rec = 2 * (size_t)num_ctas * kNW * kRecFloats * sizeof(float);
   rec = (rec + 255) / 256 * 256;
-  return rec + pairs * sizeof(int32_t);
+  return rec + (size_t)batch * (size_t)num_kv_heads * sizeof(int2);
 }
 
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
@@ -1012,13 +915,32 @@ cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
   p.score_scale = softmax_scale * 1.4426950408889634f * c.k_global_scale;
   p.v_gscale = c.v_global_scale;
   const size_t pairs = (size_t)batch * (size_t)c.num_kv_heads;
-  size_t rec = ((size_t)num_ctas + pairs) * kRecFloats * sizeof(float);
+  size_t rec = 2 * (size_t)num_ctas * kNW * kRecFloats * sizeof(float);
   rec = (rec + 255) / 256 * 256;
   p.part = static_cast<float*>(workspace);
-  p.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + rec);
+  p.hdr = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + rec);
   p.status = device_status;
   decode_kernel<<<num_ctas, kNW * 32, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || pairs == 0) return e;
+  // the combine, as a programmatic dependent of the decode on the same stream
+  // records per cut pair are about (warps / pairs) when the sequences are
+  // alike: give each thread a handful of them
+  const long long per_pair = (2LL * num_ctas * kNW) / (long long)pairs;
+  int groups = 1;
+  while (groups < kCombineMaxGroups && groups * 4 < per_pair) groups *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pairs, (unsigned)p.group);
+  cfg.blockDim = dim3(32 * groups);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, combine_kernel, p);
+  return e;
 }
 
 }  // namespace nvfp4kv

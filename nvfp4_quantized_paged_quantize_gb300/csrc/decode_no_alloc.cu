@@ -2,7 +2,7 @@
 // allocate device memory.
 //
 // nvfp4kv_decode_attention needs a caller-provided device workspace for its
-// split-K pieces and arrival counters.  Some callers cannot provide one: code
+// split-K pieces and the per-(sequence, KV head) merge headers.  Some callers cannot provide one: code
 // running inside a host allocator hook, a plug-in loaded by a runtime that
 // owns all device memory, or a process that must never call cudaMalloc on its
 // hot path.  nvfp4kv_decode_attention_static serves them by using a fixed
@@ -12,9 +12,10 @@
 // library holds NVFP4KV_STATIC_SCRATCH_BYTES of device memory until the
 // process exits.  Its device address is looked up once per device with
 // cudaGetSymbolAddress (the host-side symbol is only a stand-in and must never
-// be handed to a kernel).  Each call clears the arrival counters it uses and
-// then runs the ordinary decode through nvfp4kv_decode_attention; nothing in
-// this file allocates or frees memory.
+// be handed to a kernel).  Each call runs the ordinary decode through
+// nvfp4kv_decode_attention, which writes every part of the workspace it later
+// reads, so the scratch needs no clearing; nothing in this file allocates or
+// frees memory.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -61,13 +62,6 @@ extern "C" int nvfp4kv_decode_attention_static(const nvfp4kv_cache* cache, const
   if (need > kScratchBytes) return NVFP4KV_ERR_WORKSPACE;  // batch too large for the fixed scratch
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != NVFP4KV_OK) return st;
-  if (batch > 0) {
-    // the arrival counters sit at the end of the workspace and must start at zero
-    const size_t counter_bytes = (size_t)batch * (size_t)cache->num_kv_heads * sizeof(int32_t);
-    const cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - counter_bytes), 0,
-                                          counter_bytes, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return NVFP4KV_ERR_CUDA;
-  }
   return nvfp4kv_decode_attention(cache, q, out, page_table, max_pages_per_seq, seq_lens, batch, num_q_heads,
                                   softmax_scale, scratch, kScratchBytes, device_status, stream);
 }

@@ -30,10 +30,11 @@ def _full_compare(wl):
     ref, rs = oracle.decode_attention(o, q, wl.page_table, wl.seq_lens, wl.softmax_scale)
     assert rs == 0
     worst = check_rows(out.cpu().numpy(), ref)
-    # the workspace counters are back to zero: a second call gives the same bits
+    # the workspace is scratch that needs no initialisation: filled with
+    # garbage, a second call gives the same bits
+    ws.fill_(0xA5)
     out2, _ = decode_gpu(wl, g, q, workspace=ws)
     assert torch.equal(out, out2)
-    assert not ws[-wl.batch * wl.num_kv_heads * 4:].any()
     return worst
 
 

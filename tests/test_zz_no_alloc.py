@@ -54,9 +54,10 @@ def test_static_scratch_matches_workspace_decode_twice(cuda_lib, index, scale):
 def test_static_scratch_rejects_a_batch_that_does_not_fit(cuda_lib):
     lib = kv.load()
     cache = kv.Cache.empty(4, 8, zero=True)
-    B, Hq = 4096, 64                 # 32768 (sequence, KV head) pairs: far more than 16 MiB of pieces
-    need = kv.nvfp4kv_decode_workspace_size(cache, B, Hq)
-    assert need > (16 << 20)
+    Hq = 8
+    B = 4096                         # grow the batch until its workspace exceeds the 16 MiB scratch
+    while kv.nvfp4kv_decode_workspace_size(cache, B, Hq) <= (16 << 20):
+        B *= 2
     q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((B, Hq, 128), dtype=torch.float32, device="cuda")
     pt = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
