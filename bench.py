@@ -327,7 +327,8 @@ def gpu_arm(args):
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved / hbm_peak, "traffic": committed_traffic(wl.name),
-            "kernel": "decode_kernel", "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+            "kernel": "decode_kernel + combine_kernel (one nvfp4kv_decode_attention call)",
+            "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * 3,  # quantize-append, decode, split combine
