@@ -4,11 +4,16 @@
 //
 //   ws[cu_prefix[b] + t][h][d] = E4M3(fp32(fp32(e2m1 * E4M3val(sb)) * g) / s_ws)
 //
-// Each thread owns 32 values (two 16-value blocks) of one (row, head) in both
-// K and V: a 16-byte data load and a 2-byte scale load per tensor, two 16-byte
-// stores per tensor.  With g = s_ws = 1 the product e2m1 * E4M3val(sb) is
-// exact in f16 and is rounded straight to E4M3 (cvt e2m1x2 -> f16x2, one
-// f16x2 multiply, cvt f16x2 -> e4m3x2); otherwise the fp32 steps are taken as
+// One warp converts one page-head (16 rows of one KV head of one sequence) of
+// K or of V: lane l loads row l / 2, values [64 (l % 2), 64 (l % 2) + 64) --
+// two 16-byte data loads and one 4-byte scale load, the warp reading the
+// page-head's 1 KiB of data contiguously -- then trades blocks with the row's
+// other lane so that each store of the pair fills a 32-byte sector.
+// The page-table lookup and the row arithmetic are done once per page-head; a
+// block takes four page-heads (K and V warps), and the grid holds every block,
+// so the block scheduler keeps each SM full of independent loads.  With g = s_ws = 1 the product e2m1 * E4M3val(sb) is exact
+// in f16 and is rounded straight to E4M3 (cvt e2m1x2 -> f16x2, one f16x2
+// multiply, cvt f16x2 -> e4m3x2); otherwise the fp32 steps are taken as
 // written.  HBM-bound: 9/16 B read and 1 B written per value.
 #include "nvfp4kv_device.cuh"
 #include "nvfp4kv_launch.h"
@@ -28,116 +33,149 @@ struct DequantParams {
   const int32_t* prefix_lens;
   const int64_t* cu_prefix;
   int32_t batch;
-  int64_t items;  // total_rows * hkv
+  int64_t total_rows;
+  int32_t chunks_per_seq;  // blocks per sequence: ceil(max_pages * hkv / kHeadsPerBlock)
   float gk, gv, sk, sv;
+  float rsk, rsv;          // RN(1 / s_ws)
+  bool sk_fast, sv_fast;   // s_ws and 1 / s_ws well inside the normal range
   uint8_t* ws_k;
   uint8_t* ws_v;
   int32_t* status;
 };
 
 constexpr int kThreads = 256;
+constexpr int kHeadsPerBlock = kThreads / 64;  // page-heads per block: a K warp and a V warp each
 
-// The sequence whose row range holds `row`: the largest b with cu[b] <= row.
-__device__ __forceinline__ int find_seq(const int64_t* cu, int batch, int64_t row) {
-  int lo = 0, hi = batch;  // invariant: cu[lo] <= row (when row >= cu[0])
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(cu + mid) <= row) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// 16 data bytes + 2 scale bytes (32 values) -> 32 E4M3 bytes, unit scales.
-__device__ __forceinline__ void convert_unit(const uint4& d, uint32_t scales2, uint4 out[2]) {
-  const uint32_t s2 = e4m3x2_to_f16x2(scales2);  // (block 0 scale, block 1 scale)
-  const uint32_t s_lo = __byte_perm(s2, 0, 0x1010);
-  const uint32_t s_hi = __byte_perm(s2, 0, 0x3232);
-  const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-  uint32_t o[8];
+// 8 data bytes (16 values of one block) -> 16 E4M3 bytes with unit scales:
+// cvt e2m1x2 -> f16x2, one f16x2 multiply by the block scale (exact), cvt
+// f16x2 -> e4m3x2 (the one rounding).
+__device__ __forceinline__ uint4 convert_block_unit(uint32_t w0, uint32_t w1, uint32_t s16x2) {
+  uint32_t o[4];
+  const uint32_t w[2] = {w0, w1};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t s = j < 2 ? s_lo : s_hi;
-    const uint32_t b0 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<0>(w[j]), s));
-    const uint32_t b1 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<1>(w[j]), s));
-    const uint32_t b2 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<2>(w[j]), s));
-    const uint32_t b3 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<3>(w[j]), s));
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t b0 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<0>(w[j]), s16x2));
+    const uint32_t b1 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<1>(w[j]), s16x2));
+    const uint32_t b2 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<2>(w[j]), s16x2));
+    const uint32_t b3 = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<3>(w[j]), s16x2));
     o[2 * j] = b0 | (b1 << 16);
     o[2 * j + 1] = b2 | (b3 << 16);
   }
-  out[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// fp32(fp32(v * g) / sws) rounded to E4M3, for the two halves of an exact f16x2 product.
 template <int K>
-__device__ __forceinline__ uint32_t convert_pair_general(uint32_t w, uint32_t s, float g, float sws) {
-  const uint32_t h2 = hmul2(e2m1x2_to_f16x2<K>(w), s);  // exact e2m1 * E4M3val(sb)
-  const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-  const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-  const float z0 = __fdiv_rn(__fmul_rn(v0, g), sws);
-  const float z1 = __fdiv_rn(__fmul_rn(v1, g), sws);
+__device__ __forceinline__ uint32_t convert_pair_general(uint32_t w, uint32_t s16x2, float g, float sws, float rs,
+                                                         bool fast) {
+  const uint32_t h2 = hmul2(e2m1x2_to_f16x2<K>(w), s16x2);  // exact e2m1 * E4M3val(sb)
+  const float a0 = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), g);
+  const float a1 = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), g);
+  float z0, z1;
+  if (fast && fabsf(a0) < 0x1p+64f && fabsf(a1) < 0x1p+64f) {
+    // correctly rounded a / sws (Markstein); the sign of a zero quotient is the sign of a
+    z0 = copysignf(__fmaf_rn(__fmaf_rn(-__fmul_rn(a0, rs), sws, a0), rs, __fmul_rn(a0, rs)), a0);
+    z1 = copysignf(__fmaf_rn(__fmaf_rn(-__fmul_rn(a1, rs), sws, a1), rs, __fmul_rn(a1, rs)), a1);
+  } else {
+    z0 = __fdiv_rn(a0, sws);
+    z1 = __fdiv_rn(a1, sws);
+  }
   return e4m3x2_from_f32(z0, z1);
 }
 
-// Same, any global scale g and workspace scale s_ws.
-__device__ __forceinline__ void convert_general(const uint4& d, uint32_t scales2, float g, float sws,
-                                                uint4 out[2]) {
-  const uint32_t s2 = e4m3x2_to_f16x2(scales2);
-  const uint32_t s_lo = __byte_perm(s2, 0, 0x1010);
-  const uint32_t s_hi = __byte_perm(s2, 0, 0x3232);
-  const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-  uint32_t o[8];
+__device__ __forceinline__ uint4 convert_block_general(uint32_t w0, uint32_t w1, uint32_t s16x2, float g, float sws,
+                                                       float rs, bool fast) {
+  uint32_t o[4];
+  const uint32_t w[2] = {w0, w1};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t s = j < 2 ? s_lo : s_hi;
-    o[2 * j] = convert_pair_general<0>(w[j], s, g, sws) | (convert_pair_general<1>(w[j], s, g, sws) << 16);
-    o[2 * j + 1] = convert_pair_general<2>(w[j], s, g, sws) | (convert_pair_general<3>(w[j], s, g, sws) << 16);
+  for (int j = 0; j < 2; ++j) {
+    o[2 * j] = convert_pair_general<0>(w[j], s16x2, g, sws, rs, fast) |
+               (convert_pair_general<1>(w[j], s16x2, g, sws, rs, fast) << 16);
+    o[2 * j + 1] = convert_pair_general<2>(w[j], s16x2, g, sws, rs, fast) |
+                   (convert_pair_general<3>(w[j], s16x2, g, sws, rs, fast) << 16);
   }
-  out[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 32 data bytes + 4 scale bytes (64 values, 4 blocks) -> 64 E4M3 bytes.
 template <bool kUnit>
-__global__ void __launch_bounds__(kThreads) dequant_fp8_kernel(DequantParams p) {
-  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  const int64_t total = p.items * 4;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += nthreads) {
-    const int64_t item = idx >> 2;
-    const int q = (int)(idx & 3);  // values [32 q, 32 q + 32)
-    const int64_t row = item / p.hkv;
-    const int h = (int)(item - row * p.hkv);
-    if (row < __ldg(p.cu_prefix)) continue;
-    const int b = find_seq(p.cu_prefix, p.batch, row);
-    const int64_t t = row - __ldg(p.cu_prefix + b);
+__device__ __forceinline__ void convert_half_row(const uint4& d0, const uint4& d1, uint32_t sc4, float g, float sws,
+                                                 float rs, bool fast, uint4 out[4]) {
+  const uint32_t s01 = e4m3x2_to_f16x2(sc4 & 0xFFFFu);  // (block 0, block 1) scales as f16
+  const uint32_t s23 = e4m3x2_to_f16x2(sc4 >> 16);
+  const uint32_t sc[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
+                          __byte_perm(s23, 0, 0x3232)};
+  const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (kUnit)
+      out[k] = convert_block_unit(w[2 * k], w[2 * k + 1], sc[k]);
+    else
+      out[k] = convert_block_general(w[2 * k], w[2 * k + 1], sc[k], g, sws, rs, fast);
+  }
+}
+
+// Unit scales fit 32 registers (full occupancy); the general path keeps 40.
+template <bool kUnit>
+__global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(DequantParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tensor = warp & 1;  // 0: K, 1: V
+  const int r = lane >> 1, half = lane & 1;
+  const uint8_t* data = tensor ? p.v_data : p.k_data;
+  const uint8_t* scale = tensor ? p.v_scale : p.k_scale;
+  uint8_t* ws = tensor ? p.ws_v : p.ws_k;
+  const float g = tensor ? p.gv : p.gk, sws = tensor ? p.sv : p.sk, rs = tensor ? p.rsv : p.rsk;
+  const bool fast = tensor ? p.sv_fast : p.sk_fast;
+  const int64_t units = (int64_t)p.batch * p.chunks_per_seq;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int b = (int)(u / p.chunks_per_seq);
+    const int ph = (int)(u - (int64_t)b * p.chunks_per_seq) * kHeadsPerBlock + (warp >> 1);  // page * hkv + h
+    const int pg = ph / p.hkv, h = ph - pg * p.hkv;
+    if (pg >= p.max_pages) continue;
+    // the page id, the length and the row base are loaded together
+    const int32_t page = __ldg(p.page_table + (int64_t)b * p.max_pages + pg);
     int32_t L = __ldg(p.prefix_lens + b);
+    const int64_t base = __ldg(p.cu_prefix + b);
     if (L < 0 || L > p.max_pages * kPage) {
-      flag_error(p.status, NVFP4KV_DEVERR_LENGTH);
+      if (lane == 0 && ph == 0 && tensor == 0) flag_error(p.status, NVFP4KV_DEVERR_LENGTH);
       L = L < 0 ? 0 : p.max_pages * kPage;
     }
-    if (t >= L) continue;  // a row between this prefix and the next sequence
-    const int32_t page = __ldg(p.page_table + (int64_t)b * p.max_pages + (t >> 4));
-    uint4* dst_k = reinterpret_cast<uint4*>(p.ws_k + (item * kHeadDim + 32 * q));
-    uint4* dst_v = reinterpret_cast<uint4*>(p.ws_v + (item * kHeadDim + 32 * q));
-    if (page < 0 || page >= p.num_pages) {
-      flag_error(p.status, NVFP4KV_DEVERR_PAGE);
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      dst_k[0] = z; dst_k[1] = z; dst_v[0] = z; dst_v[1] = z;
+    if (pg * kPage >= L) continue;  // a page past this prefix
+    const bool page_ok = page >= 0 && page < p.num_pages;
+    const int64_t src_row = ((int64_t)(page_ok ? page : 0) * p.hkv + h) * kPage + r;
+    const uint4* src = reinterpret_cast<const uint4*>(data + src_row * kRowBytes) + 2 * half;
+    const uint4 d0 = __ldg(src), d1 = __ldg(src + 1);  // blocks 4 half .. 4 half + 3
+    const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(scale + src_row * kRowScales) + half);
+    const int t = pg * kPage + r;   // this lane's token of the prefix
+    const int64_t orow = base + t;  // its workspace row
+    const bool live = t < L && orow >= 0 && orow < p.total_rows;
+    // 16-byte output chunk k of this lane goes to block 2k + half of the row, so the
+    // two lanes of a row fill whole 32-byte sectors with each store
+    uint4* dst = reinterpret_cast<uint4*>(ws + (orow * p.hkv + h) * kHeadDim) + half;
+    if (!page_ok) {
+      if (lane == 0 && tensor == 0) flag_error(p.status, NVFP4KV_DEVERR_PAGE);
+      if (live) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[2 * k] = z;
+      }
       continue;
     }
-    const int64_t src_row = ((int64_t)page * p.hkv + h) * kPage + (t & (kPage - 1));
-    const uint4 kd = __ldg(reinterpret_cast<const uint4*>(p.k_data + src_row * kRowBytes) + q);
-    const uint4 vd = __ldg(reinterpret_cast<const uint4*>(p.v_data + src_row * kRowBytes) + q);
-    const uint32_t ks = __ldg(reinterpret_cast<const uint16_t*>(p.k_scale + src_row * kRowScales) + q);
-    const uint32_t vs = __ldg(reinterpret_cast<const uint16_t*>(p.v_scale + src_row * kRowScales) + q);
-    uint4 ok[2], ov[2];
-    if constexpr (kUnit) {
-      convert_unit(kd, ks, ok);
-      convert_unit(vd, vs, ov);
-    } else {
-      convert_general(kd, ks, p.gk, p.sk, ok);
-      convert_general(vd, vs, p.gv, p.sv, ov);
-    }
-    dst_k[0] = ok[0]; dst_k[1] = ok[1];
-    dst_v[0] = ov[0]; dst_v[1] = ov[1];
+    // trade blocks with the row's other lane: half 0 ends up with blocks 0, 2, 4, 6
+    // and half 1 with blocks 1, 3, 5, 7 (8 data bytes and 1 scale byte per block)
+    const uint32_t x0 = __shfl_xor_sync(0xFFFFFFFFu, half ? d0.x : d0.z, 1);
+    const uint32_t x1 = __shfl_xor_sync(0xFFFFFFFFu, half ? d0.y : d0.w, 1);
+    const uint32_t x2 = __shfl_xor_sync(0xFFFFFFFFu, half ? d1.x : d1.z, 1);
+    const uint32_t x3 = __shfl_xor_sync(0xFFFFFFFFu, half ? d1.y : d1.w, 1);
+    const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, sc4, 1);
+    const uint4 e0 = half ? make_uint4(x0, x1, x2, x3) : make_uint4(d0.x, d0.y, d1.x, d1.y);
+    const uint4 e1 = half ? make_uint4(d0.z, d0.w, d1.z, d1.w) : make_uint4(x0, x1, x2, x3);
+    const uint32_t esc = __byte_perm(sc4, other, half ? 0x3175 : 0x6420);
+    if (!live) continue;
+    uint4 o[4];
+    convert_half_row<kUnit>(e0, e1, esc, g, sws, rs, fast, o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[2 * k] = o[k];
   }
 }
 
@@ -159,18 +197,22 @@ cudaError_t launch_dequant_fp8(const nvfp4kv_cache& c, const int32_t* page_table
   p.prefix_lens = prefix_lens;
   p.cu_prefix = cu_prefix;
   p.batch = batch;
-  p.items = total_rows * c.num_kv_heads;
+  p.total_rows = total_rows;
+  p.chunks_per_seq = (int32_t)(((int64_t)max_pages * c.num_kv_heads + kHeadsPerBlock - 1) / kHeadsPerBlock);
   p.gk = c.k_global_scale;
   p.gv = c.v_global_scale;
   p.sk = k_ws_scale;
   p.sv = v_ws_scale;
+  p.rsk = 1.0f / k_ws_scale;  // host IEEE division: RN(1 / s_ws)
+  p.rsv = 1.0f / v_ws_scale;
+  p.sk_fast = k_ws_scale >= 0x1p-100f && k_ws_scale <= 0x1p+100f;
+  p.sv_fast = v_ws_scale >= 0x1p-100f && v_ws_scale <= 0x1p+100f;
   p.ws_k = ws_k;
   p.ws_v = ws_v;
   p.status = device_status;
-  const int64_t threads_needed = p.items * 4;
-  int64_t blocks = (threads_needed + kThreads - 1) / kThreads;
-  const int64_t max_blocks = (int64_t)num_sms * (2048 / kThreads);
-  if (blocks > max_blocks) blocks = max_blocks;
+  const int64_t units = (int64_t)batch * p.chunks_per_seq;
+  int64_t blocks = units;  // one unit per block: the block scheduler overlaps them
+  if (blocks > (1LL << 30)) blocks = 1LL << 30;
   if (blocks < 1) blocks = 1;
   const bool unit = c.k_global_scale == 1.0f && c.v_global_scale == 1.0f && k_ws_scale == 1.0f &&
                     v_ws_scale == 1.0f;

@@ -2,13 +2,14 @@
 // paged cache ("nvfp4-kv-cache-memory-wall", section 3: new K/V are quantised
 // to NVFP4 on the way into the cache; section 2: two-level scaling).
 //
-// One warp handles one (token, KV head) row of K (lanes 0-15) and of V (lanes
-// 16-31) per step; each lane owns 8 consecutive values (one 16-byte load), two
-// lanes form a 16-value block.  Per block:
+// One lane quantises one 16-value block (two 16-byte loads): a warp takes two
+// (token, KV head) rows of K (lanes 0-7 and 8-15) and the same two rows of V
+// (lanes 16-23 and 24-31) per step, so the per-block work (amax, the scale's
+// division, the reciprocal) is done once per block.  Per block:
 //   amax = max |x|                       (exact; inputs are bf16)
-//   sb   = E4M3(amax / (6 g))            (IEEE division, RNE, saturating)
+//   sb   = E4M3(amax / (6 g))            (correctly rounded quotient, RNE, saturating)
 //   den  = E4M3val(sb) * g
-//   code = E2M1(x / den)                 (x / den rounded to nearest, RNE, saturating)
+//   code = E2M1(x / den)                 (correctly rounded quotient, RNE, saturating)
 // A block with den == 0 stores signed zeros.  The row's 64 data bytes and 8
 // scale bytes go to slot slot_mapping[token].  HBM-bound: 2 B read and 9/16 B
 // written per value.
@@ -34,87 +35,110 @@ struct QuantParams {
 };
 
 constexpr int kThreads = 256;
-constexpr int kRowsPerStep = 2;  // rows whose loads are in flight together per warp
+constexpr int kRowsPerWarp = 2;  // (token, head) rows of K and of V per warp and step
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& x, float f[8]) {
+__device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
   f[0] = bf16_to_f32(x.x & 0xFFFFu); f[1] = bf16_to_f32(x.x >> 16);
   f[2] = bf16_to_f32(x.y & 0xFFFFu); f[3] = bf16_to_f32(x.y >> 16);
   f[4] = bf16_to_f32(x.z & 0xFFFFu); f[5] = bf16_to_f32(x.z >> 16);
   f[6] = bf16_to_f32(x.w & 0xFFFFu); f[7] = bf16_to_f32(x.w >> 16);
 }
 
+// Correctly rounded a / b from r = RN(1 / b): q0 = RN(a r), then Markstein's
+// correction RN(q0 + r RN(a - b q0)) (two FMAs).  Valid while b, 1 / b and
+// the quotient stay well inside the normal range; the caller checks.
+__device__ __forceinline__ float div_markstein(float a, float b, float r) {
+  const float q0 = __fmul_rn(a, r);
+  const float rem = __fmaf_rn(-q0, b, a);
+  return __fmaf_rn(rem, r, q0);
+}
+
 __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p) {
   const int lane = threadIdx.x & 31;
   const int tensor = lane >> 4;  // 0: K, 1: V
-  const int sub = lane & 15;     // values [8 sub, 8 sub + 8) of the row
+  const int sub = lane & 7;      // block j = sub of the row: values [16 j, 16 j + 16)
+  const int which = (lane >> 3) & 1;  // first or second row of the step
   const uint16_t* src = tensor ? p.v : p.k;
   uint8_t* data = tensor ? p.v_data : p.k_data;
   uint8_t* scale = tensor ? p.v_scale : p.k_scale;
   const float g = tensor ? p.gv : p.gk;
   const float t6 = __fmul_rn(6.0f, g);  // the block amax maps onto E2M1's 6
+  const float r6 = __frcp_rn(t6);
+  const bool t6_ok = t6 >= 0x1p-100f && t6 <= 0x1p+100f;  // t6 and 1/t6 well inside the normal range
   const int warp = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
   const int nwarps = (int)((gridDim.x * (unsigned)blockDim.x) >> 5);
 
-  for (int r0 = warp * kRowsPerStep; r0 < p.rows; r0 += nwarps * kRowsPerStep) {
-    uint4 x[kRowsPerStep];
-    int64_t slot[kRowsPerStep];
-#pragma unroll
-    for (int u = 0; u < kRowsPerStep; ++u) {
-      const int r = r0 + u;
-      slot[u] = -1;
-      if (r < p.rows) {
-        slot[u] = __ldg(p.slots + r / p.hkv);
-        x[u] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * kHeadDim) + sub);
-      }
+  // software pipeline: the next step's row (two 16-byte loads and its slot) is
+  // in flight while this step's block is quantised
+  const int64_t stride = (int64_t)nwarps * kRowsPerWarp;
+  int64_t r = (int64_t)warp * kRowsPerWarp + which;
+  uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+  int64_t slot = -1;
+  if (r < p.rows) {
+    const uint4* xs = reinterpret_cast<const uint4*>(src + (int64_t)r * kHeadDim) + 2 * sub;
+    xa = __ldg(xs);
+    xb = __ldg(xs + 1);
+    slot = __ldg(p.slots + (int)r / p.hkv);  // r < rows < 2^31
+  }
+  for (; r < p.rows; r += stride) {
+    const int64_t rn = r + stride;
+    uint4 na = make_uint4(0, 0, 0, 0), nb = na;
+    int64_t nslot = -1;
+    if (rn < p.rows) {
+      const uint4* xs = reinterpret_cast<const uint4*>(src + (int64_t)rn * kHeadDim) + 2 * sub;
+      na = __ldg(xs);
+      nb = __ldg(xs + 1);
+      nslot = __ldg(p.slots + (int)rn / p.hkv);
     }
+    const uint4 ca = xa, cb = xb;
+    const int64_t cslot = slot;
+    xa = na;
+    xb = nb;
+    slot = nslot;
+    if (cslot < 0) continue;  // padding
+    if (cslot >= p.capacity) {
+      flag_error(p.status, NVFP4KV_DEVERR_SLOT);
+      continue;
+    }
+    const int h = (int)r % p.hkv;
+    const int64_t row = ((cslot >> 4) * p.hkv + h) * kPage + (cslot & (kPage - 1));
+    float f[16];
+    unpack_bf16x8(ca, f);
+    unpack_bf16x8(cb, f + 8);
+    float amax = 0.0f;
 #pragma unroll
-    for (int u = 0; u < kRowsPerStep; ++u) {
-      const int r = r0 + u;
-      // slot[u] and r are the same in every lane: the branches are warp-uniform
-      if (r >= p.rows || slot[u] < 0) continue;
-      if (slot[u] >= p.capacity) {
-        if (lane == 0) flag_error(p.status, NVFP4KV_DEVERR_SLOT);
-        continue;
-      }
-      const int h = r % p.hkv;
-      const int64_t row = ((slot[u] >> 4) * p.hkv + h) * kPage + (slot[u] & (kPage - 1));
-      float f[8];
-      unpack_bf16x8(x[u], f);
-      float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    // the block scale's quotient: Markstein while the first product stays far
+    // from overflow (a quotient below 2^-11 encodes as 0 either way)
+    const float sq = (t6_ok && __fmul_rn(amax, r6) < 0x1p+64f) ? div_markstein(amax, t6, r6) : __fdiv_rn(amax, t6);
+    const uint32_t sb = e4m3_from_f32(sq);
+    const float den = __fmul_rn(e4m3_to_f32(sb), g);
+    uint32_t lo = 0, hi = 0;
+    if (den == 0.0f) {
+      // signed zeros: code 8 for negative inputs
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      const uint32_t sb = e4m3_from_f32(__fdiv_rn(amax, t6));
-      const float den = __fmul_rn(e4m3_to_f32(sb), g);
-      // x / den rounded to nearest: one correctly rounded reciprocal per block,
-      // then per value q0 = x*r and Markstein's correction q0 + r*(x - den*q0)
-      // (two FMAs), which gives the correctly rounded quotient while den, 1/den
-      // and every quotient of the block stay well inside the normal range (a
-      // saturated block scale can push quotients towards overflow); otherwise
-      // IEEE division.
+      for (int i = 0; i < 8; ++i) lo |= (__float_as_uint(f[i]) >> 31) << (4 * i + 3);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hi |= (__float_as_uint(f[8 + i]) >> 31) << (4 * i + 3);
+    } else {
       const float rcp = __frcp_rn(den);
-      const bool fast = den >= 0x1p-100f && den <= 0x1p+100f && __fmul_rn(amax, rcp) < 0x1p+64f;
-      float y[8];
+      float y[16];
+      if (den >= 0x1p-100f && den <= 0x1p+100f && __fmul_rn(amax, rcp) < 0x1p+64f) {
+        // a quotient that rounds to zero can come out as +0 for negative x;
+        // the sign of x / den is the sign of x (den > 0)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (den == 0.0f) {
-          y[i] = copysignf(0.0f, f[i]);
-        } else if (fast) {
-          const float q0 = __fmul_rn(f[i], rcp);
-          const float rem = __fmaf_rn(-q0, den, f[i]);
-          // a quotient that rounds to zero can come out as +0 for negative x;
-          // the sign of x / den is the sign of x (den > 0)
-          y[i] = copysignf(__fmaf_rn(rem, rcp, q0), f[i]);
-        } else {
-          y[i] = __fdiv_rn(f[i], den);
-        }
+        for (int i = 0; i < 16; ++i) y[i] = copysignf(div_markstein(f[i], den, rcp), f[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = __fdiv_rn(f[i], den);
       }
-      uint32_t packed = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) packed |= e2m1x2_from_f32(y[2 * k], y[2 * k + 1]) << (8 * k);
-      reinterpret_cast<uint32_t*>(data + row * kRowBytes)[sub] = packed;
-      if ((sub & 1) == 0) scale[row * kRowScales + (sub >> 1)] = (uint8_t)sb;
+      for (int k = 0; k < 4; ++k) lo |= e2m1x2_from_f32(y[2 * k], y[2 * k + 1]) << (8 * k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) hi |= e2m1x2_from_f32(y[8 + 2 * k], y[8 + 2 * k + 1]) << (8 * k);
     }
+    reinterpret_cast<uint2*>(data + row * kRowBytes)[sub] = make_uint2(lo, hi);
+    scale[row * kRowScales + sub] = (uint8_t)sb;
   }
 }
 
@@ -137,10 +161,19 @@ cudaError_t launch_quantize_append(const nvfp4kv_cache& c, const uint16_t* k, co
   p.gk = c.k_global_scale;
   p.gv = c.v_global_scale;
   p.status = device_status;
-  const int warps_needed = (p.rows + kRowsPerStep - 1) / kRowsPerStep;
+  const int warps_needed = (p.rows + kRowsPerWarp - 1) / kRowsPerWarp;
   const int warps_per_block = kThreads / 32;
   int blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
-  const int max_blocks = num_sms * (2048 / kThreads);
+  // a persistent grid: as many blocks as fit on the device at once (more
+  // blocks, each doing less, measured slower)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_append_kernel, kThreads, 0) != cudaSuccess || n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  const int max_blocks = num_sms * per_sm;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   quantize_append_kernel<<<blocks, kThreads, 0, stream>>>(p);

@@ -112,3 +112,36 @@ def test_full_size_layer_sampled_rows(cuda_lib):
         np.testing.assert_array_equal(wk[r0:r0 + wl.prefix_len], ek)
         np.testing.assert_array_equal(wv[r0:r0 + wl.prefix_len], ev)
         assert np.all(wk[r0 + wl.prefix_len:int(wl.cu_prefix[b + 1])] == CANARY)
+
+
+@pytest.mark.parametrize("gk,gv,sk,sv", [(1.0, 1.0, 1.0, 1.0), (0.37, 2.5, 6.0, 1e-3), (1e30, 1e-20, 1e-10, 1e31),
+                                         (1.0, 3.0, 1e-35, 1e35), (1 / 2688, 2.9e-3, 6 / 2688, 6 * 2.9e-3)])
+def test_every_code_and_scale_bit_exact(cuda_lib, gk, gv, sk, sv):
+    # One KV head, two pages: block j of row r holds scale byte 8 r + j (every
+    # non-negative, non-NaN E4M3 byte once per page) and the 16 E2M1 codes
+    # 0..15, in order for K and reversed for V.  Workspace scales inside and
+    # outside [2^-100, 2^100] take the kernel's reciprocal path and its
+    # IEEE-division fallback; (1, 1) takes the unit-scale path.
+    sc = np.zeros((2, 16, 8), np.uint8)
+    sc[:] = np.minimum(np.arange(128, dtype=np.uint8), 0x7E).reshape(16, 8)
+    sc[1] = sc[1][::-1]
+    fwd = np.array([0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE], np.uint8)
+    rev = np.array([0xEF, 0xCD, 0xAB, 0x89, 0x67, 0x45, 0x23, 0x01], np.uint8)
+    kd = np.tile(fwd, (2, 16, 8))
+    vd = np.tile(rev, (2, 16, 8))
+    g = gpu_cache(2, 1, gk, gv)
+    g.k_data.copy_(torch.from_numpy(kd.reshape(2, 1, 16, 64)))
+    g.v_data.copy_(torch.from_numpy(vd.reshape(2, 1, 16, 64)))
+    g.k_scale.copy_(torch.from_numpy(sc.reshape(2, 1, 16, 8)))
+    g.v_scale.copy_(torch.from_numpy(sc[::-1].copy().reshape(2, 1, 16, 8)))
+    o = oracle.Cache(2, 1, 128, 16, gk, gv, arrays=(kd, vd, sc, sc[::-1].copy()))
+    pt = np.array([[1, 0]], np.int32)
+    pl = np.array([32], np.int32)
+    cu = np.array([0, 32], np.int64)
+    ws = (torch.full((32, 1, 128), CANARY, dtype=torch.uint8, device="cuda"),
+          torch.full((32, 1, 128), CANARY, dtype=torch.uint8, device="cuda"))
+    kv.nvfp4kv_dequant_to_fp8_workspace(g, dev(pt), dev(pl), dev(cu), ws[0], ws[1], sk, sv)
+    ek, ev, st = oracle.dequant_to_fp8_workspace(o, pt, pl, cu, 32, sk, sv)
+    assert st == 0
+    np.testing.assert_array_equal(ws[0].cpu().numpy(), ek)
+    np.testing.assert_array_equal(ws[1].cpu().numpy(), ev)

@@ -160,3 +160,29 @@ def test_random_blocks_wide_scale_range_bit_exact(cuda_lib):
             o = oracle.Cache(pages, 1, 128, 16, gk, gv)
             assert oracle.quantize_append(o, kb, vb, slots) == 0
             _assert_pool_equal(g, o)
+
+
+@pytest.mark.parametrize("gk,gv", [(1.0, 0.37), (1 / 2688, 2.9e-3), (5e-31, 1e25), (1e-35, 1e35)])
+def test_every_bf16_block_amax_bit_exact(cuda_lib, gk, gv):
+    # The block scale is E4M3(amax / (6 g)): every finite positive bf16 value
+    # is the amax of one block, once for K and once for V, at global scales
+    # whose 6 g lies inside and outside [2^-100, 2^100] (the kernel's fast
+    # reciprocal path and its IEEE-division fallback).  The other 15 values of
+    # a block are drawn at or below the amax, with random signs.
+    rng = np.random.default_rng(17)
+    amax = inputs.bf16_bits_to_f32(np.arange(1, 0x7F80, dtype=np.uint16))
+    frac = rng.random((amax.size, 15)).astype(np.float32)
+    sign = np.where(rng.random((amax.size, 15)) < 0.5, -1.0, 1.0).astype(np.float32)
+    blocks = np.concatenate([amax[:, None], amax[:, None] * frac * sign], axis=1)
+    n = (blocks.shape[0] + 7) // 8
+    flat = np.zeros((n * 8, 16), np.float32)
+    flat[:blocks.shape[0]] = blocks
+    kb = inputs.bf16_bits(flat.reshape(n, 1, 128))
+    vb = inputs.bf16_bits(flat[::-1].copy().reshape(n, 1, 128))
+    slots = np.arange(n, dtype=np.int64)
+    pages = (n + 15) // 16
+    g = gpu_cache(pages, 1, gk, gv)
+    gpu_append(g, kb, vb, slots)
+    o = oracle.Cache(pages, 1, 128, 16, gk, gv)
+    oracle.quantize_append(o, kb, vb, slots)
+    _assert_pool_equal(g, o)
