@@ -77,6 +77,24 @@ def dist_info():
     return world, rank, local
 
 
+def world_max(torch, value, device):
+    """The largest of one float over all ranks (the value itself without an
+    initialised process group).  Replicas are timed separately; the slowest
+    rank's total is the job's time."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank_step, steps, total_ms):
+    """Whole-job units/s: every rank processed units_per_rank_step per step."""
+    return world * units_per_rank_step * steps / (total_ms / 1e3)
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled while the timed region runs
 # ---------------------------------------------------------------------------
@@ -254,13 +272,9 @@ def gpu_arm(args):
     with ClockSampler(local) as clocks:
         step_ms, dec_ms = time_steps(torch, args.steps, args.warmup, step, flush, split=True)
     torch.cuda.synchronize()
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = world_max(torch, float(sum(step_ms)), "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * kv_tokens * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, kv_tokens, args.steps, total_ms)
     dec_avg_ms = float(np.mean(dec_ms))
     achieved = alg_bytes / (dec_avg_ms / 1e3) / 1e9
 
@@ -289,12 +303,8 @@ def gpu_arm(args):
 
     e2e_steps = max(3, min(args.steps, 200))
     e2e_ms, _ = time_steps(torch, e2e_steps, args.warmup, e2e_step, flush)
-    e2e_total = float(sum(e2e_ms))
-    if world > 1:
-        t = torch.tensor([e2e_total], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * kv_tokens * e2e_steps / (e2e_total / 1e3)
+    e2e_total = world_max(torch, float(sum(e2e_ms)), "cuda")
+    e2e_value = job_throughput(world, kv_tokens, e2e_steps, e2e_total)
     del bench
 
     line = {
