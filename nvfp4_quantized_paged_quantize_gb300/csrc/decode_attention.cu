@@ -596,33 +596,81 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
 
   // ---- prologue: total work, zero outputs of empty sequences -------------------
   {
-    // bring q into L2 early (each CTA a slice, 128-byte lines): later pieces then
-    // find their q rows there instead of queueing behind the KV stream
-    const long long lines = ((long long)p.batch * p.hq * kHeadDim * 2 + 127) / 128;
-    for (long long l = (long long)blockIdx.x * blockDim.x + tid; l < lines; l += (long long)gridDim.x * blockDim.x)
+    // bring q and the page table into L2 early (each CTA a slice, 128-byte
+    // lines): the first chunk maps and later pieces then find them there
+    // instead of queueing behind the KV stream
+    const long long step = (long long)gridDim.x * blockDim.x, first = (long long)blockIdx.x * blockDim.x + tid;
+    const long long qlines = ((long long)p.batch * p.hq * kHeadDim * 2 + 127) / 128;
+    for (long long l = first; l < qlines; l += step)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(p.q) + 128 * l));
+    const long long plines = ((long long)p.batch * p.max_pages * 4 + 127) / 128;
+    for (long long l = first; l < plines; l += step)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(p.page_table) + 128 * l));
   }
-  long long pages_local = 0;
-  for (int b = tid; b < p.batch; b += kNW * 32) {
-    const int L = clamp_len(p, b);
-    pages_local += (L + kPage - 1) / kPage;
-    if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
-      float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
-      for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int h = 0; h < p.hkv; ++h) p.hdr[(long long)b * p.hkv + h] = make_int2(0, 0);  // nothing to combine
-    }
-  }
-  const long long W = block_sum_ll(pages_local, red, warp, lane) * p.hkv;
-  if (tid == 0) s_W = W;
-  if (W == 0) return;
+  long long W = 0;
+  long long r0 = 0, r1 = 0;
   const long long N = gridDim.x;
-  const long long r0 = cta_start(blockIdx.x, W, N);
-  const long long r1 = cta_start((long long)blockIdx.x + 1, W, N);
+  if (p.batch <= kNW * 32) {
+    // one pass: every sequence's length is read once, by thread b
+    const int b = tid;
+    int np = 0;
+    if (b < p.batch) {
+      const int L = clamp_len(p, b);
+      np = (L + kPage - 1) / kPage;
+      if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
+        float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
+        for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int h = 0; h < p.hkv; ++h) p.hdr[(long long)b * p.hkv + h] = make_int2(0, 0);  // nothing to combine
+      }
+    }
+    int incl = np;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    long long before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) {
+      if (w < warp) before += red[w];
+      total += red[w];
+    }
+    W = total * p.hkv;
+    if (W == 0) return;
+    r0 = cta_start(blockIdx.x, W, N);
+    r1 = cta_start((long long)blockIdx.x + 1, W, N);
+    const int excl = (int)before + incl - np;
+    if (np > 0) {
+      for (int w2 = 0; w2 < kNW; ++w2) {
+        const long long ws = r0 + (r1 - r0) * w2 / kNW, we = r0 + (r1 - r0) * (w2 + 1) / kNW;
+        if (ws < we && ws >= (long long)excl * p.hkv && ws < (long long)(excl + np) * p.hkv) {
+          wstart_b[w2] = b;
+          wstart_cu[w2] = excl;
+        }
+      }
+    }
+    if (tid == 0) s_W = W;
+    __syncthreads();
+  } else {
+    long long pages_local = 0;
+    for (int b = tid; b < p.batch; b += kNW * 32) {
+      const int L = clamp_len(p, b);
+      pages_local += (L + kPage - 1) / kPage;
+      if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
+        float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
+        for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int h = 0; h < p.hkv; ++h) p.hdr[(long long)b * p.hkv + h] = make_int2(0, 0);  // nothing to combine
+      }
+    }
+    W = block_sum_ll(pages_local, red, warp, lane) * p.hkv;
+    if (tid == 0) s_W = W;
+    if (W == 0) return;
+    r0 = cta_start(blockIdx.x, W, N);
+    r1 = cta_start((long long)blockIdx.x + 1, W, N);
 
-  // ---- locate the sequence holding each warp's first page-head ----------------
-  if (tid < kNW) wstart_b[tid] = -1;
-  __syncthreads();
-  {
+    // locate the sequence holding each warp's first page-head
     int carry = 0;
     for (int base = 0; base < p.batch; base += kNW * 32) {
       const int b = base + tid;
