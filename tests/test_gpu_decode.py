@@ -11,8 +11,8 @@ import torch
 import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import (ATTN_TOL, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle,
-                      oracle_pair, pool_host, status_word)
+from gpu_util import (ATTN_TOL, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
+                      gpu_cache, oracle_pair, pool_host, status_word)
 
 pytestmark = pytest.mark.gpu
 
@@ -145,3 +145,33 @@ def test_full_size_decode_b32_ctx8k(cuda_lib):
 
 def test_full_size_decode_b4_ctx128k(cuda_lib):
     _full_size_sampled(3, [(2, 3)])
+
+
+def test_full_size_ragged_b256(cuda_lib):
+    # 256 sequences of 512..32768 tokens, 32 q / 8 KV heads, a fragmented pool:
+    # the cache is filled one sequence at a time (its bf16 source would not
+    # fit comfortably on the host at once); sampled pairs go to the oracle
+    wl = inputs.decode_config(4)
+    lens = wl.seq_lens
+    samples = [(0, 0), (int(np.argmax(lens)), 3), (int(np.argmin(lens)), 5), (200, 7), (255, 1)]
+    keep = {b for b, _ in samples}
+    new = wl.new_kv()
+    q = wl.q()
+    g = gpu_cache(wl.num_pages, wl.num_kv_heads)
+    kept = {}
+    for b in range(wl.batch):
+        k, v = wl.prompt_kv(b)
+        gpu_append(g, k, v, wl.slots(b, 0, k.shape[0]))
+        if b in keep:
+            kept[b] = (np.concatenate([k, new[0][b:b + 1]]), np.concatenate([v, new[1][b:b + 1]]))
+    gpu_append(g, new[0], new[1], wl.append_slots())
+    st = status_word()
+    out, _ = decode_gpu(wl, g, q, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    out = out.cpu().numpy()
+    G = wl.num_q_heads // wl.num_kv_heads
+    for b, h in samples:
+        k_seq, v_seq = kept[b]
+        ref, _, _ = oracle_pair(wl, b, h, k_seq, v_seq, q, 1.0, 1.0)
+        check_rows(out[b, h * G:(h + 1) * G], ref)
