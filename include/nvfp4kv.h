@@ -156,6 +156,32 @@ int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* o
                              float softmax_scale, void* workspace, size_t workspace_bytes,
                              int32_t* device_status, nvfp4kv_stream_t stream);
 
+/*
+ * One decode step in one call: nvfp4kv_quantize_append of the step's new tokens
+ * followed by nvfp4kv_decode_attention over the cache that now holds them
+ * ("nvfp4-kv-cache-memory-wall", section 3: the new token's K/V are quantised
+ * into the cache, then decode attends over it; nmedialink repost of NVIDIA's
+ * blog, figure 3).  The results are exactly those of the two calls made one
+ * after the other on `stream`.
+ *
+ * The decode is launched as a programmatic dependent of the append: its set-up
+ * (reading seq_lens, page_table and q, splitting the work, zeroing the outputs
+ * of empty sequences) overlaps the append, and it waits for the append to
+ * finish before it reads any page of the cache.  So q, page_table and seq_lens
+ * must be ready when the call is enqueued (as for any stream-ordered call),
+ * and none of them may alias the new k, v or slot_mapping.
+ *
+ * Arguments are those of nvfp4kv_quantize_append (k .. num_tokens) and of
+ * nvfp4kv_decode_attention (q .. workspace_bytes), with one device_status for
+ * both.  All arguments are checked before anything is enqueued.
+ */
+int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, const void* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens, const void* q, float* out,
+                                    const int32_t* page_table, int32_t max_pages_per_seq,
+                                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* device_status, nvfp4kv_stream_t stream);
+
 /* Bytes of the fixed device scratch used by nvfp4kv_decode_attention_static. */
 #define NVFP4KV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 

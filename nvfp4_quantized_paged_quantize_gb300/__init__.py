@@ -81,11 +81,13 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_decode_attention.argtypes = [pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz, vp, vp]
     L.nvfp4kv_dequant_to_fp8_workspace.argtypes = [pc, vp, i32, vp, vp, i32, i64, f32, f32, vp, vp, vp, vp]
     L.nvfp4kv_decode_attention_static.argtypes = [pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, vp]
+    L.nvfp4kv_append_decode_attention.argtypes = [pc, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz,
+                                                  vp, vp]
     L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
     L.nvfp4kv_status_string.restype = ctypes.c_char_p
     for name in ("nvfp4kv_cache_bytes", "nvfp4kv_quantize_append", "nvfp4kv_decode_workspace_size",
                  "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
-                 "nvfp4kv_decode_attention_static"):
+                 "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -200,6 +202,24 @@ def nvfp4kv_decode_attention(cache: Cache, q, out, page_table, seq_lens, softmax
                                          workspace_bytes, _ptr(device_status), _stream(stream)))
 
 
+def nvfp4kv_append_decode_attention(cache: Cache, k, v, slot_mapping, q, out, page_table, seq_lens,
+                                    softmax_scale: float, workspace, device_status=None, stream=None,
+                                    workspace_bytes: int | None = None) -> None:
+    """One decode step: quantize-append of k, v at slot_mapping, then decode
+    attention of q over the cache (see include/nvfp4kv.h)."""
+    n = int(slot_mapping.shape[0])
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    maxp = int(page_table.shape[1])
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    c = cache.c_struct()
+    _check("nvfp4kv_append_decode_attention",
+           _L().nvfp4kv_append_decode_attention(ctypes.byref(c), _ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(q),
+                                                _ptr(out), _ptr(page_table), maxp, _ptr(seq_lens), B, Hq,
+                                                float(softmax_scale), _ptr(workspace), workspace_bytes,
+                                                _ptr(device_status), _stream(stream)))
+
+
 def nvfp4kv_decode_attention_static(cache: Cache, q, out, page_table, seq_lens, softmax_scale: float,
                                     device_status=None, stream=None) -> None:
     """nvfp4kv_decode_attention for callers that cannot allocate: the split-K
@@ -231,4 +251,4 @@ def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_p
 
 __all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
-           "nvfp4kv_status_string", "nvfp4kv_decode_attention_static"]
+           "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention"]

@@ -74,9 +74,9 @@ int nvfp4kv_cache_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t head_di
   return NVFP4KV_OK;
 }
 
-int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const void* v,
-                            const int64_t* slot_mapping, int64_t num_tokens, int32_t* device_status,
-                            nvfp4kv_stream_t stream) {
+// Host checks of quantize-append arguments (nothing is enqueued).
+static int check_append(const nvfp4kv_cache* cache, const void* k, const void* v, const int64_t* slot_mapping,
+                        int64_t num_tokens, int32_t* device_status) {
   int st = check_cache(cache);
   if (st != NVFP4KV_OK) return st;
   if (num_tokens < 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
@@ -85,6 +85,14 @@ int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const voi
   if (!k || !v || !slot_mapping) return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)) return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  return NVFP4KV_OK;
+}
+
+int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const void* v,
+                            const int64_t* slot_mapping, int64_t num_tokens, int32_t* device_status,
+                            nvfp4kv_stream_t stream) {
+  int st = check_append(cache, k, v, slot_mapping, num_tokens, device_status);
+  if (st != NVFP4KV_OK || num_tokens == 0) return st;
   int nsm = 0;
   if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
   return cuda_status(nvfp4kv::launch_quantize_append(
@@ -103,10 +111,12 @@ int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int
   return NVFP4KV_OK;
 }
 
-int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* out,
-                             const int32_t* page_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
-                             int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
-                             size_t workspace_bytes, int32_t* device_status, nvfp4kv_stream_t stream) {
+// Host checks of decode arguments (nothing is enqueued); *nsm gets the
+// current device's SM count when batch > 0.
+static int check_decode(const nvfp4kv_cache* cache, const void* q, float* out, const int32_t* page_table,
+                        int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                        float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* device_status,
+                        int* nsm) {
   int st = check_cache(cache);
   if (st != NVFP4KV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
@@ -123,15 +133,52 @@ int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* o
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
     return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
-  int nsm = 0;
-  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
-  const size_t need = nvfp4kv::decode_workspace_bytes(nvfp4kv::decode_num_ctas(nsm), batch,
+  if ((st = current_num_sms(nsm)) != NVFP4KV_OK) return st;
+  const size_t need = nvfp4kv::decode_workspace_bytes(nvfp4kv::decode_num_ctas(*nsm), batch,
                                                       cache->num_kv_heads);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return NVFP4KV_ERR_WORKSPACE;
+  return NVFP4KV_OK;
+}
+
+int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* out,
+                             const int32_t* page_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                             int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
+                             size_t workspace_bytes, int32_t* device_status, nvfp4kv_stream_t stream) {
+  int nsm = 0;
+  const int st = check_decode(cache, q, out, page_table, max_pages_per_seq, seq_lens, batch, num_q_heads,
+                              softmax_scale, workspace, workspace_bytes, device_status, &nsm);
+  if (st != NVFP4KV_OK || batch == 0) return st;
   return cuda_status(nvfp4kv::launch_decode(*cache, static_cast<const uint16_t*>(q), out, page_table,
                                             max_pages_per_seq, seq_lens, batch, num_q_heads, softmax_scale,
                                             workspace, device_status, nsm,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, const void* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens, const void* q, float* out,
+                                    const int32_t* page_table, int32_t max_pages_per_seq,
+                                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* device_status, nvfp4kv_stream_t stream) {
+  int st = check_append(cache, k, v, slot_mapping, num_tokens, device_status);
+  if (st != NVFP4KV_OK) return st;
+  int nsm = 0;
+  st = check_decode(cache, q, out, page_table, max_pages_per_seq, seq_lens, batch, num_q_heads, softmax_scale,
+                    workspace, workspace_bytes, device_status, &nsm);
+  if (st != NVFP4KV_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (num_tokens > 0) {
+    int asm_ = nsm;
+    if (asm_ == 0 && (st = current_num_sms(&asm_)) != NVFP4KV_OK) return st;
+    st = cuda_status(nvfp4kv::launch_quantize_append(*cache, static_cast<const uint16_t*>(k),
+                                                     static_cast<const uint16_t*>(v), slot_mapping, num_tokens,
+                                                     device_status, asm_, s));
+    if (st != NVFP4KV_OK) return st;
+  }
+  if (batch == 0) return NVFP4KV_OK;
+  return cuda_status(nvfp4kv::launch_decode(*cache, static_cast<const uint16_t*>(q), out, page_table,
+                                            max_pages_per_seq, seq_lens, batch, num_q_heads, softmax_scale,
+                                            workspace, device_status, nsm, s, num_tokens > 0));
 }
 
 int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* page_table,

@@ -737,6 +737,11 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     uint32_t vnxt = 0;
 
     bool ok = true;  // false after a wait gave up: stop waiting, computing and issuing
+    // Launched right behind the append of the same decode step
+    // (nvfp4kv_append_decode_attention), this grid ran everything above while
+    // the append was still writing the new tokens' pages: wait for it before
+    // the first page is read.  Without a prerequisite grid this returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // producer: prefill the ring (all within the first chunk: kStages < 32)
     const int pre = n < kStages ? n : kStages;
     const LaneCopy lc = lane_copy(p, lane);
@@ -936,7 +941,7 @@ size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads)
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
                           int32_t max_pages, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                           float softmax_scale, void* workspace, int32_t* device_status, int num_sms,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool after_kernel) {
   static bool attr_set = false;  // the attribute is per function, for every device
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -968,8 +973,24 @@ cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
   p.part = static_cast<float*>(workspace);
   p.hdr = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + rec);
   p.status = device_status;
-  decode_kernel<<<num_ctas, kNW * 32, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (after_kernel) {
+    // a programmatic dependent of the kernel before it on the stream
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = dim3((unsigned)num_ctas);
+    dc.blockDim = dim3(kNW * 32);
+    dc.dynamicSmemBytes = kSmemBytes;
+    dc.stream = stream;
+    cudaLaunchAttribute da[1];
+    da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    da[0].val.programmaticStreamSerializationAllowed = 1;
+    dc.attrs = da;
+    dc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&dc, decode_kernel, p);
+  } else {
+    decode_kernel<<<num_ctas, kNW * 32, kSmemBytes, stream>>>(p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || pairs == 0) return e;
   // the combine, as a programmatic dependent of the decode on the same stream
   // records per cut pair are about (warps / pairs) when the sequences are

@@ -26,6 +26,7 @@ size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads)
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                           int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
-                          int32_t* device_status, int num_sms, cudaStream_t stream);
+                          int32_t* device_status, int num_sms, cudaStream_t stream,
+                          bool after_kernel = false);
 
 }  // namespace nvfp4kv

@@ -54,6 +54,9 @@ __device__ __forceinline__ float div_markstein(float a, float b, float r) {
 }
 
 __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p) {
+  // a decode launched behind this append (nvfp4kv_append_decode_attention) may
+  // start its set-up now; it waits for this grid before reading any page
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int tensor = lane >> 4;  // 0: K, 1: V
   const int sub = lane & 7;      // block j = sub of the row: values [16 j, 16 j + 16)

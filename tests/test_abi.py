@@ -110,3 +110,18 @@ def test_host_validation_codes(lib):
                                                 None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
     assert lib.nvfp4kv_dequant_to_fp8_workspace(P(cs), 4, 1, 4, 8, 1, 0, 1.0, 1.0, 16, 16, None,
                                                 None) == kv.NVFP4KV_OK
+
+
+def test_fused_step_checks_both_calls_before_enqueueing(lib):
+    cs = _fake_cache().c_struct()
+    P = ctypes.byref
+    f = lib.nvfp4kv_append_decode_attention
+    # a bad append argument (misaligned k) or a bad decode argument (group 3)
+    # is reported; with nothing to append and an empty batch nothing happens
+    assert f(P(cs), 18, 16, 8, 1, 16, 16, 4, 1, 4, 0, 8, 0.1, 256, 1 << 20, None, None) == \
+        kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(P(cs), 16, 16, 8, 1, 16, 16, 4, 1, 4, 1, 3, 0.1, 256, 1 << 20, None, None) == \
+        kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(P(cs), 16, 16, 8, 1, 16, 16, 4, 1, 4, 1, 8, float("inf"), 256, 1 << 20, None, None) == \
+        kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(P(cs), None, None, None, 0, 16, 16, 4, 1, 4, 0, 8, 0.1, 256, 1 << 20, None, None) == kv.NVFP4KV_OK

@@ -11,7 +11,7 @@ import torch
 import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import (ATTN_TOL, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
+from gpu_util import (ATTN_TOL, bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
                       gpu_cache, oracle_pair, pool_host, status_word)
 
 pytestmark = pytest.mark.gpu
@@ -175,3 +175,48 @@ def test_full_size_ragged_b256(cuda_lib):
         k_seq, v_seq = kept[b]
         ref, _, _ = oracle_pair(wl, b, h, k_seq, v_seq, q, 1.0, 1.0)
         check_rows(out[b, h * G:(h + 1) * G], ref)
+
+
+@pytest.mark.parametrize("index,scale", [(1, 1.0), (2, 1 / 32), (4, 1 / 32), (3, 1 / 256)])
+def test_fused_append_decode_matches_two_calls(cuda_lib, index, scale):
+    # nvfp4kv_append_decode_attention gives exactly the bits of
+    # nvfp4kv_quantize_append followed by nvfp4kv_decode_attention
+    wl = inputs.decode_config(index, scale)
+    prompts = wl.all_prompt_kv()
+    new = wl.new_kv() if wl.append else None
+    q = wl.q()
+    gk, gv = wl.global_scales(prompts, new)
+
+    def prompts_only():                         # the step itself appends the new token
+        c = gpu_cache(wl.num_pages, wl.num_kv_heads, gk, gv)
+        for bb in range(wl.batch):
+            kk, vv = prompts[bb]
+            if kk.shape[0]:
+                gpu_append(c, kk, vv, wl.slots(bb, 0, kk.shape[0]))
+        return c
+
+    a = prompts_only()
+    b = prompts_only()
+    if new is not None:
+        slots = dev(wl.append_slots())
+        k, v = bf16_dev(new[0]), bf16_dev(new[1])
+    else:
+        slots = dev(np.zeros(0, np.int64))
+        k = v = bf16_dev(np.zeros((0, wl.num_kv_heads, 128), np.uint16))
+    qd, pt, lens = bf16_dev(q), dev(wl.page_table), dev(wl.seq_lens.astype(np.int32))
+    n = kv.nvfp4kv_decode_workspace_size(a, wl.batch, wl.num_q_heads)
+    ws_a = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    ws_b = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    out_a = torch.full((wl.batch, wl.num_q_heads, 128), float("nan"), device="cuda")
+    out_b = torch.full_like(out_a, float("nan"))
+    st = status_word()
+    kv.nvfp4kv_append_decode_attention(a, k, v, slots, qd, out_a, pt, lens, wl.softmax_scale, ws_a,
+                                       device_status=st)
+    if new is not None:
+        kv.nvfp4kv_quantize_append(b, k, v, slots)
+    kv.nvfp4kv_decode_attention(b, qd, out_b, pt, lens, wl.softmax_scale, ws_b)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out_a, out_b)
+    for x, y in zip(pool_host(a), pool_host(b)):
+        np.testing.assert_array_equal(x, y)
