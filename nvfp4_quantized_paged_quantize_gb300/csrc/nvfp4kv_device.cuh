@@ -1,6 +1,6 @@
 // nvfp4kv_device.cuh -- device-side building blocks of the NVFP4 paged KV cache
-// (sm_103a): format conversions through the hardware cvt instructions, TMA bulk
-// copies with mbarrier completion, and bounded waits.
+// (sm_103a): format conversions through the hardware cvt instructions, mbarrier
+// set-up, and bounded waits.
 //
 // Format ("nvfp4-kv-cache-memory-wall", section 2; "NVFP4: breaking the memory
 // wall", technical breakdown): E2M1 data (+-{0,0.5,1,1.5,2,3,4,6}), one E4M3
@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // ---------------------------------------------------------------------------
-// shared memory, mbarrier and TMA bulk copy (global -> shared, 1-D)
+// shared memory and mbarriers
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -107,27 +107,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-// Make mbarrier initialisation visible to the asynchronous (TMA) proxy.
+// Make mbarrier initialisation visible to the asynchronous proxy (the
+// cp.async arrivals).
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global memory into this CTA's shared memory; completion is counted on `bar`.
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
