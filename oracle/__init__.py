@@ -75,6 +75,10 @@ def lib():
         L.nvfp4_oracle_dequant_to_fp8_workspace.argtypes = [ctypes.POINTER(_CCache), vp, i32, vp,
                                                             vp, i32, f32, f32, vp, vp]
         L.nvfp4_oracle_dequant_to_fp8_workspace.restype = ctypes.c_int
+        L.nvfp4_oracle_tensor_amax.argtypes = [vp, i64]
+        L.nvfp4_oracle_tensor_amax.restype = f32
+        L.nvfp4_oracle_calibrated_global_scale.argtypes = [f32]
+        L.nvfp4_oracle_calibrated_global_scale.restype = f32
         _lib = L
     return _lib
 
@@ -227,3 +231,14 @@ def dequantize_rows(cache: Cache, which: str, rows) -> np.ndarray:
 
 
 __all__ = [name for name in dir() if not name.startswith("_")]
+
+
+def tensor_amax(x_bf16) -> float:
+    """Largest |x| of a bf16 tensor (uint16 bit patterns); 0 when empty."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1)
+    return float(lib().nvfp4_oracle_tensor_amax(_ptr(x), x.size))
+
+
+def calibrated_global_scale(amax: float) -> float:
+    """g = amax / (6 * 448) in binary32 (1 when amax is 0)."""
+    return float(lib().nvfp4_oracle_calibrated_global_scale(float(np.float32(amax))))

@@ -374,3 +374,24 @@ int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int
   }
   return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the FP32
+ * per-tensor scale is left at 1 by the uncalibrated public setting, and a
+ * calibrated one reduces overflow and underflow of the two-level range; the
+ * calibrated value maps the tensor's largest magnitude onto 6 x 448).        */
+
+float nvfp4_oracle_tensor_amax(const uint16_t* x_bf16, int64_t n) {
+  float m = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    const float a = fabsf(nvfp4_oracle_bf16_to_float(x_bf16[i]));
+    if (a > m) m = a;
+  }
+  return m;
+}
+
+float nvfp4_oracle_calibrated_global_scale(float amax) {
+  const float top = 6.0f * 448.0f; /* 2688, exact */
+  if (amax == 0.0f) return 1.0f;
+  return amax / top;
+}

@@ -57,6 +57,13 @@ int nvfp4_oracle_decode_attention_heads(const nvfp4_oracle_cache* c, const uint1
                                         const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                                         double softmax_scale, int32_t head_begin, int32_t head_end,
                                         double* out);
+/* Largest |x| over n bf16 values (0 for n == 0), as a float (exact: a bf16
+ * value).  The calibration statistic of a tensor's global scale. */
+float nvfp4_oracle_tensor_amax(const uint16_t* x_bf16, int64_t n);
+/* Calibrated global scale g = amax / (6 * 448), one binary32 division, so the
+ * tensor's largest value maps onto E2M1's 6 times E4M3's 448; 1 when amax is 0. */
+float nvfp4_oracle_calibrated_global_scale(float amax);
+
 int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int32_t* page_table,
                                           int32_t max_pages, const int32_t* prefix_lens,
                                           const int64_t* cu_prefix, int32_t batch,
