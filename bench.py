@@ -166,8 +166,22 @@ def _bf16(torch, bits):
     return _dev(torch, np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16), torch.bfloat16)
 
 
+def _global_scales(torch, kv, wl, prompts, new):
+    """1, or the library's calibration: nvfp4kv_tensor_amax folded over every K
+    (every V) tensor on the device, then nvfp4kv_calibrated_global_scale."""
+    pairs = wl.calibration_tensors(prompts, new)
+    if not pairs:
+        return 1.0, 1.0
+    amax = torch.zeros(2, dtype=torch.float32, device="cuda")
+    for p in pairs:
+        for i in range(2):
+            kv.nvfp4kv_tensor_amax(_bf16(torch, p[i]).reshape(-1), amax[i:i + 1], accumulate=True)
+    a = amax.cpu().tolist()
+    return kv.nvfp4kv_calibrated_global_scale(a[0]), kv.nvfp4kv_calibrated_global_scale(a[1])
+
+
 def _fill_cache(torch, kv, wl, prompts, new):
-    gk, gv = wl.global_scales(prompts, new)
+    gk, gv = _global_scales(torch, kv, wl, prompts, new)
     cache = kv.Cache.empty(wl.num_pages, wl.num_kv_heads, k_global_scale=gk, v_global_scale=gv, zero=True)
     for b in range(wl.batch):
         k, v = prompts[b]
@@ -175,6 +189,14 @@ def _fill_cache(torch, kv, wl, prompts, new):
                                    _dev(torch, wl.slots(b, 0, k.shape[0])))
     torch.cuda.synchronize()
     return cache
+
+
+def _calibration_input(torch, wl):
+    """One layer's K of a decode workload as one bf16 device tensor: the first
+    sequence's prompt K drawn by the workload, repeated over the batch."""
+    k, _ = wl.prompt_kv(0)
+    x = _bf16(torch, k).reshape(-1).repeat(wl.batch)
+    return x, torch.zeros(1, dtype=torch.float32, device="cuda")
 
 
 class DecodeBench:
@@ -382,6 +404,16 @@ def secondary(torch, kv, args, flush, hbm_peak):
                                 "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS, "frac_of_measured_peak": gbs / hbm_peak}
     del b
     torch.cuda.empty_cache()
+    # calibration: the amax pass over one layer's K of that workload (4 x 131072
+    # tokens x 8 heads x 128 bf16 values, 1.07 GB), HBM-bound at 2 B per value
+    x, amax = _calibration_input(torch, wl)
+    ms, _ = time_steps(torch, steps, args.warmup, lambda ev=None: kv.nvfp4kv_tensor_amax(x, amax), flush)
+    t = float(np.mean(ms))
+    gbs = (2 * x.numel() + 4) / (t / 1e3) / 1e9
+    out["calibrate_amax_b4_ctx128k_k"] = {"kernel_ms": t, "values": int(x.numel()), "hbm_gbs": gbs,
+                                          "frac_of_measured_peak": gbs / hbm_peak}
+    del x
+    torch.cuda.empty_cache()
     # extend: one layer (16 x 16384-token prefix -> FP8 workspace; 16 x 2048 new tokens quantized)
     ew = inputs.extend_config(num_layers=1)
     cache = kv.Cache.empty(ew.num_pages, ew.num_kv_heads, zero=True)
@@ -527,7 +559,10 @@ def only_arm(args):
     kv.load()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     flush = lambda: flush_buf.zero_()
-    if args.only in ("decode8k", "decode128k"):
+    if args.only == "calibrate":
+        x, amax = _calibration_input(torch, inputs.decode_config(3))
+        time_steps(torch, args.steps, args.warmup, lambda ev=None: kv.nvfp4kv_tensor_amax(x, amax), flush)
+    elif args.only in ("decode8k", "decode128k"):
         b = DecodeBench(torch, kv, inputs.decode_config(2 if args.only == "decode8k" else 3))
         time_steps(torch, args.steps, args.warmup, lambda ev=None: (b.append(), b.decode()), flush)
     else:
@@ -560,7 +595,7 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--cpu-total-s", type=float, default=90.0, help="reference arm: total oracle seconds")
-    ap.add_argument("--only", choices=["decode8k", "decode128k", "extend"],
+    ap.add_argument("--only", choices=["decode8k", "decode128k", "extend", "calibrate"],
                     help="run just one workload's kernels (profiler command lines); no JSON metric line")
     args = ap.parse_args()
     if args.warmup < 3:

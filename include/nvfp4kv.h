@@ -243,6 +243,34 @@ int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* 
                                      uint8_t* ws_v, int32_t* device_status,
                                      nvfp4kv_stream_t stream);
 
+/* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the
+ * FP32 per-tensor scale is 1 in the uncalibrated public setting; a calibrated
+ * scale maps the tensor's largest magnitude onto the largest NVFP4 magnitude,
+ * E2M1 6 times E4M3 448).
+ *
+ * nvfp4kv_tensor_amax writes max |x| over n bf16 values into *amax, a device
+ * float; the result is exact (a bf16 value) and is +0 when n == 0.  NaN inputs
+ * count as magnitudes above every finite value and infinity (their bit
+ * patterns are larger), so a NaN input gives a NaN amax.
+ *   x_bf16      device bf16 [n], 16-byte aligned (may be NULL when n == 0)
+ *   n           >= 0
+ *   amax        device float, 4-byte aligned
+ *   accumulate  0: *amax is zeroed on the stream first; else *amax must hold
+ *               +0 or an earlier result and becomes max(*amax, max |x|), so one
+ *               scale can be calibrated over many tensors (all of a layer's
+ *               sequences) without a host round trip
+ * Asynchronous on stream: read *amax after synchronising.
+ *
+ * nvfp4kv_calibrated_global_scale is host-only and synchronous:
+ * *g = amax / 2688 in one binary32 division (round to nearest even), or 1 when
+ * amax == 0 (an all-zero tensor keeps the uncalibrated scale).  amax must be
+ * finite and >= 0, else NVFP4KV_ERR_INVALID_ARGUMENT and *g is untouched.
+ * The result is the k_global_scale / v_global_scale of a cache whose K or V is
+ * that tensor. */
+int nvfp4kv_tensor_amax(const void* x_bf16, int64_t n, float* amax, int accumulate,
+                        nvfp4kv_stream_t stream);
+int nvfp4kv_calibrated_global_scale(float amax, float* g);
+
 /* A static, human-readable string for a status code (never NULL). */
 const char* nvfp4kv_status_string(int status);
 

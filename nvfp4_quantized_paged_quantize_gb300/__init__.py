@@ -83,11 +83,14 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_decode_attention_static.argtypes = [pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, vp]
     L.nvfp4kv_append_decode_attention.argtypes = [pc, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz,
                                                   vp, vp]
+    L.nvfp4kv_tensor_amax.argtypes = [vp, i64, vp, ctypes.c_int, vp]
+    L.nvfp4kv_calibrated_global_scale.argtypes = [f32, ctypes.POINTER(f32)]
     L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
     L.nvfp4kv_status_string.restype = ctypes.c_char_p
     for name in ("nvfp4kv_cache_bytes", "nvfp4kv_quantize_append", "nvfp4kv_decode_workspace_size",
                  "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
-                 "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention"):
+                 "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
+                 "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -249,6 +252,28 @@ def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_p
                                                  _ptr(device_status), _stream(stream)))
 
 
+def nvfp4kv_tensor_amax(x, amax, accumulate: bool = False, stream=None) -> None:
+    """max |x| of a contiguous bf16 device tensor into amax (a float32 device tensor of one element);
+    with accumulate, max(amax, max |x|)."""
+    import torch
+
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 tensor")
+    if amax.dtype != torch.float32 or amax.numel() != 1:
+        raise ValueError("amax must be a one-element float32 tensor")
+    _check("nvfp4kv_tensor_amax",
+           _L().nvfp4kv_tensor_amax(_ptr(x) if x.numel() else None, int(x.numel()), _ptr(amax),
+                                    int(bool(accumulate)), _stream(stream)))
+
+
+def nvfp4kv_calibrated_global_scale(amax: float) -> float:
+    """The FP32 global scale that maps amax onto 6 * 448 (1.0 when amax == 0)."""
+    g = ctypes.c_float()
+    _check("nvfp4kv_calibrated_global_scale", _L().nvfp4kv_calibrated_global_scale(float(amax), ctypes.byref(g)))
+    return g.value
+
+
 __all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
-           "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention"]
+           "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
+           "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale"]

@@ -181,6 +181,23 @@ int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, c
                                             workspace, device_status, nsm, s, num_tokens > 0));
 }
 
+int nvfp4kv_tensor_amax(const void* x_bf16, int64_t n, float* amax, int accumulate,
+                        nvfp4kv_stream_t stream) {
+  if (n < 0 || amax == nullptr || !aligned(amax, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (n > 0 && (x_bf16 == nullptr || !aligned(x_bf16, 16))) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  const int st = current_num_sms(&nsm);
+  if (st != NVFP4KV_OK) return st;
+  return cuda_status(nvfp4kv::launch_tensor_amax(static_cast<const uint16_t*>(x_bf16), n, amax, accumulate != 0,
+                                                 nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4kv_calibrated_global_scale(float amax, float* g) {
+  if (g == nullptr || !std::isfinite(amax) || amax < 0.0f) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  *g = amax == 0.0f ? 1.0f : amax / (6.0f * 448.0f);  // one binary32 division
+  return NVFP4KV_OK;
+}
+
 int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* page_table,
                                      int32_t max_pages_per_seq, const int32_t* prefix_lens,
                                      const int64_t* cu_prefix, int32_t batch, int64_t total_rows,

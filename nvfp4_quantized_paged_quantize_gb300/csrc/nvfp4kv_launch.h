@@ -18,6 +18,11 @@ cudaError_t launch_dequant_fp8(const nvfp4kv_cache& c, const int32_t* page_table
                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
                                uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream);
 
+// Largest |x| of n bf16 values into the device float *amax (zeroed first
+// unless accumulate, which folds into the value already there).
+cudaError_t launch_tensor_amax(const uint16_t* x, int64_t n, float* amax, bool accumulate, int num_sms,
+                               cudaStream_t stream);
+
 // Split-K decode: how many CTAs the decode launches on a device with num_sms
 // SMs, and the workspace layout that goes with it.
 int decode_num_ctas(int num_sms);

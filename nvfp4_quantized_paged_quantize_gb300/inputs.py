@@ -127,7 +127,7 @@ class DecodeWorkload:
     num_kv_heads: int
     dist: KVDist
     q_sigma: float = 1.0
-    calibrated: bool = False         # per-tensor global scale amax/(6*448), else 1.0
+    calibrated: bool = False         # per-tensor calibrated global scales, else 1.0
     pool_factor: float = 1.0         # physical pages / pages needed (>1 leaves holes)
     head_dim: int = HEAD_DIM
     page_size: int = PAGE_SIZE
@@ -233,25 +233,16 @@ class DecodeWorkload:
         with ThreadPoolExecutor(max_workers=threads) as ex:
             return list(ex.map(self.prompt_kv, range(self.batch)))
 
-    def global_scales(self, prompt=None, new=None):
-        """(k_global_scale, v_global_scale): 1.0, or amax/(6*448) of each whole
-        K and V tensor (prompt and appended tokens) when calibrated."""
+    def calibration_tensors(self, prompt=None, new=None):
+        """The (K, V) bf16 pairs a calibrated global scale is taken over: every
+        sequence's prompt and, when the step appends, the new tokens.  Empty
+        when the workload keeps the uncalibrated scale 1."""
         if not self.calibrated:
-            return 1.0, 1.0
-        if "gscale" not in self._cache:
-            prompt = prompt if prompt is not None else self.all_prompt_kv()
-            amax = [0.0, 0.0]
-            for kv in prompt:
-                for i in range(2):
-                    if kv[i].size:
-                        amax[i] = max(amax[i], float(np.abs(bf16_bits_to_f32(kv[i])).max()))
-            if self.append:
-                new = new if new is not None else self.new_kv()
-                for i in range(2):
-                    amax[i] = max(amax[i], float(np.abs(bf16_bits_to_f32(new[i])).max()))
-            self._cache["gscale"] = tuple(float(np.float32(a / (6.0 * 448.0))) if a > 0 else 1.0
-                                          for a in amax)
-        return self._cache["gscale"]
+            return []
+        pairs = list(prompt if prompt is not None else self.all_prompt_kv())
+        if self.append:
+            pairs.append(new if new is not None else self.new_kv())
+        return pairs
 
     def kv_tokens(self) -> int:
         return int(self.seq_lens.astype(np.int64).sum())

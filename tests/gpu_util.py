@@ -47,9 +47,33 @@ def pool_host(cache):
                                                                cache.v_scale))
 
 
+def oracle_global_scales(wl, prompts, new=None):
+    """(k, v) global scales by the oracle: 1, or the calibration over every K
+    (every V) tensor of the workload."""
+    pairs = wl.calibration_tensors(prompts, new)
+    if not pairs:
+        return 1.0, 1.0
+    return tuple(oracle.calibrated_global_scale(max(oracle.tensor_amax(p[i]) for p in pairs)) for i in range(2))
+
+
+def gpu_global_scales(wl, prompts, new=None):
+    """(k, v) global scales through the library: nvfp4kv_tensor_amax folded
+    over every K (every V) tensor on the device, then
+    nvfp4kv_calibrated_global_scale of the two maxima."""
+    pairs = wl.calibration_tensors(prompts, new)
+    if not pairs:
+        return 1.0, 1.0
+    amax = torch.zeros(2, dtype=torch.float32, device="cuda")
+    for p in pairs:
+        for i in range(2):
+            kv.nvfp4kv_tensor_amax(bf16_dev(p[i]).reshape(-1), amax[i:i + 1], accumulate=True)
+    a = amax.cpu().tolist()
+    return kv.nvfp4kv_calibrated_global_scale(a[0]), kv.nvfp4kv_calibrated_global_scale(a[1])
+
+
 def fill_workload_gpu(wl, prompts, new=None, status=None):
     """GPU cache holding every sequence's prompt (and the appended token)."""
-    gk, gv = wl.global_scales(prompts, new)
+    gk, gv = gpu_global_scales(wl, prompts, new)
     cache = gpu_cache(wl.num_pages, wl.num_kv_heads, gk, gv)
     for b in range(wl.batch):
         k, v = prompts[b]
@@ -62,7 +86,7 @@ def fill_workload_gpu(wl, prompts, new=None, status=None):
 
 
 def fill_workload_oracle(wl, prompts, new=None):
-    gk, gv = wl.global_scales(prompts, new)
+    gk, gv = oracle_global_scales(wl, prompts, new)
     c = oracle.Cache(wl.num_pages, wl.num_kv_heads, 128, 16, gk, gv)
     for b in range(wl.batch):
         k, v = prompts[b]

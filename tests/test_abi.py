@@ -125,3 +125,28 @@ def test_fused_step_checks_both_calls_before_enqueueing(lib):
     assert f(P(cs), 16, 16, 8, 1, 16, 16, 4, 1, 4, 1, 8, float("inf"), 256, 1 << 20, None, None) == \
         kv.NVFP4KV_ERR_INVALID_ARGUMENT
     assert f(P(cs), None, None, None, 0, 16, 16, 4, 1, 4, 0, 8, 0.1, 256, 1 << 20, None, None) == kv.NVFP4KV_OK
+
+
+def test_calibration_host_checks_and_scale(lib):
+    from oracle import calibrated_global_scale
+
+    import numpy as np
+
+    # amax: negative size, misaligned input or output are refused before CUDA
+    f = lib.nvfp4kv_tensor_amax
+    assert f(16, -1, 16, 0, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(18, 8, 16, 0, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(16, 8, 18, 1, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(None, 8, 16, 0, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(16, 8, None, 1, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    # the global scale is host arithmetic: equal to the oracle's, bit for bit
+    for bad in (-1.0, float("nan"), float("inf"), -0.5e-40):
+        with pytest.raises(kv.Nvfp4kvError):
+            kv.nvfp4kv_calibrated_global_scale(bad)
+    rng = np.random.default_rng(7)
+    amaxes = [0.0, -0.0, 1e-45, 1.0, 2688.0, 448.0, 6.0, 3.3895314e38] + \
+        list(np.exp(rng.uniform(-100, 88, 200)).astype(np.float32))
+    for a in amaxes:
+        got = np.float32(kv.nvfp4kv_calibrated_global_scale(float(a)))
+        want = np.float32(calibrated_global_scale(float(a)))
+        assert got.tobytes() == want.tobytes(), a

@@ -12,7 +12,7 @@ import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
 from gpu_util import (ATTN_TOL, bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
-                      gpu_cache, oracle_pair, pool_host, status_word)
+                      gpu_cache, gpu_global_scales, oracle_global_scales, oracle_pair, pool_host, status_word)
 
 pytestmark = pytest.mark.gpu
 
@@ -113,7 +113,7 @@ def _full_size_sampled(index, samples):
     prompts = wl.all_prompt_kv(threads=16)
     new = wl.new_kv() if wl.append else None
     q = wl.q()
-    gk, gv = wl.global_scales(prompts, new)
+    gk, gv = oracle_global_scales(wl, prompts, new)
     g = fill_workload_gpu(wl, prompts, new)
     out, _ = decode_gpu(wl, g, q)
     out = out.cpu().numpy()
@@ -185,7 +185,7 @@ def test_fused_append_decode_matches_two_calls(cuda_lib, index, scale):
     prompts = wl.all_prompt_kv()
     new = wl.new_kv() if wl.append else None
     q = wl.q()
-    gk, gv = wl.global_scales(prompts, new)
+    gk, gv = gpu_global_scales(wl, prompts, new)
 
     def prompts_only():                         # the step itself appends the new token
         c = gpu_cache(wl.num_pages, wl.num_kv_heads, gk, gv)

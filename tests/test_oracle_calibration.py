@@ -51,12 +51,28 @@ def test_calibrated_scale_maps_amax_to_top_of_range(amax):
     assert (packed[2] >> 4) & 0xF == 0xF                             # element 5 (high nibble of byte 2): -6
 
 
-def test_workload_generator_uses_the_calibrated_scale():
-    # the long-context workload's global scales are this calibration of its K and V
+def test_calibrated_workload_reaches_the_top_scale():
+    # over the long-context workload, the calibrated scale of each of K and V
+    # gives the block holding that tensor's amax E4M3 scale 448 (code 0x7E) and
+    # no block a larger one; with scale 1 the same data stays far below it
     wl = inputs.decode_config(3, 1 / 1024)
     prompts = wl.all_prompt_kv()
-    gk, gv = wl.global_scales(prompts)
-    ak = max(oracle.tensor_amax(k) for k, _ in prompts)
-    av = max(oracle.tensor_amax(v) for _, v in prompts)
-    assert gk == oracle.calibrated_global_scale(ak)
-    assert gv == oracle.calibrated_global_scale(av)
+    pairs = wl.calibration_tensors(prompts)
+    assert len(pairs) == wl.batch
+    ak = max(oracle.tensor_amax(k) for k, _ in pairs)
+    av = max(oracle.tensor_amax(v) for _, v in pairs)
+    for gk, gv, top in ((oracle.calibrated_global_scale(ak), oracle.calibrated_global_scale(av), 0x7E),
+                        (1.0, 1.0, None)):
+        c = oracle.Cache(wl.num_pages, wl.num_kv_heads, 128, 16, gk, gv)
+        for b, (k, v) in enumerate(prompts):
+            assert oracle.quantize_append(c, k, v, wl.slots(b, 0, k.shape[0])) == 0
+        for sc in (c.k_scale, c.v_scale):
+            if top is None:
+                assert sc.max() < 0x60                                  # below 32: far from 448
+            else:
+                assert sc.max() == top
+
+
+def test_uncalibrated_workloads_have_no_calibration_tensors():
+    for index in (1, 2, 4):
+        assert inputs.decode_config(index, 1 / 64).calibration_tensors() == []
