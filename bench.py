@@ -241,6 +241,22 @@ class DecodeBench:
         return 2 if self.wl.append else 1
 
 
+def make_l2_flush(torch):
+    """Flush L2 between timed steps: write one buffer larger than L2, then read
+    another.  The write evicts every line the step could reuse; the read then
+    replaces the write's dirty lines with clean ones, so the timed step neither
+    finds its inputs in L2 nor pays for writing the flush's data back (which
+    a write-only flush leaves to the next kernel: ~120 MB of write-back)."""
+    wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        wbuf.zero_()
+        rbuf.sum()
+
+    return flush
+
+
 def time_steps(torch, steps, warmup, body, flush, split=None):
     """Run `warmup` untimed then `steps` timed iterations of body(); each timed
     iteration is bracketed by CUDA events on the current stream, with an L2
@@ -281,8 +297,7 @@ def gpu_arm(args):
     kv.load()
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush = lambda: flush_buf.zero_()
+    flush = make_l2_flush(torch)
 
     wl = inputs.decode_config(2)
     bench = DecodeBench(torch, kv, wl)
@@ -361,7 +376,8 @@ def gpu_arm(args):
             "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16,
             "step": "nvfp4kv_append_decode_attention: quantize-append of 32 new tokens + decode attention "
                     "(split-K decode + combine)",
-            "l2": "flushed before every timed step (256 MiB memset, outside the step's events)",
+            "l2": "flushed before every timed step, outside the step's events: a 256 MiB memset, then a read of "
+                  "another 256 MiB (no input cached, no dirty flush lines left to write back)",
             "parallelism": f"replicas x{world}",
         },
         "decode": {
@@ -515,25 +531,50 @@ def cpu_baseline(wl, budget_s=12.0):
                       f"heads each; {wall:.1f} s wall"}
 
 
+def _reference_worker(index, b, n, warmup, steps, barrier, results):
+    """One host process of the reference arm: the oracle on one (sequence, KV
+    head) pair, n tokens per step; the timed steps start together in every
+    process (barrier) and report (KV-tokens, seconds)."""
+    wl = inputs.decode_config(index)
+    sample = OracleSample(wl, b % wl.batch, b % wl.num_kv_heads)
+    for _ in range(warmup):
+        sample.step(n)
+    barrier.wait()
+    t0 = time.perf_counter()
+    done = 0.0
+    for _ in range(steps):
+        done += sample.step(n)
+    results.put((b, done, time.perf_counter() - t0))
+
+
 def reference_arm(args):
+    """The oracle timed as the reference arm: one process per host core, each on
+    its own (sequence, KV head) pair of the headline workload, every step a
+    bounded sample (n tokens) so the whole run takes about --cpu-total-s."""
+    import multiprocessing as mp
+
     world, rank, _ = dist_info()
     if rank != 0:
         return
     wl = inputs.decode_config(2)
     sample = OracleSample(wl, 0, 0)
-    # size each step so that warmup + steps finish in about args.cpu_total_s
     t0 = time.perf_counter()
     sample.step(sample.L)
     t_full = time.perf_counter() - t0
     per_step = args.cpu_total_s / max(1, args.steps + args.warmup)
     n = int(min(sample.L, max(16, sample.L * per_step / max(t_full, 1e-6))))
-    for _ in range(args.warmup):
-        sample.step(n)
-    t0 = time.perf_counter()
-    done = 0.0
-    for _ in range(args.steps):
-        done += sample.step(n)
-    dt = time.perf_counter() - t0
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    barrier, results = ctx.Barrier(cores), ctx.Queue()
+    procs = [ctx.Process(target=_reference_worker, args=(2, b, n, args.warmup, args.steps, barrier, results))
+             for b in range(cores)]
+    for p in procs:
+        p.start()
+    res = [results.get() for _ in procs]
+    for p in procs:
+        p.join()
+    done = sum(r[1] for r in res)
+    dt = max(r[2] for r in res)
     value = done / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -542,9 +583,10 @@ def reference_arm(args):
         "data": "synthetic (same seeded inputs as the GPU arm)",
         "config": {"workload": wl.name, "batch": wl.batch, "ctx": int(wl.seq_lens[0]), "q_heads": wl.num_q_heads,
                    "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16,
-                   "step": f"oracle: append 1 token + fp64 decode over {n} tokens of one (sequence, KV head)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"one (sequence, KV head) pair, {n} of {sample.L} tokens per step"},
+                   "step": f"oracle in {cores} processes: each appends 1 token and decodes (fp64) over {n} "
+                           f"tokens of its own (sequence, KV head)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{cores} (sequence, KV head) pairs, {n} of {sample.L} tokens per step each"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -557,8 +599,7 @@ def only_arm(args):
     import nvfp4_quantized_paged_quantize_gb300 as kv
 
     kv.load()
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush = lambda: flush_buf.zero_()
+    flush = make_l2_flush(torch)
     if args.only == "calibrate":
         x, amax = _calibration_input(torch, inputs.decode_config(3))
         time_steps(torch, args.steps, args.warmup, lambda ev=None: kv.nvfp4kv_tensor_amax(x, amax), flush)

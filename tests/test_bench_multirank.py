@@ -81,5 +81,5 @@ def test_reference_arm_prints_on_rank_zero_only(tmp_path):
     assert _run_reference({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, tmp_path) == []
     (line,) = _run_reference({"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"}, tmp_path)
     assert line["impl"] == "reference" and line["unit"] == "KV-tokens/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == (os.cpu_count() or 1)
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
