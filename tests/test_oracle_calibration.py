@@ -76,3 +76,62 @@ def test_calibrated_workload_reaches_the_top_scale():
 def test_uncalibrated_workloads_have_no_calibration_tensors():
     for index in (1, 2, 4):
         assert inputs.decode_config(index, 1 / 64).calibration_tensors() == []
+
+
+def _rmse_report(wl, prompts, gk, gv):
+    """RMSE of the oracle's dequantised cache against the bf16 inputs, K and V."""
+    import math
+
+    H = wl.num_kv_heads
+    c = oracle.Cache(wl.num_pages, H, 128, 16, gk, gv)
+    err = {"k": 0.0, "v": 0.0}
+    n = 0
+    for b, (k, v) in enumerate(prompts):
+        s = wl.slots(b, 0, k.shape[0])
+        assert oracle.quantize_append(c, k, v, s) == 0
+        rows = ((((s >> 4) * H)[:, None] + np.arange(H)[None, :]) * 16 + (s & 15)[:, None]).reshape(-1)
+        for which, x in (("k", k), ("v", v)):
+            xh = oracle.dequantize_rows(c, which, rows)
+            err[which] += float(((xh - inputs.bf16_bits_to_f32(x).reshape(-1, 128).astype(np.float64)) ** 2).sum())
+        n += k.size
+    return {w: math.sqrt(e / n) for w, e in err.items()}
+
+
+@pytest.mark.parametrize("index,scale", [(2, 1 / 64), (3, 1 / 256)])
+def test_rmse_report_unit_vs_calibrated(index, scale, capsys):
+    # the RMSE of g = 1 against the calibrated scale on the decode workloads:
+    # calibration never does worse here (it moves block scales out of E4M3's
+    # subnormal range when values are small, as in the 8K workload's N(0, 0.02))
+    wl = inputs.decode_config(index, scale)
+    prompts = wl.all_prompt_kv()
+    g = [oracle.calibrated_global_scale(max(oracle.tensor_amax(p[i]) for p in prompts)) for i in range(2)]
+    unit = _rmse_report(wl, prompts, 1.0, 1.0)
+    cal = _rmse_report(wl, prompts, *g)
+    with capsys.disabled():
+        print(f"\n{wl.name} (x{scale:g}): RMSE g=1 K {unit['k']:.6g} V {unit['v']:.6g}; "
+              f"calibrated (gK {g[0]:.6g}, gV {g[1]:.6g}) K {cal['k']:.6g} V {cal['v']:.6g}")
+    for w in ("k", "v"):
+        assert cal[w] <= unit[w]
+
+
+def test_rmse_small_values_need_calibration():
+    # values of N(0, 0.002): with g = 1 most block scales round below E4M3's
+    # smallest subnormal (2^-9) and the blocks store zeros; the calibrated
+    # scale keeps the usual NVFP4 error (a few percent of the RMS value)
+    rng = np.random.default_rng(8)
+    x = inputs.bf16_bits((rng.standard_normal(4096 * 16) * 0.002).astype(np.float32))
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    rms = float(np.sqrt(np.mean(xf ** 2)))
+
+    def rmse(g):
+        err = 0.0
+        for blk in xf.reshape(-1, 16):
+            packed, sb = oracle.quantize_block(blk.astype(np.float32), g)
+            codes = np.stack([np.asarray(packed) & 0xF, np.asarray(packed) >> 4], axis=-1).reshape(-1)
+            xh = np.array([oracle.dequant_value(int(c), int(sb), g) for c in codes])
+            err += float(((xh - blk) ** 2).sum())
+        return float(np.sqrt(err / xf.size))
+
+    g_cal = oracle.calibrated_global_scale(oracle.tensor_amax(x))
+    assert rmse(1.0) > 0.6 * rms
+    assert rmse(g_cal) < 0.15 * rms
