@@ -307,6 +307,7 @@ class ExtendWorkload:
     chunk_len: int
     num_kv_heads: int
     dist: KVDist
+    num_q_heads: int = 64
     head_dim: int = HEAD_DIM
     page_size: int = PAGE_SIZE
     _cache: dict = field(default_factory=dict, repr=False)
@@ -314,6 +315,34 @@ class ExtendWorkload:
     @property
     def prefix_lens(self) -> np.ndarray:
         return np.full(self.batch, self.prefix_len, np.int32)
+
+    @property
+    def cu_q(self) -> np.ndarray:
+        """Query offsets of the chunk tokens: sequence b owns [cu_q[b], cu_q[b+1])."""
+        return np.arange(self.batch + 1, dtype=np.int64) * self.chunk_len
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def chunk_ws_rows(self) -> np.ndarray:
+        """Workspace row of every chunk token: right after its sequence's prefix."""
+        t = np.arange(self.chunk_len, dtype=np.int64)
+        return np.concatenate([self.cu_prefix[b] + self.prefix_len + t for b in range(self.batch)])
+
+    def q(self, layer: int) -> np.ndarray:
+        """bf16 bits [batch * chunk_len, Hq, d] of the chunk's queries, N(0, 1)."""
+        rng = np.random.default_rng([self.seed, _S_Q, layer])
+        n = self.batch * self.chunk_len * self.num_q_heads * self.head_dim
+        return bf16_bits(rng.standard_normal(n, dtype=np.float32)).reshape(
+            self.batch * self.chunk_len, self.num_q_heads, self.head_dim)
+
+    def attention_flops_per_layer(self) -> int:
+        """2 d flops for q.k and 2 d for p.v per (query token, query head, visible
+        key); chunk token t of a sequence sees prefix_len + t + 1 keys."""
+        C, P = self.chunk_len, self.prefix_len
+        keys = C * P + C * (C + 1) // 2
+        return 4 * self.head_dim * self.num_q_heads * self.batch * keys
 
     @property
     def cu_prefix(self) -> np.ndarray:
@@ -386,3 +415,98 @@ def extend_config(scale: float = 1.0, num_layers: int = 80) -> ExtendWorkload:
     s = lambda n: max(1, int(round(n * scale)))
     return ExtendWorkload("extend_b16_prefix16k_chunk2k_kv8", BASE_SEED + 5, num_layers, 16,
                           s(16384), s(2048), 8, KVDist("normal", 0.02, outlier=6.0, frac=0.002))
+
+
+# --------------------------------------------------------------------------
+# extend attention over a given FP8 workspace (ragged cases for the tests)
+# --------------------------------------------------------------------------
+
+def fp8_bytes_by_field(rng: np.random.Generator, shape, exp_lo: int, exp_hi: int) -> np.ndarray:
+    """Random E4M3 bytes drawn field by field: a uniform sign bit, a uniform
+    4-bit exponent field in [exp_lo, exp_hi] and a uniform 3-bit mantissa
+    (exp_hi <= 14 keeps clear of the NaN codes 0x7F / 0xFF)."""
+    sign = rng.integers(0, 2, shape, dtype=np.uint8) << 7
+    exp = rng.integers(exp_lo, exp_hi + 1, shape, dtype=np.uint8) << 3
+    man = rng.integers(0, 8, shape, dtype=np.uint8)
+    return (sign | exp | man).astype(np.uint8)
+
+
+@dataclass
+class ExtendAttnCase:
+    """A ragged extend-attention problem over an FP8 workspace: sequence b has
+    prefix_lens[b] cached rows and chunk_lens[b] new tokens, its rows starting
+    at cu_prefix[b] with `gap` unused rows before the next sequence."""
+    name: str
+    seed: int
+    prefix_lens: np.ndarray
+    chunk_lens: np.ndarray
+    num_q_heads: int
+    num_kv_heads: int
+    gap: int = 3
+    k_exp: tuple = (3, 8)     # E4M3 exponent-field range of K bytes (magnitudes 2^-4 .. 3.75)
+    v_exp: tuple = (1, 9)
+    head_dim: int = HEAD_DIM
+
+    @property
+    def batch(self) -> int:
+        return int(self.prefix_lens.shape[0])
+
+    @property
+    def cu_prefix(self) -> np.ndarray:
+        per = self.prefix_lens.astype(np.int64) + self.chunk_lens.astype(np.int64) + self.gap
+        return np.concatenate([[0], np.cumsum(per)]).astype(np.int64)
+
+    @property
+    def cu_q(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk_lens.astype(np.int64))]).astype(np.int64)
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.cu_prefix[-1])
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_q[-1])
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def workspace(self):
+        """(ws_k, ws_v): uint8 E4M3 [total_rows, Hkv, d], every row drawn (gap rows too)."""
+        rng = np.random.default_rng([self.seed, _S_PROMPT_K])
+        shape = (self.total_rows, self.num_kv_heads, self.head_dim)
+        return fp8_bytes_by_field(rng, shape, *self.k_exp), fp8_bytes_by_field(rng, shape, *self.v_exp)
+
+    def q(self) -> np.ndarray:
+        rng = np.random.default_rng([self.seed, _S_Q])
+        n = self.total_q * self.num_q_heads * self.head_dim
+        return bf16_bits(rng.standard_normal(n, dtype=np.float32)).reshape(
+            self.total_q, self.num_q_heads, self.head_dim)
+
+    def flops(self) -> int:
+        C = self.chunk_lens.astype(np.int64)
+        keys = int((C * self.prefix_lens.astype(np.int64) + C * (C + 1) // 2).sum())
+        return 4 * self.head_dim * self.num_q_heads * keys
+
+
+def extend_attn_case(index: int) -> ExtendAttnCase:
+    """Ragged extend-attention cases for the parity tests.
+
+    1 three sequences, GQA 4 (8 / 2 heads): prefixes {0, 37, 300}, chunks {19, 1, 130}
+    2 GQA 8 (16 / 2 heads), chunks that are not multiples of 16 tokens: prefixes
+      {129, 1000}, chunks {33, 260}
+    3 one sequence, G = 1 (2 / 2 heads), prefix 256, chunk 64
+    4 G = 16 (32 / 2 heads): prefixes {5, 700}, chunks {17, 40}
+    """
+    seed = BASE_SEED + 100 + index
+    a = lambda *v: np.array(v, np.int32)
+    if index == 1:
+        return ExtendAttnCase("extend_attn_gqa4", seed, a(0, 37, 300), a(19, 1, 130), 8, 2)
+    if index == 2:
+        return ExtendAttnCase("extend_attn_gqa8", seed, a(129, 1000), a(33, 260), 16, 2)
+    if index == 3:
+        return ExtendAttnCase("extend_attn_mha", seed, a(256), a(64), 2, 2)
+    if index == 4:
+        return ExtendAttnCase("extend_attn_gqa16", seed, a(5, 700), a(17, 40), 32, 2)
+    raise ValueError(index)

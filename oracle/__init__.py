@@ -79,6 +79,11 @@ def lib():
         L.nvfp4_oracle_tensor_amax.restype = f32
         L.nvfp4_oracle_calibrated_global_scale.argtypes = [f32]
         L.nvfp4_oracle_calibrated_global_scale.restype = f32
+        L.nvfp4_oracle_bf16_to_fp8_workspace.argtypes = [vp, vp, vp, i64, i32, i32, i64, f32, f32, vp, vp]
+        L.nvfp4_oracle_bf16_to_fp8_workspace.restype = ctypes.c_int
+        L.nvfp4_oracle_extend_attention_rows.argtypes = [vp, vp, i64, i32, i32, f32, f32, vp, i32, vp, vp, vp,
+                                                         i32, f64, vp, i64, vp]
+        L.nvfp4_oracle_extend_attention_rows.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -230,7 +235,6 @@ def dequantize_rows(cache: Cache, which: str, rows) -> np.ndarray:
     return e2m1[code] * sc * np.float64(np.float32(g))
 
 
-__all__ = [name for name in dir() if not name.startswith("_")]
 
 
 def tensor_amax(x_bf16) -> float:
@@ -242,3 +246,48 @@ def tensor_amax(x_bf16) -> float:
 def calibrated_global_scale(amax: float) -> float:
     """g = amax / (6 * 448) in binary32 (1 when amax is 0)."""
     return float(lib().nvfp4_oracle_calibrated_global_scale(float(np.float32(amax))))
+
+
+def bf16_to_fp8_workspace(k_bf16, v_bf16, ws_rows, ws_k, ws_v, k_ws_scale=1.0, v_ws_scale=1.0) -> int:
+    """The chunk's K/V (bf16 bits [n, Hkv, d]) into workspace rows ws_rows[t]
+    (in place in ws_k, ws_v: uint8 [rows, Hkv, d]); returns the status."""
+    k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bf16, dtype=np.uint16)
+    r = np.ascontiguousarray(ws_rows, dtype=np.int64)
+    assert ws_k.flags["C_CONTIGUOUS"] and ws_v.flags["C_CONTIGUOUS"]
+    n, H, d = k.shape
+    return lib().nvfp4_oracle_bf16_to_fp8_workspace(_ptr(k), _ptr(v), _ptr(r), n, H, d, ws_k.shape[0],
+                                                    float(np.float32(k_ws_scale)), float(np.float32(v_ws_scale)),
+                                                    _ptr(ws_k), _ptr(ws_v))
+
+
+def extend_attention_rows(ws_k, ws_v, q_bf16, cu_q, cu_prefix, prefix_lens, softmax_scale, pairs,
+                          k_ws_scale=1.0, v_ws_scale=1.0):
+    """fp64 extend-attention output rows for (global query token, query head)
+    pairs; q_bf16 [total_q, Hq, d].  Returns (out [len(pairs), d], status)."""
+    wk = np.ascontiguousarray(ws_k, dtype=np.uint8)
+    wv = np.ascontiguousarray(ws_v, dtype=np.uint8)
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    cq = np.ascontiguousarray(cu_q, dtype=np.int64)
+    cp = np.ascontiguousarray(cu_prefix, dtype=np.int64)
+    pl = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    out = np.zeros((pr.shape[0], wk.shape[2]), np.float64)
+    st = lib().nvfp4_oracle_extend_attention_rows(_ptr(wk), _ptr(wv), wk.shape[0], wk.shape[1], wk.shape[2],
+                                                  float(np.float32(k_ws_scale)), float(np.float32(v_ws_scale)),
+                                                  _ptr(q), q.shape[1], _ptr(cq), _ptr(cp), _ptr(pl), pl.shape[0],
+                                                  float(softmax_scale), _ptr(pr), pr.shape[0], _ptr(out))
+    return out, st
+
+
+def extend_attention(ws_k, ws_v, q_bf16, cu_q, cu_prefix, prefix_lens, softmax_scale, k_ws_scale=1.0,
+                     v_ws_scale=1.0):
+    """Every output row: fp64 [total_q, Hq, d] and the status."""
+    total_q, Hq = q_bf16.shape[0], q_bf16.shape[1]
+    pairs = np.stack(np.meshgrid(np.arange(total_q), np.arange(Hq), indexing="ij"), -1).reshape(-1, 2)
+    out, st = extend_attention_rows(ws_k, ws_v, q_bf16, cu_q, cu_prefix, prefix_lens, softmax_scale, pairs,
+                                    k_ws_scale, v_ws_scale)
+    return out.reshape(total_q, Hq, -1), st
+
+
+__all__ = [name for name in dir() if not name.startswith("_")]

@@ -375,6 +375,103 @@ int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int
   return bad;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Extend (chunked prefill) over the FP8 workspace ("nvfp4-kv-cache-memory-  */
+/* wall", section 3, item 2 and the data-flow figure: the chunk attends over */
+/* its cached prefix, dequantised into the FP8 workspace, and over itself;   */
+/* the current tokens' own K/V take part as FP8).                            */
+/*                                                                           */
+/* Readings: the chunk's K/V rows enter the workspace straight from bf16,    */
+/* w = E4M3(fp32(x) / s_ws) with the sign kept; sequence b's rows are        */
+/* cu_prefix[b] + j for its key j, the prefix (j < prefix_lens[b]) first and */
+/* chunk token t at j = prefix_lens[b] + t; token t sees keys 0 .. P_b + t   */
+/* (causal).  Attention is evaluated in binary64 over E4M3val(w) * s_ws.     */
+/* ------------------------------------------------------------------------- */
+
+int nvfp4_oracle_bf16_to_fp8_workspace(const uint16_t* k_bf16, const uint16_t* v_bf16,
+                                       const int64_t* ws_rows, int64_t num_tokens,
+                                       int32_t num_kv_heads, int32_t head_dim, int64_t total_rows,
+                                       float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                       uint8_t* ws_v) {
+  const int64_t row_vals = (int64_t)num_kv_heads * head_dim;
+  int bad = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t row = ws_rows[t];
+    if (row < 0) continue; /* padding */
+    if (row >= total_rows) { bad = 1; continue; }
+    for (int which = 0; which < 2; ++which) {
+      const uint16_t* x = (which == 0 ? k_bf16 : v_bf16) + t * row_vals;
+      uint8_t* w = (which == 0 ? ws_k : ws_v) + row * row_vals;
+      const float sws = which == 0 ? k_ws_scale : v_ws_scale;
+      for (int64_t i = 0; i < row_vals; ++i) {
+        const float z = nvfp4_oracle_bf16_to_float(x[i]) / sws;
+        w[i] = nvfp4_oracle_e4m3_encode(z);
+      }
+    }
+  }
+  return bad;
+}
+
+/* The sequence holding global query token i (cu_q non-decreasing), or -1. */
+static int32_t sequence_of(const int64_t* cu_q, int32_t batch, int64_t i) {
+  for (int32_t b = 0; b < batch; ++b)
+    if (i >= cu_q[b] && i < cu_q[b + 1]) return b;
+  return -1;
+}
+
+int nvfp4_oracle_extend_attention_rows(const uint8_t* ws_k, const uint8_t* ws_v, int64_t total_rows,
+                                       int32_t num_kv_heads, int32_t head_dim, float k_ws_scale,
+                                       float v_ws_scale, const uint16_t* q_bf16, int32_t num_q_heads,
+                                       const int64_t* cu_q, const int64_t* cu_prefix,
+                                       const int32_t* prefix_lens, int32_t batch,
+                                       double softmax_scale, const int64_t* pairs, int64_t num_pairs,
+                                       double* out) {
+  const int d = head_dim, H = num_kv_heads;
+  if (d > 512 || H <= 0 || num_q_heads % H != 0) return -1;
+  const int G = num_q_heads / H;
+  int bad = 0;
+  value_tables vt;
+  build_tables(&vt);
+  for (int64_t n = 0; n < num_pairs; ++n) {
+    const int64_t i = pairs[2 * n];
+    const int hq = (int)pairs[2 * n + 1];
+    double* o = out + n * d;
+    for (int dd = 0; dd < d; ++dd) o[dd] = 0.0;
+    const int32_t b = sequence_of(cu_q, batch, i);
+    if (b < 0 || hq < 0 || hq >= num_q_heads) { bad = 1; continue; }
+    const int64_t t = i - cu_q[b];
+    const int64_t L = (int64_t)prefix_lens[b] + t + 1; /* keys 0 .. P_b + t */
+    const int hk = hq / G;
+    double q[512];
+    for (int dd = 0; dd < d; ++dd)
+      q[dd] = nvfp4_oracle_bf16_to_float(q_bf16[(i * num_q_heads + hq) * d + dd]);
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    double m = -INFINITY;
+    int ok = 1;
+    for (int64_t j = 0; j < L; ++j) {
+      const int64_t row = cu_prefix[b] + j;
+      if (row < 0 || row >= total_rows) { ok = 0; break; }
+      const uint8_t* kr = ws_k + (row * H + hk) * d;
+      double acc = 0.0;
+      for (int dd = 0; dd < d; ++dd)
+        acc += q[dd] * (vt.e4m3[kr[dd]] * (double)k_ws_scale);
+      s[j] = softmax_scale * acc;
+      if (s[j] > m) m = s[j];
+    }
+    if (!ok) { bad = 1; free(s); continue; }
+    double l = 0.0;
+    for (int64_t j = 0; j < L; ++j) {
+      const double w = exp(s[j] - m);
+      l += w;
+      const uint8_t* vr = ws_v + ((cu_prefix[b] + j) * H + hk) * d;
+      for (int dd = 0; dd < d; ++dd) o[dd] += w * (vt.e4m3[vr[dd]] * (double)v_ws_scale);
+    }
+    for (int dd = 0; dd < d; ++dd) o[dd] /= l;
+    free(s);
+  }
+  return bad;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the FP32
  * per-tensor scale is left at 1 by the uncalibrated public setting, and a

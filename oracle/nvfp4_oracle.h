@@ -70,6 +70,25 @@ int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int
                                           float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
                                           uint8_t* ws_v);
 
+/* Extend over the FP8 workspace.  The chunk's K/V rows enter the workspace
+ * from bf16 (w = E4M3(fp32(x) / s_ws), signed); ws_rows[t] < 0 skips token t.
+ * Extend attention evaluates, in binary64, the output rows named by pairs
+ * (global query token i, query head h): sequence b of token i attends from
+ * chunk position t = i - cu_q[b] over keys 0 .. prefix_lens[b] + t, key j
+ * being workspace row cu_prefix[b] + j, dequantised as E4M3val(w) * s_ws. */
+int nvfp4_oracle_bf16_to_fp8_workspace(const uint16_t* k_bf16, const uint16_t* v_bf16,
+                                       const int64_t* ws_rows, int64_t num_tokens,
+                                       int32_t num_kv_heads, int32_t head_dim, int64_t total_rows,
+                                       float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                       uint8_t* ws_v);
+int nvfp4_oracle_extend_attention_rows(const uint8_t* ws_k, const uint8_t* ws_v, int64_t total_rows,
+                                       int32_t num_kv_heads, int32_t head_dim, float k_ws_scale,
+                                       float v_ws_scale, const uint16_t* q_bf16, int32_t num_q_heads,
+                                       const int64_t* cu_q, const int64_t* cu_prefix,
+                                       const int32_t* prefix_lens, int32_t batch,
+                                       double softmax_scale, const int64_t* pairs, int64_t num_pairs,
+                                       double* out);
+
 #ifdef __cplusplus
 }
 #endif
