@@ -69,8 +69,10 @@ enum {
   NVFP4KV_DEVERR_SLOT = 1,   /* a slot >= num_pages * page_size: that token was skipped */
   NVFP4KV_DEVERR_PAGE = 2,   /* a page id outside [0, num_pages): that page was skipped */
   NVFP4KV_DEVERR_LENGTH = 4, /* a length < 0 or > max_pages_per_seq * page_size: clamped */
-  NVFP4KV_DEVERR_TIMEOUT = 8 /* a copy into shared memory did not complete within ~1 s: the
-                                call's outputs are not valid */
+  NVFP4KV_DEVERR_TIMEOUT = 8, /* a copy into shared memory (or a tensor-core step) did not
+                                 complete within ~1 s: the call's outputs are not valid */
+  NVFP4KV_DEVERR_ROW = 16     /* a workspace row outside [0, total_rows): that row was skipped
+                                 (an attention key reads as zero) */
 };
 
 /* One layer's paged NVFP4 cache.  The struct itself is read on the host only. */

@@ -27,6 +27,7 @@ NVFP4KV_DEVERR_SLOT = 1
 NVFP4KV_DEVERR_PAGE = 2
 NVFP4KV_DEVERR_LENGTH = 4
 NVFP4KV_DEVERR_TIMEOUT = 8
+NVFP4KV_DEVERR_ROW = 16
 
 HEAD_DIM = 128
 PAGE_SIZE = 16
@@ -84,13 +85,17 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_append_decode_attention.argtypes = [pc, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz,
                                                   vp, vp]
     L.nvfp4kv_tensor_amax.argtypes = [vp, i64, vp, ctypes.c_int, vp]
+    L.nvfp4kv_bf16_to_fp8_workspace.argtypes = [vp, vp, vp, i64, i32, i32, i64, f32, f32, vp, vp, vp, vp]
+    L.nvfp4kv_extend_attention.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32, f32, f32, f32, vp,
+                                           vp, vp]
     L.nvfp4kv_calibrated_global_scale.argtypes = [f32, ctypes.POINTER(f32)]
     L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
     L.nvfp4kv_status_string.restype = ctypes.c_char_p
     for name in ("nvfp4kv_cache_bytes", "nvfp4kv_quantize_append", "nvfp4kv_decode_workspace_size",
                  "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
                  "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
-                 "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale"):
+                 "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
+                 "nvfp4kv_extend_attention"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -252,6 +257,32 @@ def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_p
                                                  _ptr(device_status), _stream(stream)))
 
 
+def nvfp4kv_bf16_to_fp8_workspace(k, v, ws_rows, ws_k, ws_v, k_ws_scale: float = 1.0, v_ws_scale: float = 1.0,
+                                  device_status=None, stream=None) -> None:
+    """The chunk's K/V (bf16 [n, Hkv, 128]) into FP8 workspace rows ws_rows[t] (int64 [n]; < 0 skips)
+    of ws_k, ws_v (uint8 [total_rows, Hkv, 128])."""
+    n, hkv, d = (int(x) for x in k.shape)
+    _check("nvfp4kv_bf16_to_fp8_workspace",
+           _L().nvfp4kv_bf16_to_fp8_workspace(_ptr(k), _ptr(v), _ptr(ws_rows), n, hkv, d, int(ws_k.shape[0]),
+                                              float(k_ws_scale), float(v_ws_scale), _ptr(ws_k), _ptr(ws_v),
+                                              _ptr(device_status), _stream(stream)))
+
+
+def nvfp4kv_extend_attention(q, cu_q, max_q_len: int, ws_k, ws_v, cu_prefix, prefix_lens, out,
+                             softmax_scale: float, k_ws_scale: float = 1.0, v_ws_scale: float = 1.0,
+                             device_status=None, stream=None) -> None:
+    """Causal extend attention of the chunk queries q (bf16 [total_q, Hq, 128]; sequence b owns
+    [cu_q[b], cu_q[b+1])) over the FP8 workspace (uint8 [total_rows, Hkv, 128]; sequence b's key j
+    at row cu_prefix[b] + j, prefix_lens[b] cached keys first); out: fp32 [total_q, Hq, 128]."""
+    B = int(prefix_lens.shape[0])
+    hq, d = int(q.shape[1]), int(q.shape[2])
+    _check("nvfp4kv_extend_attention",
+           _L().nvfp4kv_extend_attention(_ptr(q), _ptr(cu_q), int(max_q_len), _ptr(ws_k), _ptr(ws_v),
+                                         _ptr(cu_prefix), _ptr(prefix_lens), B, int(ws_k.shape[0]), hq,
+                                         int(ws_k.shape[1]), d, float(k_ws_scale), float(v_ws_scale),
+                                         float(softmax_scale), _ptr(out), _ptr(device_status), _stream(stream)))
+
+
 def nvfp4kv_tensor_amax(x, amax, accumulate: bool = False, stream=None) -> None:
     """max |x| of a contiguous bf16 device tensor into amax (a float32 device tensor of one element);
     with accumulate, max(amax, max |x|)."""
@@ -276,4 +307,5 @@ def nvfp4kv_calibrated_global_scale(amax: float) -> float:
 __all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
            "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
-           "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale"]
+           "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
+           "nvfp4kv_extend_attention"]

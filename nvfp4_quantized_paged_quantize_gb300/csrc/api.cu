@@ -181,6 +181,57 @@ int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, c
                                             workspace, device_status, nsm, s, num_tokens > 0));
 }
 
+int nvfp4kv_bf16_to_fp8_workspace(const void* k_bf16, const void* v_bf16, const int64_t* ws_rows,
+                                   int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                   int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                   uint8_t* ws_v, int32_t* device_status, nvfp4kv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || total_rows < 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (head_dim != 128) return NVFP4KV_ERR_UNSUPPORTED;
+  if (!std::isfinite(k_ws_scale) || !std::isfinite(v_ws_scale) || k_ws_scale <= 0.0f || v_ws_scale <= 0.0f)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return NVFP4KV_OK;
+  if (!k_bf16 || !v_bf16 || !ws_rows || !ws_k || !ws_v) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_bf16, 16) || !aligned(v_bf16, 16) || !aligned(ws_rows, 8) || !aligned(ws_k, 16) ||
+      !aligned(ws_v, 16))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_tokens > (INT64_MAX / 2) / ((int64_t)num_kv_heads * 16)) return NVFP4KV_ERR_UNSUPPORTED;
+  int nsm = 0;
+  const int st = current_num_sms(&nsm);
+  if (st != NVFP4KV_OK) return st;
+  return cuda_status(nvfp4kv::launch_chunk_to_ws(static_cast<const uint16_t*>(k_bf16),
+                                                 static_cast<const uint16_t*>(v_bf16), ws_rows, num_tokens,
+                                                 num_kv_heads, total_rows, k_ws_scale, v_ws_scale, ws_k, ws_v,
+                                                 device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4kv_extend_attention(const void* q_bf16, const int64_t* cu_q, int32_t max_q_len, const uint8_t* ws_k,
+                             const uint8_t* ws_v, const int64_t* cu_prefix, const int32_t* prefix_lens,
+                             int32_t batch, int64_t total_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, float k_ws_scale, float v_ws_scale, float softmax_scale,
+                             float* out, int32_t* device_status, nvfp4kv_stream_t stream) {
+  if (batch < 0 || max_q_len < 0 || total_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % num_kv_heads != 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  const int32_t group = num_q_heads / num_kv_heads;
+  if (head_dim != 128 || group > 128 || (group & (group - 1)) != 0 || batch > 65535 || num_kv_heads > 65535)
+    return NVFP4KV_ERR_UNSUPPORTED;
+  for (float sc : {k_ws_scale, v_ws_scale, softmax_scale})
+    if (!std::isfinite(sc) || sc <= 0.0f) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (batch == 0 || max_q_len == 0) return NVFP4KV_OK;
+  if (!q_bf16 || !cu_q || !ws_k || !ws_v || !cu_prefix || !prefix_lens || !out)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_bf16, 16) || !aligned(out, 16) || !aligned(ws_k, 16) || !aligned(ws_v, 16) || !aligned(cu_q, 8) ||
+      !aligned(cu_prefix, 8) || !aligned(prefix_lens, 4))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if ((int64_t)max_q_len * group > (int64_t)INT32_MAX) return NVFP4KV_ERR_UNSUPPORTED;
+  return cuda_status(nvfp4kv::launch_extend_attention(
+      static_cast<const uint16_t*>(q_bf16), cu_q, max_q_len, ws_k, ws_v, cu_prefix, prefix_lens, batch,
+      total_rows, num_q_heads, num_kv_heads, k_ws_scale, v_ws_scale, softmax_scale, out, device_status,
+      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int nvfp4kv_tensor_amax(const void* x_bf16, int64_t n, float* amax, int accumulate,
                         nvfp4kv_stream_t stream) {
   if (n < 0 || amax == nullptr || !aligned(amax, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;

@@ -72,10 +72,12 @@ __device__ __forceinline__ uint32_t convert_pair_general(uint32_t w, uint32_t s1
   const float a0 = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), g);
   const float a1 = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), g);
   float z0, z1;
-  if (fast && fabsf(a0) < 0x1p+64f && fabsf(a1) < 0x1p+64f) {
-    // correctly rounded a / sws (Markstein); the sign of a zero quotient is the sign of a
-    z0 = copysignf(__fmaf_rn(__fmaf_rn(-__fmul_rn(a0, rs), sws, a0), rs, __fmul_rn(a0, rs)), a0);
-    z1 = copysignf(__fmaf_rn(__fmaf_rn(-__fmul_rn(a1, rs), sws, a1), rs, __fmul_rn(a1, rs)), a1);
+  const float q0 = __fmul_rn(a0, rs), q1 = __fmul_rn(a1, rs);
+  if (fast && fabsf(q0) < 0x1p+64f && fabsf(q1) < 0x1p+64f) {
+    // correctly rounded a / sws (Markstein) while the first quotient stays far from
+    // overflow; the sign of a zero quotient is the sign of a
+    z0 = copysignf(__fmaf_rn(__fmaf_rn(-q0, sws, a0), rs, q0), a0);
+    z1 = copysignf(__fmaf_rn(__fmaf_rn(-q1, sws, a1), rs, q1), a1);
   } else {
     z0 = __fdiv_rn(a0, sws);
     z1 = __fdiv_rn(a1, sws);

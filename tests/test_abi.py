@@ -150,3 +150,28 @@ def test_calibration_host_checks_and_scale(lib):
         got = np.float32(kv.nvfp4kv_calibrated_global_scale(float(a)))
         want = np.float32(calibrated_global_scale(float(a)))
         assert got.tobytes() == want.tobytes(), a
+
+
+def test_extend_host_checks(lib):
+    f = lib.nvfp4kv_extend_attention
+    # (q, cu_q, max_q_len, ws_k, ws_v, cu_prefix, prefix_lens, batch, total_rows, hq, hkv, d, sk, sv, scale, out, st, stream)
+    ok = [16, 8, 4, 16, 16, 8, 4, 2, 100, 8, 2, 128, 1.0, 1.0, 0.1, 16, None, None]
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a9=6) == kv.NVFP4KV_ERR_UNSUPPORTED           # group 3: not a power of two
+    assert call(a9=7) == kv.NVFP4KV_ERR_INVALID_ARGUMENT      # 7 % 2 != 0
+    assert call(a11=64) == kv.NVFP4KV_ERR_UNSUPPORTED         # head_dim
+    assert call(a12=0.0) == kv.NVFP4KV_ERR_INVALID_ARGUMENT   # workspace scale
+    assert call(a14=float("nan")) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert call(a0=18) == kv.NVFP4KV_ERR_INVALID_ARGUMENT     # misaligned q
+    assert call(a5=12) == kv.NVFP4KV_ERR_INVALID_ARGUMENT     # misaligned cu_prefix
+    assert call(a7=-1) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert call(a7=0) == kv.NVFP4KV_OK and call(a2=0) == kv.NVFP4KV_OK   # nothing to do
+    g = lib.nvfp4kv_bf16_to_fp8_workspace
+    assert g(16, 16, 8, 4, 2, 64, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_UNSUPPORTED
+    assert g(16, 16, 8, 4, 2, 128, 10, -1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert g(16, 16, 12, 4, 2, 128, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert g(None, None, None, 0, 2, 128, 10, 1.0, 1.0, None, None, None, None) == kv.NVFP4KV_OK

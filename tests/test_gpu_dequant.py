@@ -115,7 +115,10 @@ def test_full_size_layer_sampled_rows(cuda_lib):
 
 
 @pytest.mark.parametrize("gk,gv,sk,sv", [(1.0, 1.0, 1.0, 1.0), (0.37, 2.5, 6.0, 1e-3), (1e30, 1e-20, 1e-10, 1e31),
-                                         (1.0, 3.0, 1e-35, 1e35), (1 / 2688, 2.9e-3, 6 / 2688, 6 * 2.9e-3)])
+                                         (1.0, 3.0, 1e-35, 1e35), (1 / 2688, 2.9e-3, 6 / 2688, 6 * 2.9e-3),
+                                         # workspace scales inside [2^-100, 2^100] whose quotients overflow
+                                         # (saturate to 448) or pass 2^64
+                                         (1e10, 1.0, 1e-29, 2.0 ** -99)])
 def test_every_code_and_scale_bit_exact(cuda_lib, gk, gv, sk, sv):
     # One KV head, two pages: block j of row r holds scale byte 8 r + j (every
     # non-negative, non-NaN E4M3 byte once per page) and the 16 E2M1 codes
