@@ -454,6 +454,27 @@ def secondary(torch, kv, args, flush, hbm_peak):
     gbs = ew.quantize_bytes_per_layer() / (t / 1e3) / 1e9
     out["extend_quantize_2048x16_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak,
                                                 "x80_layers_ms": 80 * t}
+    # the chunk's own K/V into the workspace, then the extend attention over it
+    rows = _dev(torch, ew.chunk_ws_rows())
+    ms, _ = time_steps(torch, steps, args.warmup,
+                       lambda ev=None: kv.nvfp4kv_bf16_to_fp8_workspace(kc, vc, rows, wk, wv), flush)
+    t = float(np.mean(ms))
+    vals = 2 * kc.numel()
+    gbs = (3 * vals + 8 * ew.batch * ew.chunk_len) / (t / 1e3) / 1e9
+    out["extend_chunk_to_fp8_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak}
+    q = _bf16(torch, ew.q(0))
+    cq = _dev(torch, ew.cu_q)
+    o = torch.empty((q.shape[0], ew.num_q_heads, 128), dtype=torch.float32, device="cuda")
+    attn = lambda ev=None: kv.nvfp4kv_extend_attention(q, cq, ew.chunk_len, wk, wv, cu, pl, o, ew.softmax_scale)
+    ms, _ = time_steps(torch, max(3, min(steps, 10)), args.warmup, attn, flush)
+    t = float(np.mean(ms))
+    tflops = ew.attention_flops_per_layer() / (t / 1e3) / 1e12
+    peak = measured_peaks()[0]["bf16_tflops"]
+    out["extend_attention_per_layer"] = {
+        "kernel_ms": t, "tflops": tflops, "frac_of_measured_bf16_peak": tflops / peak,
+        "flops": ew.attention_flops_per_layer(), "x80_layers_ms": 80 * t,
+        "note": "f16 operands (the tensor-core rate of bf16), f32 accumulate; 16 x 2048 queries x 64 heads over "
+                "16384 + causal chunk keys"}
     return out
 
 
@@ -619,9 +640,16 @@ def only_arm(args):
         pt, pl, cu = _dev(torch, ew.page_table), _dev(torch, ew.prefix_lens), _dev(torch, ew.cu_prefix)
         wk = torch.empty((ew.total_rows, ew.num_kv_heads, 128), dtype=torch.uint8, device="cuda")
         wv = torch.empty_like(wk)
+        rows = _dev(torch, ew.chunk_ws_rows())
+        q = _bf16(torch, ew.q(0))
+        cq = _dev(torch, ew.cu_q)
+        o = torch.empty((q.shape[0], ew.num_q_heads, 128), dtype=torch.float32, device="cuda")
         time_steps(torch, args.steps, args.warmup,
                    lambda ev=None: (kv.nvfp4kv_dequant_to_fp8_workspace(cache, pt, pl, cu, wk, wv),
-                                    kv.nvfp4kv_quantize_append(cache, kc, vc, slots)), flush)
+                                    kv.nvfp4kv_quantize_append(cache, kc, vc, slots),
+                                    kv.nvfp4kv_bf16_to_fp8_workspace(kc, vc, rows, wk, wv),
+                                    kv.nvfp4kv_extend_attention(q, cq, ew.chunk_len, wk, wv, cu, pl, o,
+                                                                ew.softmax_scale)), flush)
     torch.cuda.synchronize()
     print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, "ok": True}))
 

@@ -273,6 +273,10 @@ int nvfp4kv_tensor_amax(const void* x_bf16, int64_t n, float* amax, int accumula
                         nvfp4kv_stream_t stream);
 int nvfp4kv_calibrated_global_scale(float amax, float* g);
 
+/* Text of the CUDA error behind this thread's latest NVFP4KV_ERR_CUDA (the
+ * runtime's own message; "no CUDA error" if there was none).  Never NULL. */
+const char* nvfp4kv_last_cuda_error(void);
+
 /* A static, human-readable string for a status code (never NULL). */
 const char* nvfp4kv_status_string(int status);
 

@@ -39,6 +39,8 @@ class Nvfp4kvError(RuntimeError):
     def __init__(self, func: str, status: int):
         self.status = status
         msg = nvfp4kv_status_string(status) if _lib is not None else str(status)
+        if _lib is not None and status == NVFP4KV_ERR_CUDA:
+            msg += ": " + _lib.nvfp4kv_last_cuda_error().decode()
         super().__init__(f"{func} failed: {msg} ({status})")
 
 
@@ -89,6 +91,8 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_extend_attention.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32, f32, f32, f32, vp,
                                            vp, vp]
     L.nvfp4kv_calibrated_global_scale.argtypes = [f32, ctypes.POINTER(f32)]
+    L.nvfp4kv_last_cuda_error.argtypes = []
+    L.nvfp4kv_last_cuda_error.restype = ctypes.c_char_p
     L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
     L.nvfp4kv_status_string.restype = ctypes.c_char_p
     for name in ("nvfp4kv_cache_bytes", "nvfp4kv_quantize_append", "nvfp4kv_decode_workspace_size",

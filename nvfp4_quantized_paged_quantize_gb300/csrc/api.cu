@@ -57,7 +57,14 @@ int check_cache(const nvfp4kv_cache* c) {
   return NVFP4KV_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA; }
+// the last CUDA error a call of this thread returned NVFP4KV_ERR_CUDA for
+thread_local cudaError_t last_cuda_error = cudaSuccess;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NVFP4KV_OK;
+  last_cuda_error = e;
+  return NVFP4KV_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -271,6 +278,10 @@ int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* 
   return cuda_status(nvfp4kv::launch_dequant_fp8(*cache, page_table, max_pages_per_seq, prefix_lens, cu_prefix,
                                                  batch, total_rows, k_ws_scale, v_ws_scale, ws_k, ws_v,
                                                  device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* nvfp4kv_last_cuda_error(void) {
+  return last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(last_cuda_error);
 }
 
 const char* nvfp4kv_status_string(int status) {

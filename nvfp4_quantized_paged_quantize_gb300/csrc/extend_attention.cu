@@ -13,8 +13,9 @@
 // keys 0 .. prefix + t), on the fifth-generation tensor cores.
 //   - A CTA owns 128 query rows of one (sequence, KV head): 128 / G tokens x
 //     the G query heads that share the KV head, so each K/V tile feeds all G.
-//   - Warps 4-7 load K/V tiles of 128 keys, convert E4M3 -> f16 (exact) and
-//     store them as MMA operands (K K-major, V MN-major) in a two-stage ring.
+//   - Warps 4-7 load K/V tiles of 128 keys (one tile ahead, into registers),
+//     convert E4M3 -> f16 (exact) and store them as MMA operands (K K-major,
+//     V MN-major) in a two-stage ring.
 //   - Warp 8 issues, from one thread, S = Q K^T (f16 x f16 -> f32 in TMEM,
 //     two S buffers) and O += P V (O in TMEM) and commits each to an mbarrier.
 //   - Warps 0-3 own one query row per thread (TMEM lane = row): they read the
@@ -241,31 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
     // ------------------------------------------------------------ loaders
     const int l = threadIdx.x - kSoftmaxWarps * 32;  // 0 .. 127
-    {
-      // Q: thread l converts query row l (token t0 + l / G, head hk * G + l % G)
-      const int64_t t = t0 + (l >> p.log2_group);
-      const bool live = t < C;
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + ((q0 + (live ? t : 0)) * p.hq + hk * G + (l & (G - 1))) * kHeadDim);
-#pragma unroll 4
-      for (int c = 0; c < kHeadDim / 8; ++c) {
-        const uint4 x = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        st_shared_v4(sQ + kmajor_off(l, 8 * c), bf16x8_to_f16x8(x));
-      }
-      tc::fence_smem_to_async();
-      mbar_arrive(b_q);
-    }
-    // K / V tiles: lane (key 8 g + (lane & 7), part lane >> 3) of a warp's 32 keys
+    // K / V tiles: lane (key 8 g + (lane & 7), part lane >> 3) of a warp's 32 keys;
+    // a tile's 16-byte loads are issued one step ahead (into registers) so that
+    // their latency overlaps the wait for the stage they go to
     const int lw = warp - kSoftmaxWarps;
     const int part = lane >> 3;
-    bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      const int s = i & 1;
-      if (i >= 2 && !mbar_wait(b_kve[s], ((i >> 1) - 1) & 1, kWaitNs)) {
-        ok = false;
-        break;
-      }
-      uint4 xk[4][2], xv[4][2];
+    uint4 xk[4][2], xv[4][2];
+    auto load_tile = [&](int i) {
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const int key = lw * 32 + g * 8 + (lane & 7);
@@ -283,6 +266,29 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
           xv[g][h] = live ? __ldg(reinterpret_cast<const uint4*>(p.ws_v + off + h * 64)) : make_uint4(0, 0, 0, 0);
         }
       }
+    };
+    load_tile(0);
+    {
+      // Q: thread l converts query row l (token t0 + l / G, head hk * G + l % G)
+      const int64_t t = t0 + (l >> p.log2_group);
+      const bool live = t < C;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.q + ((q0 + (live ? t : 0)) * p.hq + hk * G + (l & (G - 1))) * kHeadDim);
+#pragma unroll 4
+      for (int c = 0; c < kHeadDim / 8; ++c) {
+        const uint4 x = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        st_shared_v4(sQ + kmajor_off(l, 8 * c), bf16x8_to_f16x8(x));
+      }
+      tc::fence_smem_to_async();
+      mbar_arrive(b_q);
+    }
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i & 1;
+      if (i >= 2 && !mbar_wait(b_kve[s], ((i >> 1) - 1) & 1, kWaitNs)) {
+        ok = false;
+        break;
+      }
       const uint32_t sK = sK0 + s * kTileBytes, sV = sV0 + s * kTileBytes;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -298,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
       }
       tc::fence_smem_to_async();
       mbar_arrive(b_kvf[s]);
+      if (i + 1 < ntiles) load_tile(i + 1);
     }
     if (!ok) flag_error(p.status, NVFP4KV_DEVERR_TIMEOUT);
   } else if (warp == kMmaWarp) {
@@ -366,29 +373,41 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[c4 * 32 + j] = __uint_as_float(v[j]);
       }
-      const int64_t j0 = (int64_t)i * kTileN;
-      float mx = -INFINITY;
+      // keys c <= lim of this tile are visible to the row (all of them away from
+      // the causal edge, none for a row past the chunk)
+      const int64_t lim64 = live ? kmax - (int64_t)i * kTileN : -1;
+      const int lim = lim64 >= kTileN - 1 ? kTileN - 1 : (int)(lim64 < -1 ? -1 : lim64);
+      float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (lim == kTileN - 1) {
 #pragma unroll
-      for (int c = 0; c < kTileN; ++c) {
-        const float y = (live && j0 + c <= kmax) ? x[c] * p.score_scale : -INFINITY;
-        x[c] = y;
-        mx = fmaxf(mx, y);
+        for (int c = 0; c < kTileN; ++c) mr[c & 3] = fmaxf(mr[c & 3], x[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c) {
+          if (c > lim) x[c] = -INFINITY;
+          mr[c & 3] = fmaxf(mr[c & 3], x[c]);
+        }
       }
+      // the row max in base-2 units (the scale is positive, so it commutes with max)
+      const float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * p.score_scale;
       float alpha = 1.0f;
       const bool grow = mx > m + kLazy;  // false for rows with nothing visible (mx = -inf)
       if (grow) {
         alpha = ex2(m - mx);  // 0 on the first visible tile (m = -inf)
         m = mx;
       }
+      // p = 2^(s * scale - m); masked scores are -inf and give 0, and so does
+      // every score of a row past the chunk (offset -inf)
+      const float off = live ? -m : -INFINITY;
       uint32_t ph[kTileN / 2];
-      float lt = 0.0f;
+      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int c = 0; c < kTileN; c += 2) {
-        const float p0 = live ? ex2(x[c] - m) : 0.0f, p1 = live ? ex2(x[c + 1] - m) : 0.0f;
+        const float p0 = ex2(fmaf(x[c], p.score_scale, off)), p1 = ex2(fmaf(x[c + 1], p.score_scale, off));
         ph[c / 2] = f16x2_bits(p0, p1);
-        const __half2 h = *reinterpret_cast<const __half2*>(&ph[c / 2]);
-        lt += __low2float(h) + __high2float(h);
+        ls[(c >> 1) & 3] += p0 + p1;
       }
+      const float lt = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (i >= 1) {
         // the previous P V must be done before P is overwritten and O rescaled
         if (!mbar_wait(b_o, (i - 1) & 1, kWaitNs)) {
