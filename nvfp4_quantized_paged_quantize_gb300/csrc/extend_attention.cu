@@ -13,15 +13,18 @@
 // keys 0 .. prefix + t), on the fifth-generation tensor cores.
 //   - A CTA owns 128 query rows of one (sequence, KV head): 128 / G tokens x
 //     the G query heads that share the KV head, so each K/V tile feeds all G.
-//   - Warps 4-7 load K/V tiles of 128 keys (one tile ahead, into registers),
-//     convert E4M3 -> f16 (exact) and store them as MMA operands (K K-major,
-//     V MN-major) in a two-stage ring.
-//   - Warp 8 issues, from one thread, S = Q K^T (f16 x f16 -> f32 in TMEM,
-//     two S buffers) and O += P V (O in TMEM) and commits each to an mbarrier.
+//   - Warps 4-7 write the Q rows (f16) into TMEM, then load K/V tiles of 128
+//     keys (one tile ahead, into registers), convert E4M3 -> f16 (exact) and
+//     store them as B operands in shared memory (K K-major, V MN-major) in a
+//     three-stage ring.
+//   - Warp 8 issues, from one thread, S = Q K^T and O += P V with the A
+//     operand (Q, P) read from TMEM and f32 accumulators in TMEM (two S
+//     buffers, one O), and commits each to an mbarrier.  Only the B operands
+//     pass through shared memory.
 //   - Warps 0-3 own one query row per thread (TMEM lane = row): they read the
 //     S row, mask, run a lazy base-2 online softmax (the running max moves
-//     only when it grows by 2^8, rescaling O in TMEM), and write P (f16) as the
-//     A operand of the next P V.  At the end: O * s_ws(V) / l -> fp32 out.
+//     only when it grows by 2^8, rescaling O in TMEM), and write P (f16) into
+//     TMEM.  At the end: O * s_ws(V) / l -> fp32 out.
 // Every wait is bounded: a stalled pipeline flags NVFP4KV_DEVERR_TIMEOUT,
 // drains its MMAs and frees its TMEM.
 #include "nvfp4kv_device.cuh"
@@ -110,10 +113,13 @@ constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
 constexpr uint32_t kLBO = 128;   // next core matrix along K
 constexpr uint32_t kSBO = 2048;  // next 8-row (M / N) group: 16 core matrices of 128 B
 constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // one f16 operand tile, 32 KB
-constexpr uint32_t kOffQ = 0, kOffK = kTileBytes, kOffV = 3 * kTileBytes, kOffP = 5 * kTileBytes;
-constexpr uint32_t kSmemBytes = 6 * kTileBytes;  // 192 KB: one CTA per SM
-constexpr uint32_t kTmemCols = 512;              // S[0] at 0, S[1] at 128, O at 256
-constexpr uint32_t kTmemO = 256;
+constexpr int kStages = 3;                              // K / V ring depth
+constexpr uint32_t kOffK = 0, kOffV = kStages * kTileBytes;
+constexpr uint32_t kSmemBytes = 2 * kStages * kTileBytes;  // 192 KB: one CTA per SM
+// TMEM columns: S[0] 0-127, S[1] 128-255, O 256-383 (f32); Q 384-447 and
+// P 448-511 (f16 pairs: the A operands of S = Q K^T and O += P V)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256, kTmemQ = 384, kTmemP = 448;
 constexpr float kLazy = 8.0f;  // the running max moves only when a row max exceeds it by this (base 2)
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -177,8 +183,8 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t lo, uint32_t hi) {
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full;
   uint64_t o_done;
@@ -212,19 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
   const int ntiles = (int)((nkeys + kTileN - 1) / kTileN);
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + kOffQ, sK0 = sbase + kOffK, sV0 = sbase + kOffV, sP = sbase + kOffP;
+  const uint32_t sK0 = sbase + kOffK, sV0 = sbase + kOffV;
   const uint32_t b_q = smem_u32(&bars.q_full), b_p = smem_u32(&bars.p_full), b_o = smem_u32(&bars.o_done);
-  const uint32_t b_kvf[2] = {smem_u32(&bars.kv_full[0]), smem_u32(&bars.kv_full[1])};
-  const uint32_t b_kve[2] = {smem_u32(&bars.kv_empty[0]), smem_u32(&bars.kv_empty[1])};
+  const uint32_t b_kvf0 = smem_u32(&bars.kv_full[0]), b_kve0 = smem_u32(&bars.kv_empty[0]);  // 8 bytes apart
   const uint32_t b_s[2] = {smem_u32(&bars.s_full[0]), smem_u32(&bars.s_full[1])};
   const uint32_t b_drain = smem_u32(&bars.drain);
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, kLoadWarps * 32);
-    mbar_init(b_kvf[0], kLoadWarps * 32);
-    mbar_init(b_kvf[1], kLoadWarps * 32);
-    mbar_init(b_kve[0], 1);
-    mbar_init(b_kve[1], 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(b_kvf0 + 8 * st, kLoadWarps * 32);
+      mbar_init(b_kve0 + 8 * st, 1);
+    }
     mbar_init(b_s[0], 1);
     mbar_init(b_s[1], 1);
     mbar_init(b_p, kSoftmaxWarps * 32);
@@ -270,22 +275,32 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
     load_tile(0);
     {
       // Q: thread l converts query row l (token t0 + l / G, head hk * G + l % G)
+      // into TMEM lane l (this warp's lane quarter), two d values per column
       const int64_t t = t0 + (l >> p.log2_group);
       const bool live = t < C;
       const uint4* src =
           reinterpret_cast<const uint4*>(p.q + ((q0 + (live ? t : 0)) * p.hq + hk * G + (l & (G - 1))) * kHeadDim);
-#pragma unroll 4
-      for (int c = 0; c < kHeadDim / 8; ++c) {
-        const uint4 x = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        st_shared_v4(sQ + kmajor_off(l, 8 * c), bf16x8_to_f16x8(x));
+      const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemQ;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 h = bf16x8_to_f16x8(live ? __ldg(src + 8 * half + c) : make_uint4(0, 0, 0, 0));
+          w[4 * c] = h.x;
+          w[4 * c + 1] = h.y;
+          w[4 * c + 2] = h.z;
+          w[4 * c + 3] = h.w;
+        }
+        tc::tmem_st32(tq + 32 * half, w);
       }
-      tc::fence_smem_to_async();
+      tc::fence_before_sync();
       mbar_arrive(b_q);
     }
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
-      const int s = i & 1;
-      if (i >= 2 && !mbar_wait(b_kve[s], ((i >> 1) - 1) & 1, kWaitNs)) {
+      const int s = i % kStages;
+      if (i >= kStages && !mbar_wait(b_kve0 + 8 * s, ((i / kStages) - 1) & 1, kWaitNs)) {
         ok = false;
         break;
       }
@@ -303,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
         }
       }
       tc::fence_smem_to_async();
-      mbar_arrive(b_kvf[s]);
+      mbar_arrive(b_kvf0 + 8 * s);
       if (i + 1 < ntiles) load_tile(i + 1);
     }
     if (!ok) flag_error(p.status, NVFP4KV_DEVERR_TIMEOUT);
@@ -315,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
       bool ok = mbar_wait(b_q, 0, kWaitNs);
       for (int i = 0; i <= ntiles && ok; ++i) {
         if (i < ntiles) {
-          const int s = i & 1;
-          if (!mbar_wait(b_kvf[s], (i >> 1) & 1, kWaitNs)) {
+          const int s = i % kStages;
+          if (!mbar_wait(b_kvf0 + 8 * s, (i / kStages) & 1, kWaitNs)) {
             ok = false;
             break;
           }
@@ -324,9 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
           const uint32_t sK = sK0 + s * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            tc::mma_f16(tmem + s * kTileN, tc::smem_desc(sQ + kk * 256, kLBO, kSBO),
-                        tc::smem_desc(sK + kk * 256, kLBO, kSBO), id_qk, kk > 0);
-          tc::commit(b_s[s]);
+            tc::mma_f16_tmem_a(tmem + (i & 1) * kTileN, tmem + kTmemQ + kk * 8, tc::smem_desc(sK + kk * 256, kLBO, kSBO),
+                               id_qk, kk > 0);
+          tc::commit(b_s[i & 1]);
         }
         if (i >= 1) {
           const int pi = i - 1;  // P V of the previous tile
@@ -335,13 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
             break;
           }
           tc::fence_after_sync();
-          const uint32_t sV = sV0 + (pi & 1) * kTileBytes;
+          const uint32_t sV = sV0 + (pi % kStages) * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            tc::mma_f16(tmem + kTmemO, tc::smem_desc(sP + kk * 256, kLBO, kSBO),
-                        tc::smem_desc(sV + kk * 256, kLBO, kSBO), id_pv, (pi > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8, tc::smem_desc(sV + kk * 256, kLBO, kSBO), id_pv,
+                               (pi > 0 || kk > 0) ? 1u : 0u);
           tc::commit(b_o);
-          if (pi + 2 < ntiles) tc::commit(b_kve[pi & 1]);  // a loader waits for this stage
+          if (pi + kStages < ntiles) tc::commit(b_kve0 + 8 * (pi % kStages));  // a loader waits for this stage
         }
       }
       if (!ok) flag_error(p.status, NVFP4KV_DEVERR_TIMEOUT);
@@ -429,10 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
         }
       }
       l = l * alpha + lt;
-#pragma unroll
-      for (int c = 0; c < kTileN / 8; ++c)
-        st_shared_v4(sP + kmajor_off(r, 8 * c), make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]));
-      tc::fence_smem_to_async();
+      // P into TMEM: the A operand of the next P V (two keys per column)
+      tc::tmem_st32(tmem + lane_base + kTmemP, *reinterpret_cast<const uint32_t(*)[32]>(&ph[0]));
+      tc::tmem_st32(tmem + lane_base + kTmemP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&ph[32]));
       tc::fence_before_sync();
       mbar_arrive(b_p);
     }
