@@ -245,6 +245,54 @@ int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* 
                                      uint8_t* ws_v, int32_t* device_status,
                                      nvfp4kv_stream_t stream);
 
+/* Chunked prefill / extend over the FP8 workspace ("nvfp4-kv-cache-memory-
+ * wall", section 3, item 2 and the data-flow figure: the chunk attends over its
+ * cached prefix, dequantised into the FP8 workspace that every layer reuses,
+ * and over itself; the current tokens' own K/V take part as FP8).
+ *
+ * nvfp4kv_bf16_to_fp8_workspace writes the chunk's own K/V rows into the
+ * workspace: ws[ws_rows[t]][h][d] = E4M3(fp32(x) / s_ws), round to nearest
+ * even, sign kept, saturating at +-448 (one correctly rounded binary32
+ * division).  Usually ws_rows[t] = cu_prefix[b] + prefix_lens[b] + (t's
+ * position in its chunk), right after the rows nvfp4kv_dequant_to_fp8_workspace
+ * wrote.
+ *   k_bf16, v_bf16  device bf16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned
+ *   ws_rows         device int64 [num_tokens]; < 0 skips the token; a row
+ *                   >= total_rows is skipped with NVFP4KV_DEVERR_ROW
+ *   head_dim        128 (else NVFP4KV_ERR_UNSUPPORTED)
+ *   k_ws_scale, v_ws_scale   finite, > 0
+ *   ws_k, ws_v      device uint8 E4M3 [total_rows][num_kv_heads][head_dim], 16-byte aligned
+ *
+ * nvfp4kv_extend_attention: for sequence b, chunk token t (query row
+ * cu_q[b] + t) and query head h (KV head h / G, G = num_q_heads /
+ * num_kv_heads), out = softmax(softmax_scale * q . K^T) V over keys
+ * j = 0 .. prefix_lens[b] + t (causal after the prefix), key j being workspace
+ * row cu_prefix[b] + j dequantised as E4M3val(w) * s_ws.  Computed on the
+ * tensor cores with f16 operands (E4M3 -> f16 is exact; q is rounded to f16,
+ * exact for 2^-14 <= |q| <= 65504) and f32 accumulation; the probabilities
+ * are rounded to f16 for the P V product.
+ *   q_bf16        device bf16 [total_q][num_q_heads][head_dim], 16-byte aligned
+ *   cu_q          device int64 [batch + 1], non-decreasing
+ *   max_q_len     host: >= every chunk length (a longer chunk is cut to it,
+ *                 with NVFP4KV_DEVERR_LENGTH); 0 does nothing
+ *   ws_k, ws_v    device uint8 E4M3 [total_rows][num_kv_heads][head_dim], 16-byte aligned
+ *   cu_prefix     device int64 [batch]: first workspace row of each sequence
+ *   prefix_lens   device int32 [batch]: cached keys of each sequence (>= 0)
+ *   G             a power of two <= 128 (else NVFP4KV_ERR_UNSUPPORTED);
+ *                 batch and num_kv_heads <= 65535
+ *   out           device fp32 [total_q][num_q_heads][head_dim], 16-byte aligned
+ * A key row outside [0, total_rows) reads as zero with NVFP4KV_DEVERR_ROW. */
+int nvfp4kv_bf16_to_fp8_workspace(const void* k_bf16, const void* v_bf16, const int64_t* ws_rows,
+                                  int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                  int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                  uint8_t* ws_v, int32_t* device_status, nvfp4kv_stream_t stream);
+int nvfp4kv_extend_attention(const void* q_bf16, const int64_t* cu_q, int32_t max_q_len,
+                             const uint8_t* ws_k, const uint8_t* ws_v, const int64_t* cu_prefix,
+                             const int32_t* prefix_lens, int32_t batch, int64_t total_rows,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             float k_ws_scale, float v_ws_scale, float softmax_scale, float* out,
+                             int32_t* device_status, nvfp4kv_stream_t stream);
+
 /* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the
  * FP32 per-tensor scale is 1 in the uncalibrated public setting; a calibrated
  * scale maps the tensor's largest magnitude onto the largest NVFP4 magnitude,
