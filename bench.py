@@ -462,6 +462,13 @@ def secondary(torch, kv, args, flush, hbm_peak):
     vals = 2 * kc.numel()
     gbs = (3 * vals + 8 * ew.batch * ew.chunk_len) / (t / 1e3) / 1e9
     out["extend_chunk_to_fp8_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak}
+    # the same chunk written once into both the NVFP4 cache and the workspace
+    ms, _ = time_steps(torch, steps, args.warmup,
+                       lambda ev=None: kv.nvfp4kv_quantize_append_fp8(cache, kc, vc, slots, rows, wk, wv), flush)
+    t = float(np.mean(ms))
+    gbs = (vals * 2 + vals * 9 // 16 + vals + 16 * ew.batch * ew.chunk_len) / (t / 1e3) / 1e9
+    out["extend_quantize_write_fp8_fused_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs,
+                                                        "frac_of_measured_peak": gbs / hbm_peak}
     q = _bf16(torch, ew.q(0))
     cq = _dev(torch, ew.cu_q)
     o = torch.empty((q.shape[0], ew.num_q_heads, 128), dtype=torch.float32, device="cuda")

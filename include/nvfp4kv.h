@@ -282,6 +282,18 @@ int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* 
  *                 batch and num_kv_heads <= 65535
  *   out           device fp32 [total_q][num_q_heads][head_dim], 16-byte aligned
  * A key row outside [0, total_rows) reads as zero with NVFP4KV_DEVERR_ROW. */
+/* nvfp4kv_quantize_append_fp8 is nvfp4kv_quantize_append and
+ * nvfp4kv_bf16_to_fp8_workspace of the same tokens in one pass over k and v
+ * (each bf16 value is read once): the initial-prefill write ("nvfp4-kv-cache-
+ * memory-wall", section 3, item 1: the prompt's K/V enter attention as FP8 and
+ * are quantised to NVFP4 for later use at the same time), and the extend
+ * chunk's write.  Arguments and errors as in the two calls; both outputs are
+ * bit-identical to theirs.  The attention of an initial prefill is
+ * nvfp4kv_extend_attention with prefix_lens = 0. */
+int nvfp4kv_quantize_append_fp8(const nvfp4kv_cache* cache, const void* k, const void* v,
+                                const int64_t* slot_mapping, int64_t num_tokens, const int64_t* ws_rows,
+                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                uint8_t* ws_v, int32_t* device_status, nvfp4kv_stream_t stream);
 int nvfp4kv_bf16_to_fp8_workspace(const void* k_bf16, const void* v_bf16, const int64_t* ws_rows,
                                   int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
                                   int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,

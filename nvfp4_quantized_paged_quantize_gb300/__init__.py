@@ -87,6 +87,7 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_append_decode_attention.argtypes = [pc, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz,
                                                   vp, vp]
     L.nvfp4kv_tensor_amax.argtypes = [vp, i64, vp, ctypes.c_int, vp]
+    L.nvfp4kv_quantize_append_fp8.argtypes = [pc, vp, vp, vp, i64, vp, i64, f32, f32, vp, vp, vp, vp]
     L.nvfp4kv_bf16_to_fp8_workspace.argtypes = [vp, vp, vp, i64, i32, i32, i64, f32, f32, vp, vp, vp, vp]
     L.nvfp4kv_extend_attention.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32, f32, f32, f32, vp,
                                            vp, vp]
@@ -99,7 +100,7 @@ def load(path: str | None = None, build_if_missing: bool = True):
                  "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
                  "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
                  "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
-                 "nvfp4kv_extend_attention"):
+                 "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -261,6 +262,17 @@ def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_p
                                                  _ptr(device_status), _stream(stream)))
 
 
+def nvfp4kv_quantize_append_fp8(cache: "Cache", k, v, slot_mapping, ws_rows, ws_k, ws_v, k_ws_scale: float = 1.0,
+                                v_ws_scale: float = 1.0, device_status=None, stream=None) -> None:
+    """nvfp4kv_quantize_append and nvfp4kv_bf16_to_fp8_workspace of the same tokens in one pass."""
+    n = int(k.shape[0])
+    c = cache.c_struct()
+    _check("nvfp4kv_quantize_append_fp8",
+           _L().nvfp4kv_quantize_append_fp8(ctypes.byref(c), _ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(ws_rows),
+                                            int(ws_k.shape[0]), float(k_ws_scale), float(v_ws_scale), _ptr(ws_k),
+                                            _ptr(ws_v), _ptr(device_status), _stream(stream)))
+
+
 def nvfp4kv_bf16_to_fp8_workspace(k, v, ws_rows, ws_k, ws_v, k_ws_scale: float = 1.0, v_ws_scale: float = 1.0,
                                   device_status=None, stream=None) -> None:
     """The chunk's K/V (bf16 [n, Hkv, 128]) into FP8 workspace rows ws_rows[t] (int64 [n]; < 0 skips)
@@ -312,4 +324,4 @@ __all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quan
            "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
            "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
            "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
-           "nvfp4kv_extend_attention"]
+           "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8"]

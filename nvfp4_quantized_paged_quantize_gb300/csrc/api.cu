@@ -107,6 +107,25 @@ int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const voi
       device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4kv_quantize_append_fp8(const nvfp4kv_cache* cache, const void* k, const void* v,
+                                const int64_t* slot_mapping, int64_t num_tokens, const int64_t* ws_rows,
+                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                uint8_t* ws_v, int32_t* device_status, nvfp4kv_stream_t stream) {
+  int st = check_append(cache, k, v, slot_mapping, num_tokens, device_status);
+  if (st != NVFP4KV_OK) return st;
+  if (total_rows < 0 || !std::isfinite(k_ws_scale) || !std::isfinite(v_ws_scale) || k_ws_scale <= 0.0f ||
+      v_ws_scale <= 0.0f)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return NVFP4KV_OK;
+  if (!ws_rows || !ws_k || !ws_v || !aligned(ws_rows, 8) || !aligned(ws_k, 16) || !aligned(ws_v, 16))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
+  return cuda_status(nvfp4kv::launch_quantize_append_fp8(
+      *cache, static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slot_mapping, num_tokens, ws_rows,
+      total_rows, k_ws_scale, v_ws_scale, ws_k, ws_v, device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
                                   size_t* bytes) {
   if (bytes == nullptr || cache == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;

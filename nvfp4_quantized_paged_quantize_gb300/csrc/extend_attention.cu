@@ -29,6 +29,7 @@
 // drains its MMAs and frees its TMEM.
 #include "nvfp4kv_device.cuh"
 #include "nvfp4kv_launch.h"
+#include "fp8_quotient.cuh"
 #include "tcgen05.cuh"
 
 namespace nvfp4kv {
@@ -59,22 +60,8 @@ __device__ __forceinline__ uint2 bf16x8_to_e4m3(const uint4& x, float s, float r
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
   uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float a0 = bf16_to_f32(w[i] & 0xFFFFu), a1 = bf16_to_f32(w[i] >> 16);
-    if (!unit) {
-      const float q0 = __fmul_rn(a0, rs), q1 = __fmul_rn(a1, rs);
-      if (fast && fabsf(q0) < 0x1p+64f && fabsf(q1) < 0x1p+64f) {
-        // correctly rounded a / s (Markstein) while the first quotient stays far
-        // from overflow; a zero quotient keeps the sign of a
-        a0 = copysignf(__fmaf_rn(__fmaf_rn(-q0, s, a0), rs, q0), a0);
-        a1 = copysignf(__fmaf_rn(__fmaf_rn(-q1, s, a1), rs, q1), a1);
-      } else {
-        a0 = __fdiv_rn(a0, s);
-        a1 = __fdiv_rn(a1, s);
-      }
-    }
-    o[i] = e4m3x2_from_f32(a0, a1);
-  }
+  for (int i = 0; i < 4; ++i)
+    o[i] = e4m3x2_from_quotients(bf16_to_f32(w[i] & 0xFFFFu), bf16_to_f32(w[i] >> 16), s, rs, fast, unit);
   return make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
 }
 

@@ -18,6 +18,12 @@ cudaError_t launch_dequant_fp8(const nvfp4kv_cache& c, const int32_t* page_table
                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
                                uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream);
 
+// Quantize-append plus the FP8 workspace rows of the same tokens, one pass.
+cudaError_t launch_quantize_append_fp8(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
+                                       const int64_t* slot_mapping, int64_t num_tokens, const int64_t* ws_rows,
+                                       int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                       uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream);
+
 // The chunk's bf16 K/V rows -> FP8 workspace rows ws_rows[t] (< 0: skipped).
 cudaError_t launch_chunk_to_ws(const uint16_t* k, const uint16_t* v, const int64_t* ws_rows, int64_t num_tokens,
                                int32_t num_kv_heads, int64_t total_rows, float k_ws_scale, float v_ws_scale,

@@ -13,6 +13,7 @@
 // A block with den == 0 stores signed zeros.  The row's 64 data bytes and 8
 // scale bytes go to slot slot_mapping[token].  HBM-bound: 2 B read and 9/16 B
 // written per value.
+#include "fp8_quotient.cuh"
 #include "nvfp4kv_device.cuh"
 #include "nvfp4kv_launch.h"
 
@@ -32,6 +33,13 @@ struct QuantParams {
   uint8_t* v_scale;
   float gk, gv;
   int32_t* status;
+  // FP8 workspace rows written in the same pass (the fused prefill / extend write)
+  const int64_t* ws_rows;
+  int64_t ws_total_rows;
+  uint8_t* ws_k;
+  uint8_t* ws_v;
+  float sk, sv, rsk, rsv;
+  bool sk_fast, sv_fast, ws_unit;
 };
 
 constexpr int kThreads = 256;
@@ -53,6 +61,9 @@ __device__ __forceinline__ float div_markstein(float a, float b, float r) {
   return __fmaf_rn(rem, r, q0);
 }
 
+// kWs: also write each row's FP8 workspace row, E4M3(fp32(x) / s_ws), at
+// ws_rows[token] (< 0: none) from the same registers.
+template <bool kWs>
 __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p) {
   // a decode launched behind this append (nvfp4kv_append_decode_attention) may
   // start its set-up now; it waits for this grid before reading any page
@@ -76,28 +87,49 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
   const int64_t stride = (int64_t)nwarps * kRowsPerWarp;
   int64_t r = (int64_t)warp * kRowsPerWarp + which;
   uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
-  int64_t slot = -1;
+  int64_t slot = -1, wrow = -1;
   if (r < p.rows) {
     const uint4* xs = reinterpret_cast<const uint4*>(src + (int64_t)r * kHeadDim) + 2 * sub;
     xa = __ldg(xs);
     xb = __ldg(xs + 1);
     slot = __ldg(p.slots + (int)r / p.hkv);  // r < rows < 2^31
+    if constexpr (kWs) wrow = __ldg(p.ws_rows + (int)r / p.hkv);
   }
   for (; r < p.rows; r += stride) {
     const int64_t rn = r + stride;
     uint4 na = make_uint4(0, 0, 0, 0), nb = na;
-    int64_t nslot = -1;
+    int64_t nslot = -1, nwrow = -1;
     if (rn < p.rows) {
       const uint4* xs = reinterpret_cast<const uint4*>(src + (int64_t)rn * kHeadDim) + 2 * sub;
       na = __ldg(xs);
       nb = __ldg(xs + 1);
       nslot = __ldg(p.slots + (int)rn / p.hkv);
+      if constexpr (kWs) nwrow = __ldg(p.ws_rows + (int)rn / p.hkv);
     }
     const uint4 ca = xa, cb = xb;
     const int64_t cslot = slot;
     xa = na;
     xb = nb;
     slot = nslot;
+    if constexpr (kWs) {
+      const int64_t cw = wrow;
+      wrow = nwrow;
+      if (cw >= p.ws_total_rows) {
+        flag_error(p.status, NVFP4KV_DEVERR_ROW);
+      } else if (cw >= 0) {
+        // this lane's 16 values -> 16 E4M3 bytes of the workspace row
+        const uint32_t w[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+        const float s = tensor ? p.sv : p.sk, rs = tensor ? p.rsv : p.rsk;
+        const bool fast = tensor ? p.sv_fast : p.sk_fast;
+        uint32_t e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          e[i] = e4m3x2_from_quotients(bf16_to_f32(w[i] & 0xFFFFu), bf16_to_f32(w[i] >> 16), s, rs, fast, p.ws_unit);
+        uint8_t* ws = tensor ? p.ws_v : p.ws_k;
+        reinterpret_cast<uint4*>(ws + (cw * p.hkv + (int)r % p.hkv) * kHeadDim)[sub] =
+            make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+      }
+    }
     if (cslot < 0) continue;  // padding
     if (cslot >= p.capacity) {
       flag_error(p.status, NVFP4KV_DEVERR_SLOT);
@@ -147,10 +179,33 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
 
 }  // namespace
 
-cudaError_t launch_quantize_append(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
-                                   const int64_t* slot_mapping, int64_t num_tokens,
-                                   int32_t* device_status, int num_sms, cudaStream_t stream) {
-  QuantParams p;
+namespace {
+
+template <bool kWs>
+cudaError_t launch_quantize(QuantParams& p, int num_sms, cudaStream_t stream) {
+  const int warps_needed = (p.rows + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int warps_per_block = kThreads / 32;
+  int blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
+  // a persistent grid: as many blocks as fit on the device at once (more
+  // blocks, each doing less, measured slower)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_append_kernel<kWs>, kThreads, 0) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  const int max_blocks = num_sms * per_sm;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  quantize_append_kernel<kWs><<<blocks, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+QuantParams cache_params(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
+                         int64_t num_tokens, int32_t* device_status) {
+  QuantParams p = {};
   p.k = k;
   p.v = v;
   p.slots = slot_mapping;
@@ -164,23 +219,35 @@ cudaError_t launch_quantize_append(const nvfp4kv_cache& c, const uint16_t* k, co
   p.gk = c.k_global_scale;
   p.gv = c.v_global_scale;
   p.status = device_status;
-  const int warps_needed = (p.rows + kRowsPerWarp - 1) / kRowsPerWarp;
-  const int warps_per_block = kThreads / 32;
-  int blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
-  // a persistent grid: as many blocks as fit on the device at once (more
-  // blocks, each doing less, measured slower)
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_append_kernel, kThreads, 0) != cudaSuccess || n < 1)
-      n = 1;
-    per_sm = n;
-  }
-  const int max_blocks = num_sms * per_sm;
-  if (blocks > max_blocks) blocks = max_blocks;
-  if (blocks < 1) blocks = 1;
-  quantize_append_kernel<<<blocks, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_append(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
+                                   const int64_t* slot_mapping, int64_t num_tokens,
+                                   int32_t* device_status, int num_sms, cudaStream_t stream) {
+  QuantParams p = cache_params(c, k, v, slot_mapping, num_tokens, device_status);
+  return launch_quantize<false>(p, num_sms, stream);
+}
+
+cudaError_t launch_quantize_append_fp8(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
+                                       const int64_t* slot_mapping, int64_t num_tokens, const int64_t* ws_rows,
+                                       int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
+                                       uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream) {
+  QuantParams p = cache_params(c, k, v, slot_mapping, num_tokens, device_status);
+  p.ws_rows = ws_rows;
+  p.ws_total_rows = total_rows;
+  p.ws_k = ws_k;
+  p.ws_v = ws_v;
+  p.sk = k_ws_scale;
+  p.sv = v_ws_scale;
+  p.rsk = 1.0f / k_ws_scale;  // host IEEE division: RN(1 / s_ws)
+  p.rsv = 1.0f / v_ws_scale;
+  p.sk_fast = k_ws_scale >= 0x1p-100f && k_ws_scale <= 0x1p+100f;
+  p.sv_fast = v_ws_scale >= 0x1p-100f && v_ws_scale <= 0x1p+100f;
+  p.ws_unit = k_ws_scale == 1.0f && v_ws_scale == 1.0f;
+  return launch_quantize<true>(p, num_sms, stream);
 }
 
 }  // namespace nvfp4kv

@@ -175,3 +175,14 @@ def test_extend_host_checks(lib):
     assert g(16, 16, 8, 4, 2, 128, 10, -1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
     assert g(16, 16, 12, 4, 2, 128, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
     assert g(None, None, None, 0, 2, 128, 10, 1.0, 1.0, None, None, None, None) == kv.NVFP4KV_OK
+
+
+def test_fused_write_host_checks(lib):
+    cs = _fake_cache().c_struct()
+    f = lib.nvfp4kv_quantize_append_fp8
+    P = ctypes.byref
+    # (cache, k, v, slots, n, ws_rows, total_rows, sk, sv, ws_k, ws_v, status, stream)
+    assert f(P(cs), 16, 16, 8, 4, 8, 10, 0.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(P(cs), 16, 16, 8, 4, 12, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(P(cs), 18, 16, 8, 4, 8, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(P(cs), None, None, None, 0, None, 10, 1.0, 1.0, None, None, None, None) == kv.NVFP4KV_OK

@@ -13,7 +13,7 @@ import torch
 import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import ATTN_TOL, bf16_dev, check_rows, dev, gpu_append, gpu_cache, status_word
+from gpu_util import ATTN_TOL, bf16_dev, check_rows, dev, gpu_append, gpu_cache, pool_host, status_word
 
 pytestmark = pytest.mark.gpu
 
@@ -170,3 +170,65 @@ def test_extend_layer_full_size_sampled(cuda_lib):
     # one layer at full size (16 x (16384 prefix + 2048 chunk), 64 / 8 heads), as the bench times it
     same, _ = _pipeline(inputs.extend_config(num_layers=1), 0, 3, np.random.default_rng(2))
     assert same
+
+
+# --------------------------------------------------------------------------
+# the fused write: NVFP4 cache rows and FP8 workspace rows in one pass
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("sk,sv", [(1.0, 1.0), (0.37, 5.5)])
+def test_fused_write_matches_oracle(cuda_lib, sk, sv):
+    rng = np.random.default_rng(23)
+    n, H, pages, rows = 333, 4, 40, 500
+    x = (rng.standard_normal((n, H, 128)) * 2.0 ** rng.integers(-8, 8, (n, H, 128))).astype(np.float32)
+    k, v = inputs.bf16_bits(x), inputs.bf16_bits(x[::-1].copy() * 0.5)
+    slots = rng.permutation(pages * 16)[:n].astype(np.int64)
+    slots[::41] = -1                                      # padding tokens
+    slots[7] = pages * 16 + 3                             # outside the pool
+    ws_rows = rng.permutation(rows)[:n].astype(np.int64)
+    ws_rows[::29] = -1
+    ws_rows[11] = rows                                    # outside the workspace
+    g = gpu_cache(pages, H, 0.37, 2.5)
+    wk, wv = _u8(np.full((rows, H, 128), 0x5A)), _u8(np.full((rows, H, 128), 0x5A))
+    st = status_word()
+    kv.nvfp4kv_quantize_append_fp8(g, bf16_dev(k), bf16_dev(v), dev(slots), dev(ws_rows), wk, wv, sk, sv,
+                                   device_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & kv.NVFP4KV_DEVERR_SLOT and st.item() & kv.NVFP4KV_DEVERR_ROW
+    o = oracle.Cache(pages, H, 128, 16, 0.37, 2.5)
+    assert oracle.quantize_append(o, k, v, slots) != 0   # the out-of-pool slot is reported
+    owk, owv = (np.full((rows, H, 128), 0x5A, np.uint8) for _ in range(2))
+    assert oracle.bf16_to_fp8_workspace(k, v, ws_rows, owk, owv, sk, sv) != 0
+    for got, want in zip(pool_host(g), (o.k_data, o.v_data, o.k_scale, o.v_scale)):
+        assert np.array_equal(got, want)
+    assert np.array_equal(wk.cpu().numpy(), owk) and np.array_equal(wv.cpu().numpy(), owv)
+
+
+def test_initial_prefill_through_the_fused_write(cuda_lib):
+    # prompts {1, 77, 300}: one pass writes the NVFP4 cache and the FP8 rows,
+    # then the extend attention runs with empty prefixes
+    case = inputs.ExtendAttnCase("prefill", inputs.BASE_SEED + 160, np.zeros(3, np.int32),
+                                 np.array([1, 77, 300], np.int32), 16, 2, gap=0)
+    rng = np.random.default_rng(5)
+    n, H = case.total_q, case.num_kv_heads
+    k = inputs.bf16_bits((rng.standard_normal((n, H, 128)) * 0.5).astype(np.float32))
+    v = inputs.bf16_bits(rng.standard_normal((n, H, 128)).astype(np.float32))
+    q = case.q()
+    pages = (n + 15) // 16 + 3
+    slots = rng.permutation(pages * 16)[:n].astype(np.int64)
+    ws_rows = np.arange(n, dtype=np.int64)                # cu_prefix == cu_q: each prompt's rows in order
+    g = gpu_cache(pages, H)
+    wk = torch.zeros((case.total_rows, H, 128), dtype=torch.uint8, device="cuda")
+    wv = torch.zeros_like(wk)
+    kv.nvfp4kv_quantize_append_fp8(g, bf16_dev(k), bf16_dev(v), dev(slots), dev(ws_rows), wk, wv)
+    got = _extend_gpu(case, wk, wv, q)
+    o = oracle.Cache(pages, H, 128, 16)
+    assert oracle.quantize_append(o, k, v, slots) == 0
+    owk, owv = (np.zeros((case.total_rows, H, 128), np.uint8) for _ in range(2))
+    assert oracle.bf16_to_fp8_workspace(k, v, ws_rows, owk, owv) == 0
+    for gg, want in zip(pool_host(g), (o.k_data, o.v_data, o.k_scale, o.v_scale)):
+        assert np.array_equal(gg, want)
+    assert np.array_equal(wk.cpu().numpy(), owk)
+    ref, st = oracle.extend_attention(owk, owv, q, case.cu_q, case.cu_prefix, case.prefix_lens, case.softmax_scale)
+    assert st == 0
+    check_rows(got, ref)
