@@ -418,6 +418,19 @@ def extend_config(scale: float = 1.0, num_layers: int = 80) -> ExtendWorkload:
 
 
 # --------------------------------------------------------------------------
+# random bytes drawn by the stochastic-rounding variant (an input of the method)
+# --------------------------------------------------------------------------
+
+_S_ROUND = 9
+
+
+def rounding_bytes(index: int, n: int) -> np.ndarray:
+    """n uniform random bytes for stochastic rounding, one per value."""
+    rng = np.random.default_rng([BASE_SEED, _S_ROUND, index])
+    return rng.integers(0, 256, n, dtype=np.uint8)
+
+
+# --------------------------------------------------------------------------
 # extend attention over a given FP8 workspace (ragged cases for the tests)
 # --------------------------------------------------------------------------
 

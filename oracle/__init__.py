@@ -79,6 +79,18 @@ def lib():
         L.nvfp4_oracle_tensor_amax.restype = f32
         L.nvfp4_oracle_calibrated_global_scale.argtypes = [f32]
         L.nvfp4_oracle_calibrated_global_scale.restype = f32
+        L.nvfp4_oracle_e8m0_value.argtypes = [u8]
+        L.nvfp4_oracle_e8m0_value.restype = f64
+        L.nvfp4_oracle_mxfp4_quantize_block.argtypes = [vp, vp, vp]
+        L.nvfp4_oracle_mxfp4_quantize_block.restype = None
+        L.nvfp4_oracle_mxfp4_dequant_value.argtypes = [u8, u8]
+        L.nvfp4_oracle_mxfp4_dequant_value.restype = f64
+        L.nvfp4_oracle_e2m1_encode_sr.argtypes = [f32, u8]
+        L.nvfp4_oracle_e2m1_encode_sr.restype = u8
+        L.nvfp4_oracle_quantize_block_sr.argtypes = [vp, f32, vp, vp, vp]
+        L.nvfp4_oracle_quantize_block_sr.restype = None
+        L.nvfp4_oracle_hadamard.argtypes = [vp, ctypes.c_int, vp]
+        L.nvfp4_oracle_hadamard.restype = ctypes.c_int
         L.nvfp4_oracle_bf16_to_fp8_workspace.argtypes = [vp, vp, vp, i64, i32, i32, i64, f32, f32, vp, vp]
         L.nvfp4_oracle_bf16_to_fp8_workspace.restype = ctypes.c_int
         L.nvfp4_oracle_extend_attention_rows.argtypes = [vp, vp, i64, i32, i32, f32, f32, vp, i32, vp, vp, vp,
@@ -288,6 +300,96 @@ def extend_attention(ws_k, ws_v, q_bf16, cu_q, cu_prefix, prefix_lens, softmax_s
     out, st = extend_attention_rows(ws_k, ws_v, q_bf16, cu_q, cu_prefix, prefix_lens, softmax_scale, pairs,
                                     k_ws_scale, v_ws_scale)
     return out.reshape(total_q, Hq, -1), st
+
+
+
+# --------------------------------------------------------------------------
+# format variants (MXFP4, stochastic rounding, Hadamard rotation)
+# --------------------------------------------------------------------------
+
+MX_BLOCK = 32
+
+
+def e8m0_value(code: int) -> float:
+    return lib().nvfp4_oracle_e8m0_value(code)
+
+
+def mxfp4_quantize_block(x):
+    """One 32-value block -> (16 packed bytes, E8M0 scale byte)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.shape == (MX_BLOCK,)
+    packed = np.zeros(MX_BLOCK // 2, np.uint8)
+    scale = np.zeros(1, np.uint8)
+    lib().nvfp4_oracle_mxfp4_quantize_block(_ptr(x), _ptr(packed), _ptr(scale))
+    return packed, int(scale[0])
+
+
+def mxfp4_dequant_value(code: int, scale: int) -> float:
+    return lib().nvfp4_oracle_mxfp4_dequant_value(code, scale)
+
+
+def e2m1_encode_sr(y, r: int) -> int:
+    return lib().nvfp4_oracle_e2m1_encode_sr(float(np.float32(y)), int(r))
+
+
+def quantize_block_sr(x, g, r):
+    """One 16-value block with stochastic element rounding (r: 16 random bytes)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rr = np.ascontiguousarray(r, dtype=np.uint8)
+    assert x.shape == (BLOCK,) and rr.shape == (BLOCK,)
+    packed = np.zeros(BLOCK // 2, np.uint8)
+    scale = np.zeros(1, np.uint8)
+    lib().nvfp4_oracle_quantize_block_sr(_ptr(x), float(np.float32(g)), _ptr(rr), _ptr(packed), _ptr(scale))
+    return packed, int(scale[0])
+
+
+def hadamard(x) -> np.ndarray:
+    """Orthonormal Walsh-Hadamard transform (Sylvester order, binary32 butterflies) of a vector."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.zeros_like(x)
+    assert lib().nvfp4_oracle_hadamard(_ptr(x), x.shape[0], _ptr(y)) == 0
+    return y
+
+
+def _unpack(packed) -> np.ndarray:
+    p = np.asarray(packed, np.uint8)
+    return np.stack([p & 0xF, p >> 4], axis=-1).reshape(-1)
+
+
+def fake_quant(x, variant: str, g: float = 1.0, rand=None) -> np.ndarray:
+    """Quantise then dequantise (fp64) a 1-D array whose length is a multiple of 128,
+    in one of the variants: "nvfp4" (blocks of 16, E4M3 scale, nearest even),
+    "nvfp4_sr" (elements rounded stochastically with rand, one byte per value),
+    "nvfp4_hadamard" (each 128-value vector rotated first and rotated back after),
+    "mxfp4" (blocks of 32, E8M0 scale)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.zeros(x.shape[0], np.float64)
+    e2m1 = np.array([e2m1_value(c) for c in range(16)])
+    if variant == "mxfp4":
+        for i in range(0, x.shape[0], MX_BLOCK):
+            packed, sc = mxfp4_quantize_block(x[i:i + MX_BLOCK])
+            out[i:i + MX_BLOCK] = e2m1[_unpack(packed)] * e8m0_value(sc)
+        return out
+    gg = float(np.float32(g))
+    vecs = x.reshape(-1, 128)
+    if variant == "nvfp4_hadamard":
+        vecs = np.stack([hadamard(v) for v in vecs])
+    flat = vecs.reshape(-1)
+    for i in range(0, flat.shape[0], BLOCK):
+        blk = flat[i:i + BLOCK]
+        if variant == "nvfp4_sr":
+            packed, sc = quantize_block_sr(blk, gg, rand[i:i + BLOCK])
+        else:
+            packed, sc = quantize_block(blk, gg)
+        out[i:i + BLOCK] = e2m1[_unpack(packed)] * e4m3_value(sc) * gg
+    if variant == "nvfp4_hadamard":
+        # the rotation is orthonormal: its transpose (itself) undoes it, here in fp64
+        n = 128
+        h = np.array([[1.0]])
+        while h.shape[0] < n:
+            h = np.block([[h, h], [h, -h]])
+        out = (out.reshape(-1, n) @ (h / np.sqrt(n))).reshape(-1)
+    return out
 
 
 __all__ = [name for name in dir() if not name.startswith("_")]

@@ -472,6 +472,123 @@ int nvfp4_oracle_extend_attention_rows(const uint8_t* ws_k, const uint8_t* ws_v,
   return bad;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Format variants the pages compare with NVFP4.                             */
+/* ------------------------------------------------------------------------- */
+
+/* MXFP4 ("NVIDIA NVFP4: LLM memory doubled, inference 3x" (nmedialink),
+ * figure 6 and its text: NVFP4's finer blocks and more precise E4M3 scale beat
+ * MXFP4; "NVFP4: breaking the memory wall" (cloud.tencent.com), technical
+ * breakdown: MXFP4 shares one scale among 32 values, NVFP4 among 16).
+ * Reading: the public microscaling layout -- a power-of-two scale stored as an
+ * E8M0 byte (exponent + 127), X = 2^(floor(log2 amax) - 2), 2 being E2M1's
+ * largest exponent; elements E2M1(x / X), nearest even, saturating; an all-zero
+ * block takes the smallest scale, 2^-127. */
+double nvfp4_oracle_e8m0_value(uint8_t code) {
+  if (code == 0xFF) return NAN;
+  return ldexp(1.0, (int)code - 127);
+}
+
+void nvfp4_oracle_mxfp4_quantize_block(const float x[32], uint8_t packed[16], uint8_t* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; ++i) {
+    const float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  int e = -127;
+  if (amax > 0.0f) {
+    int ex;
+    frexpf(amax, &ex); /* amax = m * 2^ex with m in [0.5, 1): floor(log2 amax) = ex - 1 */
+    e = ex - 1 - 2;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+  }
+  *scale = (uint8_t)(e + 127);
+  for (int i = 0; i < 16; ++i) {
+    /* division by a power of two: exact unless the quotient is subnormal */
+    const uint8_t lo = nvfp4_oracle_e2m1_encode((float)((double)x[2 * i] / ldexp(1.0, e)));
+    const uint8_t hi = nvfp4_oracle_e2m1_encode((float)((double)x[2 * i + 1] / ldexp(1.0, e)));
+    packed[i] = (uint8_t)(lo | (hi << 4));
+  }
+}
+
+double nvfp4_oracle_mxfp4_dequant_value(uint8_t code, uint8_t scale) {
+  return nvfp4_oracle_e2m1_value(code) * nvfp4_oracle_e8m0_value(scale);
+}
+
+/* Stochastic rounding ("NVFP4: breaking the memory wall" (cloud.tencent.com),
+ * the quantisation techniques and the two engineering tricks: a value between
+ * two grid points goes up with probability equal to its distance past the
+ * lower point, 2.3 -> 2 with 70 %, -> 3 with 30 %, so the errors cancel on
+ * average).  Reading: applied to the E2M1 element codes (the block scale stays
+ * nearest-even); the random number is an input byte r, read as the uniform
+ * (r + 0.5) / 256: |y| rounds up iff (r + 0.5) / 256 < (|y| - a) / (b - a) for
+ * the grid neighbours a <= |y| < b.  Every E2M1 gap is a power of two, so that
+ * fraction is exact in binary32 and so is the decision.  Sign kept; |y| >= 6
+ * gives 6. */
+uint8_t nvfp4_oracle_e2m1_encode_sr(float y, uint8_t r) {
+  init_tables();
+  const float m = fabsf(y);
+  uint8_t code;
+  if (m >= 6.0f) {
+    code = 7;
+  } else {
+    int c = 0; /* largest code with value <= m */
+    while (c < 7 && e2m1_mag[c + 1] <= (double)m) ++c;
+    const double a = e2m1_mag[c], b = e2m1_mag[c + 1];
+    const double frac = ((double)m - a) / (b - a); /* exact: the gap is a power of two */
+    code = (uint8_t)(((double)r + 0.5) / 256.0 < frac ? c + 1 : c);
+  }
+  return (uint8_t)(code | (signbit(y) ? 0x8 : 0x0));
+}
+
+void nvfp4_oracle_quantize_block_sr(const float x[NVFP4_ORACLE_BLOCK], float g, const uint8_t r[NVFP4_ORACLE_BLOCK],
+                                    uint8_t packed[NVFP4_ORACLE_BLOCK / 2], uint8_t* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < NVFP4_ORACLE_BLOCK; ++i) {
+    const float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  const float t = 6.0f * g;
+  const uint8_t sb = nvfp4_oracle_e4m3_encode(amax / t);
+  const float den = (float)nvfp4_oracle_e4m3_value(sb) * g;
+  *scale = sb;
+  for (int i = 0; i < NVFP4_ORACLE_BLOCK / 2; ++i) {
+    uint8_t c[2];
+    for (int h = 0; h < 2; ++h) {
+      const float xv = x[2 * i + h];
+      if (den == 0.0f)
+        c[h] = (uint8_t)(signbit(xv) ? 0x8 : 0x0);
+      else
+        c[h] = nvfp4_oracle_e2m1_encode_sr(xv / den, r[2 * i + h]);
+    }
+    packed[i] = (uint8_t)(c[0] | (c[1] << 4));
+  }
+}
+
+/* Hadamard rotation before quantisation (the same page, same two passages: an
+ * orthogonal transform spreads a local outlier over the whole vector; its
+ * worked numbers are garbled and not used).  Reading: the
+ * orthonormal Walsh-Hadamard transform of order n (a power of two; the head
+ * vector, n = 128), Sylvester ordering (H_2n = [[H_n, H_n], [H_n, -H_n]]),
+ * evaluated in binary32 as log2(n) butterfly passes y_j, y_(j+h) <- y_j + y_(j+h),
+ * y_j - y_(j+h) for h = 1, 2, 4, ... followed by one multiplication by
+ * RN(1 / sqrt(n)).  The transform is its own inverse. */
+int nvfp4_oracle_hadamard(const float* x, int n, float* y) {
+  if (n <= 0 || (n & (n - 1)) != 0) return -1;
+  for (int i = 0; i < n; ++i) y[i] = x[i];
+  for (int h = 1; h < n; h *= 2)
+    for (int i = 0; i < n; i += 2 * h)
+      for (int j = i; j < i + h; ++j) {
+        const float a = y[j], b = y[j + h];
+        y[j] = a + b;
+        y[j + h] = a - b;
+      }
+  const float c = (float)(1.0 / sqrt((double)n));
+  for (int i = 0; i < n; ++i) y[i] = y[i] * c;
+  return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the FP32
  * per-tensor scale is left at 1 by the uncalibrated public setting, and a

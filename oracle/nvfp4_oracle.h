@@ -70,6 +70,17 @@ int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int
                                           float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
                                           uint8_t* ws_v);
 
+/* Format variants (MXFP4 blocks of 32 with an E8M0 scale; stochastic rounding
+ * of the E2M1 codes from input random bytes; the orthonormal Walsh-Hadamard
+ * rotation in binary32 butterflies). */
+double nvfp4_oracle_e8m0_value(uint8_t code);
+void nvfp4_oracle_mxfp4_quantize_block(const float x[32], uint8_t packed[16], uint8_t* scale);
+double nvfp4_oracle_mxfp4_dequant_value(uint8_t code, uint8_t scale);
+uint8_t nvfp4_oracle_e2m1_encode_sr(float y, uint8_t r);
+void nvfp4_oracle_quantize_block_sr(const float x[NVFP4_ORACLE_BLOCK], float g, const uint8_t r[NVFP4_ORACLE_BLOCK],
+                                    uint8_t packed[NVFP4_ORACLE_BLOCK / 2], uint8_t* scale);
+int nvfp4_oracle_hadamard(const float* x, int n, float* y);
+
 /* Extend over the FP8 workspace.  The chunk's K/V rows enter the workspace
  * from bf16 (w = E4M3(fp32(x) / s_ws), signed); ws_rows[t] < 0 skips token t.
  * Extend attention evaluates, in binary64, the output rows named by pairs
