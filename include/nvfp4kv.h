@@ -64,6 +64,13 @@ enum {
   NVFP4KV_ERR_WORKSPACE = -4         /* workspace null, too small or misaligned */
 };
 
+/* Format variants of nvfp4kv_quantize_append_variant. */
+enum {
+  NVFP4KV_VARIANT_SR = 1,       /* NVFP4 with stochastically rounded E2M1 codes */
+  NVFP4KV_VARIANT_HADAMARD = 2, /* NVFP4 of the Hadamard-rotated head vector */
+  NVFP4KV_VARIANT_MXFP4 = 3     /* MXFP4: blocks of 32, E8M0 scales (4 per row) */
+};
+
 /* Device-side error bits (ORed into *device_status when it is given). */
 enum {
   NVFP4KV_DEVERR_SLOT = 1,   /* a slot >= num_pages * page_size: that token was skipped */
@@ -304,6 +311,34 @@ int nvfp4kv_extend_attention(const void* q_bf16, const int64_t* cu_q, int32_t ma
                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                              float k_ws_scale, float v_ws_scale, float softmax_scale, float* out,
                              int32_t* device_status, nvfp4kv_stream_t stream);
+
+/* Quantize-on-append of the format variants the pages compare with NVFP4
+ * ("NVFP4: breaking the memory wall" (cloud.tencent.com): stochastic rounding
+ * and a Hadamard rotation before quantisation, MXFP4's 32-value blocks;
+ * "NVIDIA NVFP4: LLM memory doubled, inference 3x" (nmedialink), figure 6).
+ * Same rows, slots and errors as nvfp4kv_quantize_append; the data pages are
+ * the NVFP4 ones.
+ *   NVFP4KV_VARIANT_SR        the block scale as in NVFP4; each element code
+ *                             rounds to one of its two E2M1 neighbours, up iff
+ *                             (r + 0.5) / 256 < (|y| - a) / (b - a) for the
+ *                             input byte r of that value (rand_k / rand_v:
+ *                             device uint8 [num_tokens][num_kv_heads][head_dim],
+ *                             16-byte aligned)
+ *   NVFP4KV_VARIANT_HADAMARD  NVFP4 of H x, H the orthonormal Walsh-Hadamard
+ *                             transform of the 128-value head vector (Sylvester
+ *                             order; binary32 butterfly passes h = 1 .. 64, then
+ *                             one product with RN(1 / sqrt(128))); a reader
+ *                             applies H again (or rotates q the same way)
+ *   NVFP4KV_VARIANT_MXFP4     blocks of 32 with a power-of-two scale, the E8M0
+ *                             byte e + 127, e = floor(log2 amax) - 2 (clamped to
+ *                             [-127, 127]); elements E2M1(x * 2^-e); the scale
+ *                             pools hold head_dim / 32 bytes per row
+ *                             ([num_pages][num_kv_heads][page_size][4]) and the
+ *                             global scales are not used
+ * Unknown variants return NVFP4KV_ERR_INVALID_ARGUMENT. */
+int nvfp4kv_quantize_append_variant(int variant, const nvfp4kv_cache* cache, const void* k, const void* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens, const uint8_t* rand_k,
+                                    const uint8_t* rand_v, int32_t* device_status, nvfp4kv_stream_t stream);
 
 /* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the
  * FP32 per-tensor scale is 1 in the uncalibrated public setting; a calibrated

@@ -28,6 +28,9 @@ NVFP4KV_DEVERR_PAGE = 2
 NVFP4KV_DEVERR_LENGTH = 4
 NVFP4KV_DEVERR_TIMEOUT = 8
 NVFP4KV_DEVERR_ROW = 16
+NVFP4KV_VARIANT_SR = 1
+NVFP4KV_VARIANT_HADAMARD = 2
+NVFP4KV_VARIANT_MXFP4 = 3
 
 HEAD_DIM = 128
 PAGE_SIZE = 16
@@ -87,6 +90,7 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_append_decode_attention.argtypes = [pc, vp, vp, vp, i64, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz,
                                                   vp, vp]
     L.nvfp4kv_tensor_amax.argtypes = [vp, i64, vp, ctypes.c_int, vp]
+    L.nvfp4kv_quantize_append_variant.argtypes = [ctypes.c_int, pc, vp, vp, vp, i64, vp, vp, vp, vp]
     L.nvfp4kv_quantize_append_fp8.argtypes = [pc, vp, vp, vp, i64, vp, i64, f32, f32, vp, vp, vp, vp]
     L.nvfp4kv_bf16_to_fp8_workspace.argtypes = [vp, vp, vp, i64, i32, i32, i64, f32, f32, vp, vp, vp, vp]
     L.nvfp4kv_extend_attention.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32, f32, f32, f32, vp,
@@ -100,7 +104,7 @@ def load(path: str | None = None, build_if_missing: bool = True):
                  "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
                  "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
                  "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
-                 "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8"):
+                 "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -262,6 +266,17 @@ def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_p
                                                  _ptr(device_status), _stream(stream)))
 
 
+def nvfp4kv_quantize_append_variant(variant: int, cache: "Cache", k, v, slot_mapping, rand_k=None, rand_v=None,
+                                    device_status=None, stream=None) -> None:
+    """Quantize-append of a format variant (NVFP4KV_VARIANT_SR / _HADAMARD / _MXFP4); for MXFP4 the
+    cache's scale tensors are [num_pages, Hkv, 16, 4] E8M0 bytes."""
+    c = cache.c_struct()
+    _check("nvfp4kv_quantize_append_variant",
+           _L().nvfp4kv_quantize_append_variant(int(variant), ctypes.byref(c), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                                int(k.shape[0]), _ptr(rand_k), _ptr(rand_v), _ptr(device_status),
+                                                _stream(stream)))
+
+
 def nvfp4kv_quantize_append_fp8(cache: "Cache", k, v, slot_mapping, ws_rows, ws_k, ws_v, k_ws_scale: float = 1.0,
                                 v_ws_scale: float = 1.0, device_status=None, stream=None) -> None:
     """nvfp4kv_quantize_append and nvfp4kv_bf16_to_fp8_workspace of the same tokens in one pass."""
@@ -324,4 +339,4 @@ __all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quan
            "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
            "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
            "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
-           "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8"]
+           "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant"]

@@ -126,6 +126,21 @@ int nvfp4kv_quantize_append_fp8(const nvfp4kv_cache* cache, const void* k, const
       total_rows, k_ws_scale, v_ws_scale, ws_k, ws_v, device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4kv_quantize_append_variant(int variant, const nvfp4kv_cache* cache, const void* k, const void* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens, const uint8_t* rand_k,
+                                    const uint8_t* rand_v, int32_t* device_status, nvfp4kv_stream_t stream) {
+  if (variant != NVFP4KV_VARIANT_SR && variant != NVFP4KV_VARIANT_HADAMARD && variant != NVFP4KV_VARIANT_MXFP4)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  const int st = check_append(cache, k, v, slot_mapping, num_tokens, device_status);
+  if (st != NVFP4KV_OK || num_tokens == 0) return st;
+  if (variant == NVFP4KV_VARIANT_SR && (!rand_k || !rand_v || !aligned(rand_k, 16) || !aligned(rand_v, 16)))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  return cuda_status(nvfp4kv::launch_quantize_variant(variant, *cache, static_cast<const uint16_t*>(k),
+                                                      static_cast<const uint16_t*>(v), slot_mapping, num_tokens,
+                                                      rand_k, rand_v, device_status,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
                                   size_t* bytes) {
   if (bytes == nullptr || cache == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;

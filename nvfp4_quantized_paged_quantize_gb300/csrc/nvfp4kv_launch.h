@@ -24,6 +24,11 @@ cudaError_t launch_quantize_append_fp8(const nvfp4kv_cache& c, const uint16_t* k
                                        int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
                                        uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream);
 
+// Quantize-append of a format variant (NVFP4KV_VARIANT_*).
+cudaError_t launch_quantize_variant(int variant, const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens, const uint8_t* rand_k,
+                                    const uint8_t* rand_v, int32_t* device_status, cudaStream_t stream);
+
 // The chunk's bf16 K/V rows -> FP8 workspace rows ws_rows[t] (< 0: skipped).
 cudaError_t launch_chunk_to_ws(const uint16_t* k, const uint16_t* v, const int64_t* ws_rows, int64_t num_tokens,
                                int32_t num_kv_heads, int64_t total_rows, float k_ws_scale, float v_ws_scale,

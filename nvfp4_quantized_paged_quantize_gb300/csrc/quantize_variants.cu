@@ -1,0 +1,221 @@
+// quantize_variants.cu -- the quantize-on-append of the format variants the
+// pages compare with NVFP4:
+//  - stochastic rounding of the E2M1 codes ("NVFP4: breaking the memory wall",
+//    quantisation techniques: 2.3 -> 2 with 70 %, -> 3 with 30 %), one input
+//    random byte per value, read as the uniform (r + 0.5) / 256;
+//  - a Hadamard rotation of each 128-value head vector before the NVFP4 block
+//    quantisation (same page: an orthogonal transform spreads an outlier):
+//    the orthonormal Walsh-Hadamard transform as seven binary32 butterfly
+//    passes (h = 1, 2, 4, ..., 64) and one multiplication by RN(1 / sqrt(128));
+//  - MXFP4 ("NVIDIA NVFP4: LLM memory doubled, inference 3x", figure 6; "NVFP4:
+//    breaking the memory wall", technical breakdown): blocks of 32 values with
+//    a power-of-two scale, an E8M0 byte e + 127 with e = floor(log2 amax) - 2,
+//    elements E2M1(x * 2^-e); its scale pool holds 4 bytes per row.
+// The data pages are the NVFP4 ones (64 bytes of E2M1 pairs per row).
+//
+// Eight lanes own one (token, head) row of K or of V, 16 values each; a warp
+// takes four rows.  Block scales divide exactly (IEEE); these are comparison
+// paths, not the tuned one.
+#include "nvfp4kv_device.cuh"
+#include "nvfp4kv_launch.h"
+
+namespace nvfp4kv {
+namespace {
+
+struct VariantParams {
+  const uint16_t* k;
+  const uint16_t* v;
+  const int64_t* slots;
+  const uint8_t* rand_k;  // stochastic rounding: one byte per value, [tokens][hkv][128]
+  const uint8_t* rand_v;
+  int64_t rows;  // num_tokens * hkv * 2 (K rows then V rows of each (token, head))
+  int32_t hkv;
+  int64_t capacity;
+  uint8_t* k_data;
+  uint8_t* v_data;
+  uint8_t* k_scale;
+  uint8_t* v_scale;
+  float gk, gv;
+  int32_t* status;
+};
+
+constexpr int kThreads = 256;
+
+// E2M1 code of |y| < 6 (grid neighbours a <= |y| < b) rounded up with
+// probability (|y| - a) / (b - a): up iff 2 r + 1 < 512 (|y| - a) / (b - a).
+// Every gap is a power of two, so the scaled fraction is exact.
+__device__ __forceinline__ uint32_t e2m1_code_sr(float y, uint32_t r) {
+  const float m = fabsf(y);
+  uint32_t c;
+  if (m >= 6.0f) {
+    c = 7;
+  } else {
+    float a, inv_gap;  // lower neighbour and 1 / gap
+    if (m < 2.0f) {
+      c = (uint32_t)(m * 2.0f);  // 0 .. 3, exact
+      a = (float)c * 0.5f;
+      inv_gap = 2.0f;
+    } else if (m < 4.0f) {
+      c = m < 3.0f ? 4u : 5u;
+      a = m < 3.0f ? 2.0f : 3.0f;
+      inv_gap = 1.0f;
+    } else {
+      c = 6;
+      a = 4.0f;
+      inv_gap = 0.5f;
+    }
+    const float frac512 = (m - a) * inv_gap * 512.0f;  // exact
+    if ((float)(2 * r + 1) < frac512) ++c;
+  }
+  return c | (__float_as_uint(y) >> 31 << 3);
+}
+
+template <int kVariant>
+__global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParams p) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;  // values [16 sub, 16 sub + 16) of the row
+  // every lane stays to the end (the rotation and MXFP4 exchange values across
+  // the row's lanes with full-warp shuffles); lanes past the last row work on
+  // row 0 and store nothing
+  const int64_t gid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
+  const bool live = gid < p.rows;
+  const int64_t row_id = live ? gid : 0;
+  const int tensor = (int)(row_id & 1);
+  const int64_t th = row_id >> 1;  // token * hkv + h
+  const int64_t token = th / p.hkv;
+  const int h = (int)(th - token * p.hkv);
+  const uint16_t* src = (tensor ? p.v : p.k) + th * kHeadDim + 16 * sub;
+  const uint4 xa = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 xb = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+  const uint32_t w[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16_to_f32(w[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_to_f32(w[i] >> 16);
+  }
+  if constexpr (kVariant == NVFP4KV_VARIANT_HADAMARD) {
+    // passes h = 1, 2, 4, 8 inside the lane, then 16, 32, 64 across the row's lanes
+#pragma unroll
+    for (int hh = 1; hh < 16; hh *= 2)
+#pragma unroll
+      for (int i = 0; i < 16; i += 2 * hh)
+#pragma unroll
+        for (int j = i; j < i + hh; ++j) {
+          const float a = f[j], b = f[j + hh];
+          f[j] = a + b;
+          f[j + hh] = a - b;
+        }
+#pragma unroll
+    for (int x = 1; x < 8; x *= 2) {
+      const bool upper = (sub & x) != 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, f[i], x);
+        f[i] = upper ? o - f[i] : f[i] + o;  // lower: a + b; upper: a - b (a from the lower lane)
+      }
+    }
+    const float c = 0x1.6a09e6p-4f;  // RN(1 / sqrt(128)) = RN(sqrt(2)) / 16
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(f[i], c);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+
+  uint32_t lo = 0, hi = 0, sbyte;
+  if constexpr (kVariant == NVFP4KV_VARIANT_MXFP4) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // the block of 32 spans a lane pair
+    int e = -127;
+    if (amax > 0.0f) {
+      const int be = (int)((__float_as_uint(amax) >> 23) & 0xFFu);  // 0 for subnormals: floor(log2) <= -127
+      e = be == 0 ? -127 : be - 127 - 2;
+      e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    }
+    sbyte = (uint32_t)(e + 127);
+    // 2^-e (e <= 125 since amax < 2^128, so 2^-e is a normal float): each
+    // product rounds once, as the exact quotient x / 2^e does
+    const float sc = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      lo |= e2m1x2_from_f32(__fmul_rn(f[2 * k], sc), __fmul_rn(f[2 * k + 1], sc)) << (8 * k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      hi |= e2m1x2_from_f32(__fmul_rn(f[8 + 2 * k], sc), __fmul_rn(f[8 + 2 * k + 1], sc)) << (8 * k);
+  } else {
+    const float g = tensor ? p.gv : p.gk;
+    sbyte = e4m3_from_f32(__fdiv_rn(amax, __fmul_rn(6.0f, g)));
+    const float den = __fmul_rn(e4m3_to_f32(sbyte), g);
+    if (den == 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) lo |= (__float_as_uint(f[i]) >> 31) << (4 * i + 3);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hi |= (__float_as_uint(f[8 + i]) >> 31) << (4 * i + 3);
+    } else if constexpr (kVariant == NVFP4KV_VARIANT_SR) {
+      const uint8_t* rs = (tensor ? p.rand_v : p.rand_k) + th * kHeadDim + 16 * sub;
+      const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(rs));
+      const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        lo |= e2m1_code_sr(__fdiv_rn(f[i], den), (rw[i >> 2] >> (8 * (i & 3))) & 0xFFu) << (4 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        hi |= e2m1_code_sr(__fdiv_rn(f[8 + i], den), (rw[2 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu) << (4 * i);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        lo |= e2m1x2_from_f32(__fdiv_rn(f[2 * k], den), __fdiv_rn(f[2 * k + 1], den)) << (8 * k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        hi |= e2m1x2_from_f32(__fdiv_rn(f[8 + 2 * k], den), __fdiv_rn(f[8 + 2 * k + 1], den)) << (8 * k);
+    }
+  }
+  if (!live) return;
+  const int64_t slot = __ldg(p.slots + token);
+  if (slot < 0) return;  // padding
+  if (slot >= p.capacity) {
+    if (sub == 0) flag_error(p.status, NVFP4KV_DEVERR_SLOT);
+    return;
+  }
+  const int64_t row = ((slot >> 4) * p.hkv + h) * kPage + (slot & (kPage - 1));
+  reinterpret_cast<uint2*>((tensor ? p.v_data : p.k_data) + row * kRowBytes)[sub] = make_uint2(lo, hi);
+  uint8_t* scale = tensor ? p.v_scale : p.k_scale;
+  if constexpr (kVariant == NVFP4KV_VARIANT_MXFP4) {
+    if ((sub & 1) == 0) scale[row * (kHeadDim / 32) + (sub >> 1)] = (uint8_t)sbyte;
+  } else {
+    scale[row * kRowScales + sub] = (uint8_t)sbyte;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_variant(int variant, const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens, const uint8_t* rand_k,
+                                    const uint8_t* rand_v, int32_t* device_status, cudaStream_t stream) {
+  VariantParams p;
+  p.k = k;
+  p.v = v;
+  p.slots = slot_mapping;
+  p.rand_k = rand_k;
+  p.rand_v = rand_v;
+  p.rows = num_tokens * c.num_kv_heads * 2;
+  p.hkv = c.num_kv_heads;
+  p.capacity = c.num_pages * (int64_t)c.page_size;
+  p.k_data = c.k_data;
+  p.v_data = c.v_data;
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  p.gk = c.k_global_scale;
+  p.gv = c.v_global_scale;
+  p.status = device_status;
+  const int64_t blocks = (p.rows * 8 + kThreads - 1) / kThreads;
+  if (variant == NVFP4KV_VARIANT_SR)
+    quantize_variant_kernel<NVFP4KV_VARIANT_SR><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+  else if (variant == NVFP4KV_VARIANT_HADAMARD)
+    quantize_variant_kernel<NVFP4KV_VARIANT_HADAMARD><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+  else
+    quantize_variant_kernel<NVFP4KV_VARIANT_MXFP4><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4kv
