@@ -469,6 +469,23 @@ def secondary(torch, kv, args, flush, hbm_peak):
     gbs = (vals * 2 + vals * 9 // 16 + vals + 16 * ew.batch * ew.chunk_len) / (t / 1e3) / 1e9
     out["extend_quantize_write_fp8_fused_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs,
                                                         "frac_of_measured_peak": gbs / hbm_peak}
+    # the format variants' quantize-append of the same chunk (comparison paths)
+    rk = _dev(torch, inputs.rounding_bytes(10, kc.numel())).view(kc.shape)
+    rv = _dev(torch, inputs.rounding_bytes(11, vc.numel())).view(vc.shape)
+    mxs = torch.zeros((ew.num_pages, ew.num_kv_heads, 16, 4), dtype=torch.uint8, device="cuda")
+    mxc = kv.Cache(cache.k_data, cache.v_data, mxs, mxs.clone(), ew.num_pages, ew.num_kv_heads)
+    toks = ew.batch * ew.chunk_len
+    # bytes besides the bf16 read: the pages written (and SR's random byte per value)
+    for name, var, c_, other in (("sr", kv.NVFP4KV_VARIANT_SR, cache, vals * 9 // 16 + vals),
+                                  ("hadamard", kv.NVFP4KV_VARIANT_HADAMARD, cache, vals * 9 // 16),
+                                  ("mxfp4", kv.NVFP4KV_VARIANT_MXFP4, mxc, vals // 2 + vals // 32)):
+        ms, _ = time_steps(torch, steps, args.warmup,
+                           lambda ev=None, var=var, c_=c_: kv.nvfp4kv_quantize_append_variant(var, c_, kc, vc, slots,
+                                                                                              rk, rv), flush)
+        t = float(np.mean(ms))
+        gbs = (2 * vals + other + 8 * toks) / (t / 1e3) / 1e9
+        out[f"extend_quantize_variant_{name}_per_layer"] = {"kernel_ms": t, "hbm_gbs": gbs,
+                                                             "frac_of_measured_peak": gbs / hbm_peak}
     q = _bf16(torch, ew.q(0))
     cq = _dev(torch, ew.cu_q)
     o = torch.empty((q.shape[0], ew.num_q_heads, 128), dtype=torch.float32, device="cuda")
