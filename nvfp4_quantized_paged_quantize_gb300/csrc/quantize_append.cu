@@ -188,14 +188,13 @@ cudaError_t launch_quantize(QuantParams& p, int num_sms, cudaStream_t stream) {
   int blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
   // a persistent grid: as many blocks as fit on the device at once (more
   // blocks, each doing less, measured slower)
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static const int per_sm = [] {  // once per instantiation, thread-safely
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_append_kernel<kWs>, kThreads, 0) != cudaSuccess ||
         n < 1)
       n = 1;
-    per_sm = n;
-  }
+    return n;
+  }();
   const int max_blocks = num_sms * per_sm;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;

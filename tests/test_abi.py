@@ -186,3 +186,17 @@ def test_fused_write_host_checks(lib):
     assert f(P(cs), 16, 16, 8, 4, 12, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
     assert f(P(cs), 18, 16, 8, 4, 8, 10, 1.0, 1.0, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
     assert f(P(cs), None, None, None, 0, None, 10, 1.0, 1.0, None, None, None, None) == kv.NVFP4KV_OK
+
+
+def test_variant_append_host_checks(lib):
+    cs = _fake_cache().c_struct()
+    f = lib.nvfp4kv_quantize_append_variant
+    P = ctypes.byref
+    # (variant, cache, k, v, slots, n, rand_k, rand_v, status, stream)
+    assert f(0, P(cs), 16, 16, 8, 4, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT   # unknown variant
+    assert f(4, P(cs), 16, 16, 8, 4, 16, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(kv.NVFP4KV_VARIANT_SR, P(cs), 16, 16, 8, 4, None, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(kv.NVFP4KV_VARIANT_SR, P(cs), 16, 16, 8, 4, 24, 16, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
+    assert f(kv.NVFP4KV_VARIANT_MXFP4, P(cs), 18, 16, 8, 4, None, None, None, None) == \
+        kv.NVFP4KV_ERR_INVALID_ARGUMENT                                                      # misaligned k
+    assert f(kv.NVFP4KV_VARIANT_HADAMARD, P(cs), None, None, None, 0, None, None, None, None) == kv.NVFP4KV_OK
