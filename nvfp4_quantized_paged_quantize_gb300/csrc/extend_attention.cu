@@ -139,16 +139,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-// 16-byte read-only load that does not allocate in L1: each K/V byte is read
-// once per CTA, and the L1 is the kernel's busiest unit
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -264,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
         const int64_t off = (row * p.hkv + hk) * kHeadDim + part * 16;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          xk[g][h] = live ? ldg_stream(p.ws_k + off + h * 64) : make_uint4(0, 0, 0, 0);
-          xv[g][h] = live ? ldg_stream(p.ws_v + off + h * 64) : make_uint4(0, 0, 0, 0);
+          xk[g][h] = live ? __ldg(reinterpret_cast<const uint4*>(p.ws_k + off + h * 64)) : make_uint4(0, 0, 0, 0);
+          xv[g][h] = live ? __ldg(reinterpret_cast<const uint4*>(p.ws_v + off + h * 64)) : make_uint4(0, 0, 0, 0);
         }
       }
     };
