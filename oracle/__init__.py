@@ -91,6 +91,9 @@ def lib():
         L.nvfp4_oracle_quantize_block_sr.restype = None
         L.nvfp4_oracle_hadamard.argtypes = [vp, ctypes.c_int, vp]
         L.nvfp4_oracle_hadamard.restype = ctypes.c_int
+        L.nvfp4_oracle_decode_attention_format.argtypes = [ctypes.POINTER(_CCache), ctypes.c_int, vp, vp, i32, vp,
+                                                           i32, i32, f64, vp]
+        L.nvfp4_oracle_decode_attention_format.restype = ctypes.c_int
         L.nvfp4_oracle_bf16_to_fp8_workspace.argtypes = [vp, vp, vp, i64, i32, i32, i64, f32, f32, vp, vp]
         L.nvfp4_oracle_bf16_to_fp8_workspace.restype = ctypes.c_int
         L.nvfp4_oracle_extend_attention_rows.argtypes = [vp, vp, i64, i32, i32, f32, f32, vp, i32, vp, vp, vp,
@@ -390,6 +393,24 @@ def fake_quant(x, variant: str, g: float = 1.0, rand=None) -> np.ndarray:
             h = np.block([[h, h], [h, -h]])
         out = (out.reshape(-1, n) @ (h / np.sqrt(n))).reshape(-1)
     return out
+
+
+
+FORMAT_NVFP4, FORMAT_NVFP4_HADAMARD, FORMAT_MXFP4 = 0, 1, 2
+
+
+def decode_attention_format(cache: Cache, fmt: int, q_bf16, page_table, seq_lens, softmax_scale):
+    """fp64 decode attention over a variant's cache (FORMAT_*); for MXFP4 the
+    cache's scale arrays hold head_dim / 32 E8M0 bytes per row."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, d = q.shape
+    out = np.zeros((B, Hq, d), np.float64)
+    c = cache._c()
+    st = lib().nvfp4_oracle_decode_attention_format(ctypes.byref(c), int(fmt), _ptr(q), _ptr(pt), pt.shape[1],
+                                                    _ptr(sl), B, Hq, float(softmax_scale), _ptr(out))
+    return out, st
 
 
 __all__ = [name for name in dir() if not name.startswith("_")]

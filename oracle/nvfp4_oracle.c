@@ -376,6 +376,99 @@ int nvfp4_oracle_dequant_to_fp8_workspace(const nvfp4_oracle_cache* c, const int
 }
 
 /* ------------------------------------------------------------------------- */
+/* Decode attention over a cache written by a format variant (the decode side */
+/* of the comparison the pages draw between NVFP4 and its variants).          */
+/*   format 0: NVFP4, as nvfp4_oracle_decode_attention;                       */
+/*   format 1: NVFP4 of Hadamard-rotated rows: each dequantised row is        */
+/*             rotated back (the orthonormal transform is its own inverse;    */
+/*             binary64 butterflies) before the attention;                    */
+/*   format 2: MXFP4: head_dim/32 E8M0 scale bytes per row, value =           */
+/*             E2M1(code) * 2^(scale - 127); the global scales are not used.   */
+/* ------------------------------------------------------------------------- */
+
+static void variant_row(const nvfp4_oracle_cache* c, const value_tables* vt, int format, int which,
+                        int64_t page, int h, int off, double* dst) {
+  const int d = c->head_dim;
+  if (format == 2) {
+    const int64_t r = row_index(page, h, off, c->num_kv_heads, c->page_size);
+    const uint8_t* data = (which == 0 ? c->k_data : c->v_data) + r * nvfp4_oracle_row_bytes(d);
+    const uint8_t* scl = (which == 0 ? c->k_scale : c->v_scale) + r * (d / 32);
+    for (int dd = 0; dd < d; ++dd) {
+      const uint8_t byte = data[dd / 2];
+      const uint8_t code = (dd & 1) ? (byte >> 4) : (byte & 0xF);
+      dst[dd] = vt->e2m1[code] * nvfp4_oracle_e8m0_value(scl[dd / 32]);
+    }
+    return;
+  }
+  cached_row(c, vt, which, page, h, off, dst);
+  if (format == 1) {
+    for (int hh = 1; hh < d; hh *= 2)
+      for (int i = 0; i < d; i += 2 * hh)
+        for (int j = i; j < i + hh; ++j) {
+          const double a = dst[j], b = dst[j + hh];
+          dst[j] = a + b;
+          dst[j + hh] = a - b;
+        }
+    const double sc = 1.0 / sqrt((double)d);
+    for (int dd = 0; dd < d; ++dd) dst[dd] *= sc;
+  }
+}
+
+int nvfp4_oracle_decode_attention_format(const nvfp4_oracle_cache* c, int format, const uint16_t* q_bf16,
+                                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                                         int32_t batch, int32_t num_q_heads, double softmax_scale, double* out) {
+  const int d = c->head_dim, H = c->num_kv_heads, P = c->page_size;
+  if (format < 0 || format > 2 || d > 512 || d % 32 != 0 || (d & (d - 1)) != 0 || H <= 0 ||
+      num_q_heads % H != 0)
+    return -1;
+  const int G = num_q_heads / H;
+  int bad = 0;
+  value_tables vt;
+  build_tables(&vt);
+  double row[512];
+  for (int32_t b = 0; b < batch; ++b) {
+    int64_t L = seq_lens[b];
+    if (L < 0 || L > (int64_t)max_pages * P) { bad = 1; L = L < 0 ? 0 : (int64_t)max_pages * P; }
+    for (int hq = 0; hq < num_q_heads; ++hq) {
+      double* o = out + ((int64_t)b * num_q_heads + hq) * d;
+      for (int dd = 0; dd < d; ++dd) o[dd] = 0.0;
+      if (L == 0) continue;
+      const int hk = hq / G;
+      double q[512];
+      for (int dd = 0; dd < d; ++dd)
+        q[dd] = nvfp4_oracle_bf16_to_float(q_bf16[((int64_t)b * num_q_heads + hq) * d + dd]);
+      double* s = (double*)malloc(sizeof(double) * (size_t)L);
+      int* valid = (int*)malloc(sizeof(int) * (size_t)L);
+      double m = -INFINITY;
+      for (int64_t t = 0; t < L; ++t) {
+        const int32_t page = page_table[(int64_t)b * max_pages + t / P];
+        valid[t] = page >= 0 && page < c->num_pages;
+        if (!valid[t]) { bad = 1; continue; }
+        variant_row(c, &vt, format, 0, page, hk, (int)(t % P), row);
+        double acc = 0.0;
+        for (int dd = 0; dd < d; ++dd) acc += q[dd] * row[dd];
+        s[t] = softmax_scale * acc;
+        if (s[t] > m) m = s[t];
+      }
+      double l = 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        if (!valid[t]) continue;
+        const double w = exp(s[t] - m);
+        l += w;
+        const int32_t page = page_table[(int64_t)b * max_pages + t / P];
+        variant_row(c, &vt, format, 1, page, hk, (int)(t % P), row);
+        for (int dd = 0; dd < d; ++dd) o[dd] += w * row[dd];
+      }
+      if (l > 0.0)
+        for (int dd = 0; dd < d; ++dd) o[dd] /= l;
+      free(s);
+      free(valid);
+    }
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Extend (chunked prefill) over the FP8 workspace ("nvfp4-kv-cache-memory-  */
 /* wall", section 3, item 2 and the data-flow figure: the chunk attends over */
 /* its cached prefix, dequantised into the FP8 workspace, and over itself;   */

@@ -81,6 +81,13 @@ void nvfp4_oracle_quantize_block_sr(const float x[NVFP4_ORACLE_BLOCK], float g, 
                                     uint8_t packed[NVFP4_ORACLE_BLOCK / 2], uint8_t* scale);
 int nvfp4_oracle_hadamard(const float* x, int n, float* y);
 
+/* Decode attention over a variant's cache: format 0 NVFP4, 1 NVFP4 of
+ * Hadamard-rotated rows (rotated back before the attention), 2 MXFP4 (scale
+ * pools of head_dim/32 E8M0 bytes per row). */
+int nvfp4_oracle_decode_attention_format(const nvfp4_oracle_cache* c, int format, const uint16_t* q_bf16,
+                                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                                         int32_t batch, int32_t num_q_heads, double softmax_scale, double* out);
+
 /* Extend over the FP8 workspace.  The chunk's K/V rows enter the workspace
  * from bf16 (w = E4M3(fp32(x) / s_ws), signed); ws_rows[t] < 0 skips token t.
  * Extend attention evaluates, in binary64, the output rows named by pairs

@@ -9,44 +9,12 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
 from gpu_util import bf16_dev, dev, status_word
+from variant_util import oracle_variant_pools
 
 pytestmark = pytest.mark.gpu
-
-
-def _oracle_variant(variant, k, v, slots, pages, H, gk, gv, rk=None, rv=None):
-    """The variant's pools (data [rows, 64], scales [rows, 8 or 4]) from the oracle's block functions."""
-    rows = pages * H * 16
-    nsc = 4 if variant == kv.NVFP4KV_VARIANT_MXFP4 else 8
-    out = {t: (np.zeros((rows, 64), np.uint8), np.zeros((rows, nsc), np.uint8)) for t in "kv"}
-    for t, slot in enumerate(slots):
-        if slot < 0 or slot >= pages * 16:
-            continue
-        for h in range(H):
-            row = ((slot // 16) * H + h) * 16 + slot % 16
-            for name, bits, g, rnd in (("k", k, gk, rk), ("v", v, gv, rv)):
-                x = inputs.bf16_bits_to_f32(bits[t, h])
-                data, scale = out[name]
-                if variant == kv.NVFP4KV_VARIANT_MXFP4:
-                    for j in range(4):
-                        packed, sc = oracle.mxfp4_quantize_block(x[32 * j:32 * j + 32])
-                        data[row, 16 * j:16 * j + 16] = packed
-                        scale[row, j] = sc
-                    continue
-                if variant == kv.NVFP4KV_VARIANT_HADAMARD:
-                    x = oracle.hadamard(x)
-                for j in range(8):
-                    blk = x[16 * j:16 * j + 16]
-                    if variant == kv.NVFP4KV_VARIANT_SR:
-                        packed, sc = oracle.quantize_block_sr(blk, g, rnd[t, h, 16 * j:16 * j + 16])
-                    else:
-                        packed, sc = oracle.quantize_block(blk, g)
-                    data[row, 8 * j:8 * j + 8] = packed
-                    scale[row, j] = sc
-    return out
 
 
 @pytest.mark.parametrize("variant", [kv.NVFP4KV_VARIANT_SR, kv.NVFP4KV_VARIANT_HADAMARD, kv.NVFP4KV_VARIANT_MXFP4])
@@ -71,7 +39,7 @@ def test_variant_quantize_bit_exact(cuda_lib, variant, gk, gv):
                                        device_status=st)
     torch.cuda.synchronize()
     assert st.item() & kv.NVFP4KV_DEVERR_SLOT
-    want = _oracle_variant(variant, k, v, slots, pages, H, np.float32(gk), np.float32(gv), rk, rv)
+    want = oracle_variant_pools(variant, k, v, slots, pages, H, np.float32(gk), np.float32(gv), rk, rv)
     rows = pages * H * 16
     for name, (data, scale) in want.items():
         gd = (cache.k_data if name == "k" else cache.v_data).reshape(rows, -1).cpu().numpy()

@@ -189,3 +189,125 @@ def test_rmse_report_variants(name, x, capsys):
               f"; mean error nvfp4 {bias['nvfp4']:.2e}, nvfp4_sr {bias['nvfp4_sr']:.2e}")
     assert rm["mxfp4"] > rm["nvfp4"]                   # the pages: NVFP4's finer, E4M3-scaled blocks win
     assert rm["nvfp4_sr"] >= rm["nvfp4"]               # stochastic rounding trades RMSE for no bias
+
+
+# --------------------------------------------------------------------------
+# decode over a variant's cache
+# --------------------------------------------------------------------------
+
+from variant_util import HADAMARD, MXFP4, SR, oracle_variant_pools  # noqa: E402
+
+
+def _variant_cache(wl, variant, b_count=None, rk=None, rv=None):
+    """An oracle cache holding the first b_count sequences of a decode workload (prompt + new token)."""
+    prompts = wl.all_prompt_kv()
+    new_k, new_v = wl.new_kv()
+    B = wl.batch if b_count is None else b_count
+    ks, vs, ss = [], [], []
+    for b in range(B):
+        k, v = prompts[b]
+        ks += [k, new_k[b:b + 1]]
+        vs += [v, new_v[b:b + 1]]
+        ss += [wl.slots(b, 0, k.shape[0]), wl.append_slots()[b:b + 1]]
+    k, v, slots = np.concatenate(ks), np.concatenate(vs), np.concatenate(ss)
+    pools = oracle_variant_pools(variant, k, v, slots, wl.num_pages, wl.num_kv_heads, 1.0, 1.0, rk, rv)
+    c = oracle.Cache(wl.num_pages, wl.num_kv_heads, 128, 16,
+                     arrays=(pools["k"][0], pools["v"][0], pools["k"][1], pools["v"][1]))
+    return c, k, v, slots
+
+
+def _sdpa(q, K, V, scale):
+    import torch
+
+    G = q.shape[0] // K.shape[0]
+    out = np.zeros_like(q)
+    for h in range(K.shape[0]):
+        Q = torch.from_numpy(q[h * G:(h + 1) * G])[:, None, :]              # [G, 1, d]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            Q, torch.from_numpy(K[h])[None].expand(G, -1, -1), torch.from_numpy(V[h])[None].expand(G, -1, -1),
+            scale=scale)
+        out[h * G:(h + 1) * G] = o[:, 0, :].numpy()
+    return out
+
+
+def _dequant_rows(c, which, fmt):
+    """Every pool row in fp64, decoded here without the oracle: E2M1 from the
+    pages' value list, E4M3 through torch's float8_e4m3fn, E8M0 as 2^(s - 127)."""
+    import torch
+
+    vals = np.array(E2M1 + [-v for v in E2M1])
+    data = c.k_data if which == "k" else c.v_data
+    scl = c.k_scale if which == "k" else c.v_scale
+    codes = np.stack([data & 0xF, data >> 4], -1).reshape(data.shape[0], -1)
+    x = vals[codes]
+    if fmt == oracle.FORMAT_MXFP4:
+        return x * np.repeat(2.0 ** (scl.astype(np.float64) - 127), 32, axis=1)
+    sc = torch.from_numpy(np.ascontiguousarray(scl)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    x = x * np.repeat(sc, 16, axis=1)
+    if fmt == oracle.FORMAT_NVFP4_HADAMARD:
+        x = x @ _hadamard_matrix(128)                                       # symmetric, its own inverse
+    return x
+
+
+@pytest.mark.parametrize("fmt,variant", [(oracle.FORMAT_NVFP4, None), (oracle.FORMAT_NVFP4_HADAMARD, HADAMARD),
+                                         (oracle.FORMAT_MXFP4, MXFP4)])
+def test_variant_decode_matches_sdpa(fmt, variant):
+    wl = inputs.decode_config(1)                           # B = 2, lengths {101, 258}, 8 q / 2 KV heads
+    if variant is None:
+        c = oracle.Cache(wl.num_pages, wl.num_kv_heads)
+        for b, (k, v) in enumerate(wl.all_prompt_kv()):
+            oracle.quantize_append(c, k, v, wl.slots(b, 0, k.shape[0]))
+        nk, nv = wl.new_kv()
+        oracle.quantize_append(c, nk, nv, wl.append_slots())
+    else:
+        c, _, _, _ = _variant_cache(wl, variant)
+    q = wl.q()
+    got, st = oracle.decode_attention_format(c, fmt, q, wl.page_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    if fmt == oracle.FORMAT_NVFP4:
+        same, _ = oracle.decode_attention(c, q, wl.page_table, wl.seq_lens, wl.softmax_scale)
+        assert np.array_equal(got, same)
+    Kr, Vr = _dequant_rows(c, "k", fmt), _dequant_rows(c, "v", fmt)
+    qf = inputs.bf16_bits_to_f32(q).astype(np.float64)
+    H = wl.num_kv_heads
+    for b in range(wl.batch):
+        L = int(wl.seq_lens[b])
+        t = np.arange(L)
+        slot = wl.page_table[b, t // 16].astype(np.int64) * 16 + t % 16
+        rows = ((slot // 16)[None, :] * H + np.arange(H)[:, None]) * 16 + (slot % 16)[None, :]   # [H, L]
+        ref = _sdpa(qf[b], Kr[rows], Vr[rows], wl.softmax_scale)
+        np.testing.assert_allclose(got[b], ref, rtol=1e-10, atol=1e-10)
+
+
+def test_attention_error_report_variants(capsys):
+    # decode attention over each variant's cache against attention over the
+    # unquantised bf16 K/V (8K workload's values, 3 sequences of 129 tokens)
+    wl = inputs.decode_config(2, 1 / 64)
+    B = 3
+    q = wl.q()[:B]
+    rows_k = inputs.rounding_bytes(20, 10 ** 6)
+    errs = {}
+    for name, fmt, variant in (("nvfp4", oracle.FORMAT_NVFP4, 0), ("mxfp4", oracle.FORMAT_MXFP4, MXFP4),
+                               ("nvfp4_sr", oracle.FORMAT_NVFP4, SR),
+                               ("nvfp4_hadamard", oracle.FORMAT_NVFP4_HADAMARD, HADAMARD)):
+        n = sum(int(l) for l in wl.seq_lens[:B])
+        rk = rows_k[: n * wl.num_kv_heads * 128].reshape(n, wl.num_kv_heads, 128)
+        rv = rows_k[-n * wl.num_kv_heads * 128:].reshape(n, wl.num_kv_heads, 128)
+        c, k, v, slots = _variant_cache(wl, variant, B, rk, rv)
+        got, st = oracle.decode_attention_format(c, fmt, q, wl.page_table[:B], wl.seq_lens[:B], wl.softmax_scale)
+        assert st == 0
+        # exact attention over the bf16 values, gathered in token order
+        kf, vf = inputs.bf16_bits_to_f32(k).astype(np.float64), inputs.bf16_bits_to_f32(v).astype(np.float64)
+        qf = inputs.bf16_bits_to_f32(q).astype(np.float64)
+        rel, start = [], 0
+        for b in range(B):
+            L = int(wl.seq_lens[b])
+            toks = np.concatenate([np.arange(start, start + L - 1), [start + L - 1]])
+            ref = _sdpa(qf[b], kf[toks].transpose(1, 0, 2), vf[toks].transpose(1, 0, 2), wl.softmax_scale)
+            rel.append(np.abs(got[b] - ref).max(axis=-1) / np.linalg.norm(ref, axis=-1))
+            start += L
+        errs[name] = float(np.mean(np.concatenate(rel)))
+    with capsys.disabled():
+        print("\nattention error vs bf16 K/V (mean over rows of max-abs / row norm): " +
+              ", ".join(f"{k} {v:.3e}" for k, v in errs.items()))
+    assert errs["mxfp4"] > errs["nvfp4"]
