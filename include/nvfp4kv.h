@@ -58,8 +58,9 @@ typedef struct CUstream_st* nvfp4kv_stream_t;
 enum {
   NVFP4KV_OK = 0,
   NVFP4KV_ERR_INVALID_ARGUMENT = -1, /* null pointer, bad size, misaligned pool, bad scale */
-  NVFP4KV_ERR_UNSUPPORTED = -2,      /* head_dim != 128, page_size != 16, GQA group > 8, or
-                                        sizes whose indices would not fit in 32 bits */
+  NVFP4KV_ERR_UNSUPPORTED = -2,      /* head_dim != 128, page_size != 16, a GQA group the call
+                                        does not take (decode: > 8; extend: not a power of two
+                                        <= 128), or sizes whose indices would not fit */
   NVFP4KV_ERR_CUDA = -3,             /* a CUDA runtime call or launch failed */
   NVFP4KV_ERR_WORKSPACE = -4         /* workspace null, too small or misaligned */
 };
