@@ -232,3 +232,9 @@ def test_initial_prefill_through_the_fused_write(cuda_lib):
     ref, st = oracle.extend_attention(owk, owv, q, case.cu_q, case.cu_prefix, case.prefix_lens, case.softmax_scale)
     assert st == 0
     check_rows(got, ref)
+
+
+def test_extend_layer_79_pipeline(cuda_lib):
+    # the last of the 80 layers (its own seeds), at 1/32 of the lengths
+    same, _ = _pipeline(inputs.extend_config(scale=1 / 32, num_layers=80), 79, 4, np.random.default_rng(79))
+    assert same
