@@ -16,7 +16,6 @@ metric, bounded samples).  With torchrun (N > 1) every rank runs a replica.
 """
 import argparse
 import json
-import math
 import os
 import subprocess
 import sys

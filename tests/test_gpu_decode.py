@@ -11,7 +11,7 @@ import torch
 import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import (ATTN_TOL, bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
+from gpu_util import (bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
                       gpu_cache, gpu_global_scales, oracle_global_scales, oracle_pair, pool_host, status_word)
 
 pytestmark = pytest.mark.gpu

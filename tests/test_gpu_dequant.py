@@ -10,7 +10,7 @@ import torch
 import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import bf16_dev, dev, gpu_append, gpu_cache, status_word
+from gpu_util import dev, gpu_append, gpu_cache, status_word
 
 pytestmark = pytest.mark.gpu
 

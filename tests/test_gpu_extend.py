@@ -13,7 +13,7 @@ import torch
 import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import ATTN_TOL, bf16_dev, check_rows, dev, gpu_append, gpu_cache, pool_host, status_word
+from gpu_util import bf16_dev, check_rows, dev, gpu_append, gpu_cache, pool_host, status_word
 
 pytestmark = pytest.mark.gpu
 
