@@ -190,6 +190,21 @@ def _fill_cache(torch, kv, wl, prompts, new):
     return cache
 
 
+def _fill_cache_streaming(torch, kv, wl, threads=16):
+    """The cache of an uncalibrated workload (global scales 1), each sequence
+    drawn by a worker thread and appended as soon as it is ready, so the host
+    never holds the whole batch (the ragged workload is 7.4 GB of bf16)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    cache = kv.Cache.empty(wl.num_pages, wl.num_kv_heads, zero=True)
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for b, (k, v) in enumerate(ex.map(wl.prompt_kv, range(wl.batch))):
+            kv.nvfp4kv_quantize_append(cache, _bf16(torch, k), _bf16(torch, v),
+                                       _dev(torch, wl.slots(b, 0, k.shape[0])))
+    torch.cuda.synchronize()
+    return cache
+
+
 def _calibration_input(torch, wl):
     """One layer's K of a decode workload as one bf16 device tensor: the first
     sequence's prompt K drawn by the workload, repeated over the batch."""
@@ -203,11 +218,14 @@ class DecodeBench:
 
     def __init__(self, torch, kv, wl):
         self.torch, self.kv, self.wl = torch, kv, wl
-        prompts = wl.all_prompt_kv(threads=16)
         self.new = wl.new_kv() if wl.append else None
         self.q_bits = wl.q()
-        self.cache = _fill_cache(torch, kv, wl, prompts, self.new)
-        del prompts
+        if wl.calibrated:
+            prompts = wl.all_prompt_kv(threads=16)
+            self.cache = _fill_cache(torch, kv, wl, prompts, self.new)
+            del prompts
+        else:
+            self.cache = _fill_cache_streaming(torch, kv, wl)
         self.q = _bf16(torch, self.q_bits)
         self.pt = _dev(torch, wl.page_table)
         self.lens = _dev(torch, wl.seq_lens.astype(np.int32))
@@ -419,6 +437,19 @@ def secondary(torch, kv, args, flush, hbm_peak):
                                 "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS, "frac_of_measured_peak": gbs / hbm_peak}
     del b
     torch.cuda.empty_cache()
+    # ragged continuous batching: 256 sequences, log-uniform lengths in [512,
+    # 32768] (+1 appended), 32 q / 8 KV heads; the bytes are those of the
+    # seeded lengths
+    wl4 = inputs.decode_config(4)
+    b = DecodeBench(torch, kv, wl4)
+    ms, _ = time_steps(torch, steps, args.warmup, lambda ev=None: b.decode(), flush)
+    t = float(np.mean(ms))
+    gbs = wl4.algorithmic_bytes() / (t / 1e3) / 1e9
+    out["decode_ragged_b256"] = {"kernel_ms": t, "kv_tokens_per_s": wl4.kv_tokens() / (t / 1e3), "hbm_gbs": gbs,
+                                 "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS, "frac_of_measured_peak": gbs / hbm_peak,
+                                 "algorithmic_bytes": wl4.algorithmic_bytes(), "kv_tokens": wl4.kv_tokens()}
+    del b
+    torch.cuda.empty_cache()
     # calibration: the amax pass over one layer's K of that workload (4 x 131072
     # tokens x 8 heads x 128 bf16 values, 1.07 GB), HBM-bound at 2 B per value
     x, amax = _calibration_input(torch, wl)
@@ -471,8 +502,7 @@ def secondary(torch, kv, args, flush, hbm_peak):
     # the format variants' quantize-append of the same chunk (comparison paths)
     rk = _dev(torch, inputs.rounding_bytes(10, kc.numel())).view(kc.shape)
     rv = _dev(torch, inputs.rounding_bytes(11, vc.numel())).view(vc.shape)
-    mxs = torch.zeros((ew.num_pages, ew.num_kv_heads, 16, 4), dtype=torch.uint8, device="cuda")
-    mxc = kv.Cache(cache.k_data, cache.v_data, mxs, mxs.clone(), ew.num_pages, ew.num_kv_heads)
+    mxc = kv.Cache.empty(ew.num_pages, ew.num_kv_heads, zero=True, mxfp4=True)
     toks = ew.batch * ew.chunk_len
     # bytes besides the bf16 read: the pages written (and SR's random byte per value)
     for name, var, c_, other in (("sr", kv.NVFP4KV_VARIANT_SR, cache, vals * 9 // 16 + vals),
@@ -647,8 +677,8 @@ def only_arm(args):
     if args.only == "calibrate":
         x, amax = _calibration_input(torch, inputs.decode_config(3))
         time_steps(torch, args.steps, args.warmup, lambda ev=None: kv.nvfp4kv_tensor_amax(x, amax), flush)
-    elif args.only in ("decode8k", "decode128k"):
-        b = DecodeBench(torch, kv, inputs.decode_config(2 if args.only == "decode8k" else 3))
+    elif args.only in ("decode8k", "decode128k", "ragged"):
+        b = DecodeBench(torch, kv, inputs.decode_config({"decode8k": 2, "decode128k": 3, "ragged": 4}[args.only]))
         time_steps(torch, args.steps, args.warmup, lambda ev=None: (b.append(), b.decode()), flush)
     else:
         ew = inputs.extend_config(num_layers=1)
@@ -687,7 +717,7 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--cpu-total-s", type=float, default=90.0, help="reference arm: total oracle seconds")
-    ap.add_argument("--only", choices=["decode8k", "decode128k", "extend", "calibrate"],
+    ap.add_argument("--only", choices=["decode8k", "decode128k", "ragged", "extend", "calibrate"],
                     help="run just one workload's kernels (profiler command lines); no JSON metric line")
     args = ap.parse_args()
     if args.warmup < 3:

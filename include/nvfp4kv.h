@@ -18,14 +18,20 @@
  * Inputs (K, V, q) must be finite; non-finite inputs give unspecified codes
  * and outputs (never an out-of-bounds access).
  *
- * Cache layout (all arrays caller-owned device memory, byte-addressed):
- *     k_data, v_data   : uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
- *                        element 2i of a row in the low nibble of byte i
- *     k_scale, v_scale : uint8 [num_pages][num_kv_heads][page_size][head_dim/16]
- *                        E4M3 block scale j covers elements 16j..16j+15
+ * Cache layout (one caller-owned device pool, byte-addressed):
+ *     pages : uint8 [num_pages][num_kv_heads][NVFP4KV_PAGE_HEAD_BYTES]
+ * One page-head (16 tokens of one KV head of one page) is 2304 contiguous
+ * bytes, and the page-heads of a page follow one another, so a whole page
+ * (every KV head) is one contiguous run of num_kv_heads * 2304 bytes:
+ *     [   0, 1024)  K data    16 rows x 64 bytes; element 2i of a row in the
+ *                             low nibble of byte i
+ *     [1024, 1152)  K scales  16 rows x 8 E4M3 bytes; scale j covers elements
+ *                             16j..16j+15 of the row
+ *     [1152, 2176)  V data    as K
+ *     [2176, 2304)  V scales  as K
  * A slot s is row (s % page_size) of page (s / page_size).  Supported:
- * head_dim = 128, page_size = 16.  All four base pointers must be 16-byte
- * aligned.
+ * head_dim = 128, page_size = 16.  The pool must be 16-byte aligned (256-byte
+ * alignment lets every page-head start on a 128-byte line).
  *
  * Conventions for every call:
  *   - All pointers named device are CUDA device pointers; the library never
@@ -83,12 +89,17 @@ enum {
                                  (an attention key reads as zero) */
 };
 
+/* Bytes of one page-head: 16 rows of K data and scales, then of V (9/16 byte
+ * per value). */
+#define NVFP4KV_PAGE_HEAD_BYTES 2304
+/* Bytes of one page-head of the MXFP4 variant's pool (4 E8M0 scale bytes per
+ * row): K data [0, 1024), K scales [1024, 1088), V data [1088, 2112),
+ * V scales [2112, 2176). */
+#define NVFP4KV_MXFP4_PAGE_HEAD_BYTES 2176
+
 /* One layer's paged NVFP4 cache.  The struct itself is read on the host only. */
 typedef struct nvfp4kv_cache {
-  uint8_t* k_data;      /* device, [num_pages][num_kv_heads][page_size][head_dim/2] */
-  uint8_t* v_data;      /* device, same shape */
-  uint8_t* k_scale;     /* device, [num_pages][num_kv_heads][page_size][head_dim/16] */
-  uint8_t* v_scale;     /* device, same shape */
+  uint8_t* pages;       /* device, [num_pages][num_kv_heads][NVFP4KV_PAGE_HEAD_BYTES] */
   int64_t num_pages;    /* > 0 */
   int32_t num_kv_heads; /* > 0 */
   int32_t head_dim;     /* 128 */
@@ -98,13 +109,15 @@ typedef struct nvfp4kv_cache {
 } nvfp4kv_cache;
 
 /*
- * Bytes of one data pool and of one scale pool (each of K and V) for a cache
- * of this shape: num_pages*num_kv_heads*page_size*head_dim/2 and /16.  The
- * per-value total is 9/16 byte ("nvfp4-kv-cache-memory-wall", section 1).
- * Host only.  Returns NVFP4KV_OK or NVFP4KV_ERR_INVALID_ARGUMENT.
+ * Bytes of the pool of a cache of this shape:
+ * num_pages * num_kv_heads * page_size * 2 * (head_dim/2 + head_dim/16), i.e.
+ * 9/16 byte per K or V value ("nvfp4-kv-cache-memory-wall", section 1).
+ * Host only.  Returns NVFP4KV_OK, NVFP4KV_ERR_INVALID_ARGUMENT (null output,
+ * non-positive sizes, head_dim not a multiple of 16) or NVFP4KV_ERR_UNSUPPORTED
+ * (a size that overflows).
  */
 int nvfp4kv_cache_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t head_dim,
-                        int32_t page_size, size_t* data_bytes, size_t* scale_bytes);
+                        int32_t page_size, size_t* pool_bytes);
 
 /*
  * Quantise new K and V tokens into the cache ("nvfp4-kv-cache-memory-wall",
@@ -131,6 +144,19 @@ int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const voi
  */
 int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
                                   size_t* bytes);
+
+/*
+ * The same size from the batch shape alone, for callers that size the
+ * workspace before a cache exists: bytes enough for any cache with
+ * num_q_heads / G KV heads, on a device with num_sms SMs (pass that device's
+ * cudaDevAttrMultiProcessorCount).  max_seq_len is accepted and ignored: the
+ * split-K partition cuts the pages of all sequences together into as many
+ * ranges as the device runs at once, so the scratch depends on the SM count
+ * and the number of (sequence, KV head) pairs, not on any length.  Host only;
+ * returns 0 for batch < 0, num_q_heads <= 0 or num_sms <= 0.
+ */
+size_t nvfp4kv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+                                      int32_t num_sms);
 
 /*
  * Paged decode attention with the NVFP4 dequantisation inside the kernel
@@ -193,7 +219,7 @@ int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, c
                                     int32_t* device_status, nvfp4kv_stream_t stream);
 
 /* Bytes of the fixed device scratch used by nvfp4kv_decode_attention_static. */
-#define NVFP4KV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+#define NVFP4KV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 
 /*
  * nvfp4kv_decode_attention without a caller-provided workspace, for callers
@@ -202,7 +228,7 @@ int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, c
  * The source pages have no counterpart to this call; it only changes where
  * the decode's split-K scratch lives.
  *
- * The scratch is a fixed NVFP4KV_STATIC_SCRATCH_BYTES (16 MiB) array in the
+ * The scratch is a fixed NVFP4KV_STATIC_SCRATCH_BYTES (32 MiB) array in the
  * library's device image: every GPU that loads the library holds it until the
  * process exits.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
@@ -317,8 +343,10 @@ int nvfp4kv_extend_attention(const void* q_bf16, const int64_t* cu_q, int32_t ma
  * ("NVFP4: breaking the memory wall" (cloud.tencent.com): stochastic rounding
  * and a Hadamard rotation before quantisation, MXFP4's 32-value blocks;
  * "NVIDIA NVFP4: LLM memory doubled, inference 3x" (nmedialink), figure 6).
- * Same rows, slots and errors as nvfp4kv_quantize_append; the data pages are
- * the NVFP4 ones.
+ * Same rows, slots and errors as nvfp4kv_quantize_append.  The SR and Hadamard
+ * variants write the NVFP4 pool layout; MXFP4 writes its own page-heads of
+ * NVFP4KV_MXFP4_PAGE_HEAD_BYTES (cache->pages is then
+ * [num_pages][num_kv_heads][NVFP4KV_MXFP4_PAGE_HEAD_BYTES]).
  *   NVFP4KV_VARIANT_SR        the block scale as in NVFP4; each element code
  *                             rounds to one of its two E2M1 neighbours, up iff
  *                             (r + 0.5) / 256 < (|y| - a) / (b - a) for the
@@ -332,10 +360,9 @@ int nvfp4kv_extend_attention(const void* q_bf16, const int64_t* cu_q, int32_t ma
  *                             applies H again (or rotates q the same way)
  *   NVFP4KV_VARIANT_MXFP4     blocks of 32 with a power-of-two scale, the E8M0
  *                             byte e + 127, e = floor(log2 amax) - 2 (clamped to
- *                             [-127, 127]); elements E2M1(x * 2^-e); the scale
- *                             pools hold head_dim / 32 bytes per row
- *                             ([num_pages][num_kv_heads][page_size][4]) and the
- *                             global scales are not used
+ *                             [-127, 127]); elements E2M1(x * 2^-e); each row
+ *                             has head_dim / 32 = 4 scale bytes and the global
+ *                             scales are not used
  * Unknown variants return NVFP4KV_ERR_INVALID_ARGUMENT. */
 int nvfp4kv_quantize_append_variant(int variant, const nvfp4kv_cache* cache, const void* k, const void* v,
                                     const int64_t* slot_mapping, int64_t num_tokens, const uint8_t* rand_k,

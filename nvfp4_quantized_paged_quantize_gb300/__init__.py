@@ -34,6 +34,9 @@ NVFP4KV_VARIANT_MXFP4 = 3
 
 HEAD_DIM = 128
 PAGE_SIZE = 16
+# bytes of one page-head (16 tokens of one KV head): K data, K scales, V data, V scales
+NVFP4KV_PAGE_HEAD_BYTES = 2304
+NVFP4KV_MXFP4_PAGE_HEAD_BYTES = 2176
 
 _lib = None
 
@@ -49,10 +52,7 @@ class Nvfp4kvError(RuntimeError):
 
 class _CCache(ctypes.Structure):
     _fields_ = [
-        ("k_data", ctypes.c_void_p),
-        ("v_data", ctypes.c_void_p),
-        ("k_scale", ctypes.c_void_p),
-        ("v_scale", ctypes.c_void_p),
+        ("pages", ctypes.c_void_p),
         ("num_pages", ctypes.c_int64),
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
@@ -81,9 +81,11 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L = ctypes.CDLL(path)
     vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     pc = ctypes.POINTER(_CCache)
-    L.nvfp4kv_cache_bytes.argtypes = [i64, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.nvfp4kv_cache_bytes.argtypes = [i64, i32, i32, i32, ctypes.POINTER(sz)]
     L.nvfp4kv_quantize_append.argtypes = [pc, vp, vp, vp, i64, vp, vp]
     L.nvfp4kv_decode_workspace_size.argtypes = [pc, i32, i32, ctypes.POINTER(sz)]
+    L.nvfp4kv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.nvfp4kv_decode_workspace_bytes.restype = sz
     L.nvfp4kv_decode_attention.argtypes = [pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz, vp, vp]
     L.nvfp4kv_dequant_to_fp8_workspace.argtypes = [pc, vp, i32, vp, vp, i32, i64, f32, f32, vp, vp, vp, vp]
     L.nvfp4kv_decode_attention_static.argtypes = [pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, vp]
@@ -140,38 +142,64 @@ def _check(func: str, status: int) -> None:
 
 @dataclass
 class Cache:
-    """One layer's paged NVFP4 cache: four caller-owned device byte tensors.
+    """One layer's paged NVFP4 cache: one caller-owned device byte pool.
 
-    k_data/v_data: uint8 [num_pages, num_kv_heads, page_size, head_dim // 2]
-    k_scale/v_scale: uint8 [num_pages, num_kv_heads, page_size, head_dim // 16] (E4M3)
+    pages: uint8 [num_pages, num_kv_heads, 2304]; each page-head holds K data
+    (16 x 64 bytes), K scales (16 x 8 E4M3 bytes), V data, V scales, in that
+    order (include/nvfp4kv.h).  With mxfp4=True the pool holds the MXFP4
+    variant's page-heads of 2176 bytes (4 E8M0 scale bytes per row).
+
+    k_data / v_data ([num_pages, num_kv_heads, 16, 64]) and k_scale / v_scale
+    ([num_pages, num_kv_heads, 16, 8], or 4 for MXFP4) are views of the pool.
     """
-    k_data: object
-    v_data: object
-    k_scale: object
-    v_scale: object
+    pages: object
     num_pages: int
     num_kv_heads: int
     k_global_scale: float = 1.0
     v_global_scale: float = 1.0
     head_dim: int = HEAD_DIM
     page_size: int = PAGE_SIZE
+    mxfp4: bool = False
 
     @classmethod
     def empty(cls, num_pages, num_kv_heads, device="cuda", k_global_scale=1.0, v_global_scale=1.0,
-              zero=False):
+              zero=False, mxfp4=False):
         import torch
 
         mk = torch.zeros if zero else torch.empty
-        shape_d = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 2)
-        shape_s = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 16)
-        return cls(mk(shape_d, dtype=torch.uint8, device=device), mk(shape_d, dtype=torch.uint8, device=device),
-                   mk(shape_s, dtype=torch.uint8, device=device), mk(shape_s, dtype=torch.uint8, device=device),
-                   num_pages, num_kv_heads, k_global_scale, v_global_scale)
+        phb = NVFP4KV_MXFP4_PAGE_HEAD_BYTES if mxfp4 else NVFP4KV_PAGE_HEAD_BYTES
+        return cls(mk((num_pages, num_kv_heads, phb), dtype=torch.uint8, device=device), num_pages, num_kv_heads,
+                   k_global_scale, v_global_scale, mxfp4=mxfp4)
+
+    # byte ranges of a page-head: K data, K scales, V data, V scales
+    def _parts(self):
+        d = PAGE_SIZE * (HEAD_DIM // 2)
+        sc = PAGE_SIZE * (HEAD_DIM // (32 if self.mxfp4 else 16))
+        return (0, d), (d, d + sc), (d + sc, 2 * d + sc), (2 * d + sc, 2 * d + 2 * sc)
+
+    def _view(self, part, row_bytes):
+        lo, hi = self._parts()[part]
+        return self.pages[:, :, lo:hi].unflatten(-1, (PAGE_SIZE, row_bytes))
+
+    @property
+    def k_data(self):
+        return self._view(0, HEAD_DIM // 2)
+
+    @property
+    def k_scale(self):
+        return self._view(1, HEAD_DIM // (32 if self.mxfp4 else 16))
+
+    @property
+    def v_data(self):
+        return self._view(2, HEAD_DIM // 2)
+
+    @property
+    def v_scale(self):
+        return self._view(3, HEAD_DIM // (32 if self.mxfp4 else 16))
 
     def c_struct(self) -> _CCache:
-        return _CCache(_ptr(self.k_data), _ptr(self.v_data), _ptr(self.k_scale), _ptr(self.v_scale),
-                       int(self.num_pages), int(self.num_kv_heads), int(self.head_dim), int(self.page_size),
-                       float(self.k_global_scale), float(self.v_global_scale))
+        return _CCache(_ptr(self.pages), int(self.num_pages), int(self.num_kv_heads), int(self.head_dim),
+                       int(self.page_size), float(self.k_global_scale), float(self.v_global_scale))
 
 
 def nvfp4kv_status_string(status: int) -> str:
@@ -179,12 +207,12 @@ def nvfp4kv_status_string(status: int) -> str:
 
 
 def nvfp4kv_cache_bytes(num_pages: int, num_kv_heads: int, head_dim: int = HEAD_DIM,
-                        page_size: int = PAGE_SIZE) -> tuple[int, int]:
-    d, s = ctypes.c_size_t(), ctypes.c_size_t()
+                        page_size: int = PAGE_SIZE) -> int:
+    """Bytes of the pool of a cache of this shape (9/16 byte per K or V value)."""
+    n = ctypes.c_size_t()
     _check("nvfp4kv_cache_bytes",
-           _L().nvfp4kv_cache_bytes(num_pages, num_kv_heads, head_dim, page_size, ctypes.byref(d),
-                                    ctypes.byref(s)))
-    return d.value, s.value
+           _L().nvfp4kv_cache_bytes(num_pages, num_kv_heads, head_dim, page_size, ctypes.byref(n)))
+    return n.value
 
 
 def nvfp4kv_quantize_append(cache: Cache, k, v, slot_mapping, device_status=None, stream=None) -> None:
@@ -202,6 +230,11 @@ def nvfp4kv_decode_workspace_size(cache: Cache, batch: int, num_q_heads: int) ->
     _check("nvfp4kv_decode_workspace_size",
            _L().nvfp4kv_decode_workspace_size(ctypes.byref(c), batch, num_q_heads, ctypes.byref(n)))
     return n.value
+
+
+def nvfp4kv_decode_workspace_bytes(batch: int, num_q_heads: int, max_seq_len: int, num_sms: int) -> int:
+    """Workspace bytes for a batch shape on a device with num_sms SMs (0 for invalid sizes)."""
+    return int(_L().nvfp4kv_decode_workspace_bytes(int(batch), int(num_q_heads), int(max_seq_len), int(num_sms)))
 
 
 def nvfp4kv_decode_attention(cache: Cache, q, out, page_table, seq_lens, softmax_scale: float, workspace,
@@ -269,7 +302,7 @@ def nvfp4kv_dequant_to_fp8_workspace(cache: Cache, page_table, prefix_lens, cu_p
 def nvfp4kv_quantize_append_variant(variant: int, cache: "Cache", k, v, slot_mapping, rand_k=None, rand_v=None,
                                     device_status=None, stream=None) -> None:
     """Quantize-append of a format variant (NVFP4KV_VARIANT_SR / _HADAMARD / _MXFP4); for MXFP4 the
-    cache's scale tensors are [num_pages, Hkv, 16, 4] E8M0 bytes."""
+    cache is an MXFP4 pool (Cache.empty(..., mxfp4=True): 4 E8M0 scale bytes per row)."""
     c = cache.c_struct()
     _check("nvfp4kv_quantize_append_variant",
            _L().nvfp4kv_quantize_append_variant(int(variant), ctypes.byref(c), _ptr(k), _ptr(v), _ptr(slot_mapping),
@@ -335,8 +368,9 @@ def nvfp4kv_calibrated_global_scale(amax: float) -> float:
     return g.value
 
 
-__all__ = ["Cache", "Nvfp4kvError", "load", "nvfp4kv_cache_bytes", "nvfp4kv_quantize_append",
-           "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
+__all__ = ["Cache", "Nvfp4kvError", "load", "NVFP4KV_PAGE_HEAD_BYTES", "NVFP4KV_MXFP4_PAGE_HEAD_BYTES",
+           "nvfp4kv_cache_bytes", "nvfp4kv_quantize_append",
+           "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
            "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
            "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
            "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant"]

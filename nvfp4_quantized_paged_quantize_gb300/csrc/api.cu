@@ -48,10 +48,7 @@ int check_cache(const nvfp4kv_cache* c) {
   // row indices (page * heads + head) * page_size stay below 2^31
   if (c->num_pages * (int64_t)c->num_kv_heads * kPageSize >= (int64_t(1) << 31))
     return NVFP4KV_ERR_UNSUPPORTED;
-  if (!c->k_data || !c->v_data || !c->k_scale || !c->v_scale) return NVFP4KV_ERR_INVALID_ARGUMENT;
-  if (!aligned(c->k_data, 16) || !aligned(c->v_data, 16) || !aligned(c->k_scale, 16) ||
-      !aligned(c->v_scale, 16))
-    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (!c->pages || !aligned(c->pages, 16)) return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (!positive_finite(c->k_global_scale) || !positive_finite(c->v_global_scale))
     return NVFP4KV_ERR_INVALID_ARGUMENT;
   return NVFP4KV_OK;
@@ -71,13 +68,14 @@ int cuda_status(cudaError_t e) {
 extern "C" {
 
 int nvfp4kv_cache_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
-                        size_t* data_bytes, size_t* scale_bytes) {
-  if (data_bytes == nullptr || scale_bytes == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;
+                        size_t* pool_bytes) {
+  if (pool_bytes == nullptr) return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (num_pages <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || head_dim % 16 != 0)
     return NVFP4KV_ERR_INVALID_ARGUMENT;
-  const int64_t rows = num_pages * num_kv_heads * (int64_t)page_size;
-  *data_bytes = (size_t)(rows * (head_dim / 2));
-  *scale_bytes = (size_t)(rows * (head_dim / 16));
+  // rows of K (and of V), each head_dim / 2 data bytes and head_dim / 16 scale bytes
+  const int64_t row_bytes = 2 * (int64_t)(head_dim / 2 + head_dim / 16);
+  if (num_pages > INT64_MAX / num_kv_heads / page_size / row_bytes) return NVFP4KV_ERR_UNSUPPORTED;
+  *pool_bytes = (size_t)(num_pages * num_kv_heads * (int64_t)page_size * row_bytes);
   return NVFP4KV_OK;
 }
 
@@ -148,8 +146,15 @@ int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int
   int nsm = 0;
   int st = current_num_sms(&nsm);
   if (st != NVFP4KV_OK) return st;
-  *bytes = nvfp4kv::decode_workspace_bytes(nvfp4kv::decode_num_ctas(nsm), batch, cache->num_kv_heads);
+  *bytes = nvfp4kv::decode_workspace_bytes(nsm, batch, cache->num_kv_heads);
   return NVFP4KV_OK;
+}
+
+size_t nvfp4kv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t max_seq_len, int32_t num_sms) {
+  (void)max_seq_len;  // the split is over pages of all sequences together: lengths do not size it
+  if (batch < 0 || num_q_heads <= 0 || num_sms <= 0) return 0;
+  // the KV-head count divides num_q_heads (num_q_heads = G * num_kv_heads)
+  return nvfp4kv::decode_workspace_bound(num_sms, batch, num_q_heads);
 }
 
 // Host checks of decode arguments (nothing is enqueued); *nsm gets the
@@ -175,8 +180,7 @@ static int check_decode(const nvfp4kv_cache* cache, const void* q, float* out, c
     return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
   if ((st = current_num_sms(nsm)) != NVFP4KV_OK) return st;
-  const size_t need = nvfp4kv::decode_workspace_bytes(nvfp4kv::decode_num_ctas(*nsm), batch,
-                                                      cache->num_kv_heads);
+  const size_t need = nvfp4kv::decode_workspace_bytes(*nsm, batch, cache->num_kv_heads);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return NVFP4KV_ERR_WORKSPACE;
   return NVFP4KV_OK;
 }

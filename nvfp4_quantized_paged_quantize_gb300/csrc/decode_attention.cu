@@ -9,9 +9,10 @@
 // whose sizes differ by at most one, one per CTA, and each CTA range into kNW
 // such ranges, one per warp.
 // A warp streams its pages through a private ring of kStages shared-memory
-// stages (K data 1 KiB, V data 1 KiB, K and V scales 128 B each per page and
-// head) that all 32 lanes fill with 16-byte cp.async copies, completion
-// counted on one mbarrier per stage.  For each page it
+// stages.  A page-head is 2304 contiguous bytes of the pool (K data, K scales,
+// V data, V scales); all 32 lanes copy it into a stage as it is, in 16-byte
+// cp.async pieces, completion counted on one mbarrier per stage.  For each
+// page it
 //   1. converts K's E2M1 pairs to f16x2 with cvt.rn.f16x2.e2m1x2, multiplies
 //      by the E4M3 block scale (exact in f16), and computes S^T = Khat q^T for
 //      the 16 tokens x G query heads with mma.sync m16n8k16 (f16 in, f32 acc);
@@ -60,12 +61,13 @@ constexpr int kCtasPerSm = NVFP4KV_DECODE_CTAS_PER_SM; // resident CTAs per SM t
 constexpr int kGMax = 8;        // query heads per KV head (one MMA n-tile)
 constexpr float kLazy = 8.0f;   // running-max slack (log2 units): P <= 2^8 in f16
 
-// stage layout: K data | V data | K scales | V scales
-constexpr int kOffKD = 0;
-constexpr int kOffVD = kPageDataBytes;
-constexpr int kOffKS = 2 * kPageDataBytes;
-constexpr int kOffVS = 2 * kPageDataBytes + kPageScaleBytes;
-constexpr int kStageBytes = 2 * kPageDataBytes + 2 * kPageScaleBytes;  // 2304
+// stage layout: the page-head as stored (K data | K scales | V data | V scales)
+constexpr int kOffKD = kOffKData;
+constexpr int kOffVD = kOffVData;
+constexpr int kOffKS = kOffKScale;
+constexpr int kOffVS = kOffVScale;
+constexpr int kStageBytes = kPageHeadBytes;  // 2304
+constexpr int kCopyChunks = kStageBytes / 16;  // 144 16-byte pieces per page-head
 
 // a (partial) result record: O[kGMax][128] unnormalised, m[kGMax] (base 2), l[kGMax]
 constexpr int kRecFloats = kGMax * kHeadDim + 2 * kGMax;
@@ -77,10 +79,7 @@ constexpr int kBarBytes = kNW * kStages * 8;
 constexpr int kSmemBytes = kRingBytes + kBarBytes;
 
 struct DecodeParams {
-  const uint8_t* k_data;
-  const uint8_t* v_data;
-  const uint8_t* k_scale;
-  const uint8_t* v_scale;
+  const uint8_t* pages;  // [num_pages][hkv][kPageHeadBytes]
   int32_t num_pages;
   int32_t hkv;
   const uint16_t* q;
@@ -258,25 +257,21 @@ __device__ __forceinline__ int item_row(const ItemMap& cur, const ItemMap& nxt, 
   return r;
 }
 
-// cp.async staging: each lane copies fixed 16-byte chunks of every page-head
-// (two of K's data, two of V's, and lanes 0-15 one scale chunk), then arrives
+// cp.async staging: lane l copies the 16-byte pieces l, l + 32, ... of the
+// page-head (lanes 0-15 five of the 144, the others four), then arrives
 // (no-increment) on the stage's mbarrier, which expects 32 arrivals.  The
-// lane's source bases and shared-memory offsets are set up once.
+// lane's source base and shared-memory offset are set up once.
 struct LaneCopy {
-  const uint8_t* kd;  // k_data + 16 * lane
-  const uint8_t* vd;  // v_data + 16 * lane
-  const uint8_t* sc;  // (lanes 0-7: k_scale, 8-15: v_scale) + 16 * (lane % 8)
-  uint32_t off;       // 16 * lane
-  uint32_t sc_off;    // stage offset of the lane's scale chunk
+  const uint8_t* src;  // pages + 16 * lane
+  uint32_t off;        // 16 * lane
+  bool fifth;          // lanes 0-15: a fifth piece at 16 * (lane + 128)
 };
 
 __device__ __forceinline__ LaneCopy lane_copy(const DecodeParams& p, int lane) {
   LaneCopy c;
-  c.kd = p.k_data + 16 * lane;
-  c.vd = p.v_data + 16 * lane;
-  c.sc = (lane < 8 ? p.k_scale : p.v_scale) + 16 * (lane & 7);
+  c.src = p.pages + 16 * lane;
   c.off = 16u * lane;
-  c.sc_off = (lane < 8 ? kOffKS : kOffVS) + 16u * (lane & 7);
+  c.fifth = lane + 128 < kCopyChunks;
   return c;
 }
 
@@ -287,13 +282,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void issue_page_cpasync(const LaneCopy& c, int row, uint32_t st, uint32_t bar,
                                                    int lane) {
   if (row >= 0) {
-    const size_t data_off = (size_t)row * kPageDataBytes;
-    const size_t scale_off = (size_t)row * kPageScaleBytes;
-    cp_async16(st + kOffKD + c.off, c.kd + data_off);
-    cp_async16(st + kOffKD + 512 + c.off, c.kd + data_off + 512);
-    cp_async16(st + kOffVD + c.off, c.vd + data_off);
-    cp_async16(st + kOffVD + 512 + c.off, c.vd + data_off + 512);
-    if (lane < 16) cp_async16(st + c.sc_off, c.sc + scale_off);
+    const uint8_t* src = c.src + (size_t)row * kPageHeadBytes;
+    const uint32_t dst = st + c.off;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) cp_async16(dst + 512 * k, src + 512 * k);
+    if (c.fifth) cp_async16(dst + 2048, src + 2048);
   }
   // fires once all of this lane's earlier copies have landed (also for an
   // invalid page, which copies nothing): a stage's barrier therefore covers
@@ -712,6 +705,12 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   const uint32_t wbar = smem_u32(bars + warp * kStages);
   const long long gwarp = (long long)blockIdx.x * kNW + warp;  // global warp index
 
+  if (n == 0 && lane < kGMax) {
+    // a warp with no items lies between the pieces of a cut pair when a CTA's
+    // range is shorter than kNW: its first record is marked empty (m = -inf),
+    // which the combine skips
+    p.part[2 * gwarp * kRecFloats + kOffM + lane] = -INFINITY;
+  }
   if (n > 0) {
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) mbar_init(wbar + 8 * s, 32);
@@ -913,7 +912,9 @@ __global__ void __launch_bounds__(kCombineMaxGroups * 32) combine_kernel(const D
   for (int c = grp; c < cnt; c += groups) {
     const long long ri = c == 0 ? (long long)h.x : 2LL * (gw_first + c);
     const float* r = p.part + ri * kRecFloats;
-    const float m = __ldcg(r + kOffM + head), l = __ldcg(r + kOffL + head);
+    const float m = __ldcg(r + kOffM + head);
+    if (m == -INFINITY) continue;  // a warp with no items (or no valid page): nothing to merge
+    const float l = __ldcg(r + kOffL + head);
     const float4 v = __ldcg(reinterpret_cast<const float4*>(r + head * kHeadDim) + col);
     online_merge(M, L, acc, m, l, v);
   }
@@ -932,29 +933,30 @@ __global__ void __launch_bounds__(kCombineMaxGroups * 32) combine_kernel(const D
 
 int decode_num_ctas(int num_sms) { return num_sms * kCtasPerSm; }
 
-size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads) {
-  size_t rec = 2 * (size_t)num_ctas * kNW * kRecFloats * sizeof(float);
+size_t decode_workspace_bytes(int num_sms, int32_t batch, int32_t num_kv_heads) {
+  size_t rec = 2 * (size_t)decode_num_ctas(num_sms) * kNW * kRecFloats * sizeof(float);
   rec = (rec + 255) / 256 * 256;
   return rec + (size_t)batch * (size_t)num_kv_heads * sizeof(int2);
+}
+
+size_t decode_workspace_bound(int num_sms, int32_t batch, int32_t num_q_heads) {
+  // the headers grow with the KV-head count, which is at most num_q_heads
+  return decode_workspace_bytes(num_sms, batch, num_q_heads);
 }
 
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
                           int32_t max_pages, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                           float softmax_scale, void* workspace, int32_t* device_status, int num_sms,
                           cudaStream_t stream, bool after_kernel) {
-  static bool attr_set = false;  // the attribute is per function, for every device
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory limit is an attribute of the function on each device
+  static PerDeviceOnce attr_once;
+  const cudaError_t ae = attr_once.run([] {
+    return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (ae != cudaSuccess) return ae;
   const int num_ctas = decode_num_ctas(num_sms);
   DecodeParams p;
-  p.k_data = c.k_data;
-  p.v_data = c.v_data;
-  p.k_scale = c.k_scale;
-  p.v_scale = c.v_scale;
+  p.pages = c.pages;
   p.num_pages = (int32_t)c.num_pages;
   p.hkv = c.num_kv_heads;
   p.q = q;

@@ -22,10 +22,7 @@ namespace nvfp4kv {
 namespace {
 
 struct DequantParams {
-  const uint8_t* k_data;
-  const uint8_t* v_data;
-  const uint8_t* k_scale;
-  const uint8_t* v_scale;
+  const uint8_t* pages;  // [num_pages][hkv][kPageHeadBytes]
   int64_t num_pages;
   int32_t hkv;
   const int32_t* page_table;
@@ -123,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(De
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tensor = warp & 1;  // 0: K, 1: V
   const int r = lane >> 1, half = lane & 1;
-  const uint8_t* data = tensor ? p.v_data : p.k_data;
-  const uint8_t* scale = tensor ? p.v_scale : p.k_scale;
+  const int off_data = tensor ? kOffVData : kOffKData;  // within a page-head
+  const int off_scale = tensor ? kOffVScale : kOffKScale;
   uint8_t* ws = tensor ? p.ws_v : p.ws_k;
   const float g = tensor ? p.gv : p.gk, sws = tensor ? p.sv : p.sk, rs = tensor ? p.rsv : p.rsk;
   const bool fast = tensor ? p.sv_fast : p.sk_fast;
@@ -144,10 +141,10 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(De
     }
     if (pg * kPage >= L) continue;  // a page past this prefix
     const bool page_ok = page >= 0 && page < p.num_pages;
-    const int64_t src_row = ((int64_t)(page_ok ? page : 0) * p.hkv + h) * kPage + r;
-    const uint4* src = reinterpret_cast<const uint4*>(data + src_row * kRowBytes) + 2 * half;
+    const uint8_t* phd = p.pages + ((int64_t)(page_ok ? page : 0) * p.hkv + h) * kPageHeadBytes;
+    const uint4* src = reinterpret_cast<const uint4*>(phd + off_data + r * kRowBytes) + 2 * half;
     const uint4 d0 = __ldg(src), d1 = __ldg(src + 1);  // blocks 4 half .. 4 half + 3
-    const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(scale + src_row * kRowScales) + half);
+    const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(phd + off_scale + r * kRowScales) + half);
     const int t = pg * kPage + r;   // this lane's token of the prefix
     const int64_t orow = base + t;  // its workspace row
     const bool live = t < L && orow >= 0 && orow < p.total_rows;
@@ -188,10 +185,7 @@ cudaError_t launch_dequant_fp8(const nvfp4kv_cache& c, const int32_t* page_table
                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
                                uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream) {
   DequantParams p;
-  p.k_data = c.k_data;
-  p.v_data = c.v_data;
-  p.k_scale = c.k_scale;
-  p.v_scale = c.v_scale;
+  p.pages = c.pages;
   p.num_pages = c.num_pages;
   p.hkv = c.num_kv_heads;
   p.page_table = page_table;

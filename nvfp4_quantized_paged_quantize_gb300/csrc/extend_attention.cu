@@ -519,9 +519,11 @@ cudaError_t launch_extend_attention(const uint16_t* q, const int64_t* cu_q, int3
   p.out_scale = v_ws_scale;
   p.out = out;
   p.status = device_status;
-  // the attribute belongs to the function (every device); set once, thread-safely
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(extend_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the shared-memory limit is an attribute of the function on each device
+  static PerDeviceOnce attr_once;
+  const cudaError_t attr = attr_once.run([] {
+    return cudaFuncSetAttribute(extend_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
   if (attr != cudaSuccess) return attr;
   const int64_t tiles = ((int64_t)max_q_len * p.group + kTileM - 1) / kTileM;
   const dim3 grid((unsigned)tiles, (unsigned)batch, (unsigned)num_kv_heads);

@@ -23,6 +23,22 @@ constexpr int kPageDataBytes = kPage * kRowBytes;      // 1024: one head's page 
 constexpr int kPageScaleBytes = kPage * kRowScales;    // 128: one head's page of scales
 constexpr int kDevErrTimeout = 8;                      // a bounded wait gave up
 
+// One page-head (16 tokens of one KV head) of the pool: K data, K scales,
+// V data, V scales, contiguous; the page-heads of a page follow one another.
+constexpr int kOffKData = 0;
+constexpr int kOffKScale = kPageDataBytes;                        // 1024
+constexpr int kOffVData = kPageDataBytes + kPageScaleBytes;       // 1152
+constexpr int kOffVScale = 2 * kPageDataBytes + kPageScaleBytes;  // 2176
+constexpr int kPageHeadBytes = 2 * (kPageDataBytes + kPageScaleBytes);  // 2304
+static_assert(kPageHeadBytes == NVFP4KV_PAGE_HEAD_BYTES, "page-head size");
+// The MXFP4 variant's page-head: 4 E8M0 scale bytes per row.
+constexpr int kMxRowScales = kHeadDim / 32;                       // 4
+constexpr int kMxOffKScale = kPageDataBytes;                      // 1024
+constexpr int kMxOffVData = kPageDataBytes + kPage * kMxRowScales;  // 1088
+constexpr int kMxOffVScale = 2 * kPageDataBytes + kPage * kMxRowScales;  // 2112
+constexpr int kMxPageHeadBytes = 2 * (kPageDataBytes + kPage * kMxRowScales);  // 2176
+static_assert(kMxPageHeadBytes == NVFP4KV_MXFP4_PAGE_HEAD_BYTES, "MXFP4 page-head size");
+
 // ---------------------------------------------------------------------------
 // E2M1 / E4M3 conversions (round to nearest even, saturating, as the
 // satfinite cvt forms do).

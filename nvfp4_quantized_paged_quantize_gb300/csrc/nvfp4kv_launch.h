@@ -3,11 +3,42 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "nvfp4kv.h"
 
 namespace nvfp4kv {
+
+// A set-up step that must run once on every device before a kernel is
+// launched there (a function attribute such as the dynamic shared-memory
+// limit belongs to the function as loaded on the current device).  run()
+// calls set_up() with the device current the first time that device is seen
+// and caches the success; concurrent first calls from several host threads
+// serialise on the mutex.  Devices past kMaxDevices run the set-up every time.
+class PerDeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(F set_up) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return set_up();
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = set_up();
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::atomic<bool> done_[kMaxDevices] = {};
+  std::mutex mu_;
+};
 
 cudaError_t launch_quantize_append(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
                                    const int64_t* slot_mapping, int64_t num_tokens,
@@ -49,9 +80,13 @@ cudaError_t launch_tensor_amax(const uint16_t* x, int64_t n, float* amax, bool a
                                cudaStream_t stream);
 
 // Split-K decode: how many CTAs the decode launches on a device with num_sms
-// SMs, and the workspace layout that goes with it.
+// SMs, and the workspace it needs there (two split records per warp of the
+// launch, a merge header per (sequence, KV head)).
 int decode_num_ctas(int num_sms);
-size_t decode_workspace_bytes(int num_ctas, int32_t batch, int32_t num_kv_heads);
+size_t decode_workspace_bytes(int num_sms, int32_t batch, int32_t num_kv_heads);
+// An upper bound of decode_workspace_bytes over every KV-head count that
+// divides num_q_heads.
+size_t decode_workspace_bound(int num_sms, int32_t batch, int32_t num_q_heads);
 
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,

@@ -11,7 +11,8 @@
 //   den  = E4M3val(sb) * g
 //   code = E2M1(x / den)                 (correctly rounded quotient, RNE, saturating)
 // A block with den == 0 stores signed zeros.  The row's 64 data bytes and 8
-// scale bytes go to slot slot_mapping[token].  HBM-bound: 2 B read and 9/16 B
+// scale bytes go to slot slot_mapping[token]: row slot % 16 of the K (or V)
+// part of the page-head (slot / 16, head).  HBM-bound: 2 B read and 9/16 B
 // written per value.
 #include "fp8_quotient.cuh"
 #include "nvfp4kv_device.cuh"
@@ -27,10 +28,7 @@ struct QuantParams {
   int32_t rows;  // num_tokens * num_kv_heads (< 2^31, checked on the host)
   int32_t hkv;
   int64_t capacity;  // num_pages * page_size
-  uint8_t* k_data;
-  uint8_t* v_data;
-  uint8_t* k_scale;
-  uint8_t* v_scale;
+  uint8_t* pages;  // [num_pages][hkv][kPageHeadBytes]
   float gk, gv;
   int32_t* status;
   // FP8 workspace rows written in the same pass (the fused prefill / extend write)
@@ -73,8 +71,8 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
   const int sub = lane & 7;      // block j = sub of the row: values [16 j, 16 j + 16)
   const int which = (lane >> 3) & 1;  // first or second row of the step
   const uint16_t* src = tensor ? p.v : p.k;
-  uint8_t* data = tensor ? p.v_data : p.k_data;
-  uint8_t* scale = tensor ? p.v_scale : p.k_scale;
+  const int off_data = tensor ? kOffVData : kOffKData;    // within a page-head
+  const int off_scale = tensor ? kOffVScale : kOffKScale;
   const float g = tensor ? p.gv : p.gk;
   const float t6 = __fmul_rn(6.0f, g);  // the block amax maps onto E2M1's 6
   const float r6 = __frcp_rn(t6);
@@ -136,7 +134,8 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
       continue;
     }
     const int h = (int)r % p.hkv;
-    const int64_t row = ((cslot >> 4) * p.hkv + h) * kPage + (cslot & (kPage - 1));
+    uint8_t* ph = p.pages + ((cslot >> 4) * p.hkv + h) * kPageHeadBytes;  // the slot's page-head
+    const int rin = (int)(cslot & (kPage - 1));                            // its row there
     float f[16];
     unpack_bf16x8(ca, f);
     unpack_bf16x8(cb, f + 8);
@@ -172,8 +171,8 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
 #pragma unroll
       for (int k = 0; k < 4; ++k) hi |= e2m1x2_from_f32(y[8 + 2 * k], y[8 + 2 * k + 1]) << (8 * k);
     }
-    reinterpret_cast<uint2*>(data + row * kRowBytes)[sub] = make_uint2(lo, hi);
-    scale[row * kRowScales + sub] = (uint8_t)sb;
+    reinterpret_cast<uint2*>(ph + off_data + rin * kRowBytes)[sub] = make_uint2(lo, hi);
+    ph[off_scale + rin * kRowScales + sub] = (uint8_t)sb;
   }
 }
 
@@ -211,10 +210,7 @@ QuantParams cache_params(const nvfp4kv_cache& c, const uint16_t* k, const uint16
   p.rows = (int32_t)(num_tokens * c.num_kv_heads);
   p.hkv = c.num_kv_heads;
   p.capacity = c.num_pages * (int64_t)c.page_size;
-  p.k_data = c.k_data;
-  p.v_data = c.v_data;
-  p.k_scale = c.k_scale;
-  p.v_scale = c.v_scale;
+  p.pages = c.pages;
   p.gk = c.k_global_scale;
   p.gv = c.v_global_scale;
   p.status = device_status;

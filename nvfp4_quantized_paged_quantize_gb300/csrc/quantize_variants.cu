@@ -11,7 +11,8 @@
 //    breaking the memory wall", technical breakdown): blocks of 32 values with
 //    a power-of-two scale, an E8M0 byte e + 127 with e = floor(log2 amax) - 2,
 //    elements E2M1(x * 2^-e); its scale pool holds 4 bytes per row.
-// The data pages are the NVFP4 ones (64 bytes of E2M1 pairs per row).
+// SR and Hadamard write the NVFP4 page-heads; MXFP4 writes its own page-heads
+// (the same 64 data bytes per row, 4 scale bytes per row).
 //
 // Eight lanes own one (token, head) row of K or of V, 16 values each; a warp
 // takes four rows.  Block scales divide exactly (IEEE); these are comparison
@@ -31,10 +32,7 @@ struct VariantParams {
   int64_t rows;  // num_tokens * hkv * 2 (K rows then V rows of each (token, head))
   int32_t hkv;
   int64_t capacity;
-  uint8_t* k_data;
-  uint8_t* v_data;
-  uint8_t* k_scale;
-  uint8_t* v_scale;
+  uint8_t* pages;  // [num_pages][hkv][page-head bytes of the variant's layout]
   float gk, gv;
   int32_t* status;
 };
@@ -177,13 +175,15 @@ __global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParam
     if (sub == 0) flag_error(p.status, NVFP4KV_DEVERR_SLOT);
     return;
   }
-  const int64_t row = ((slot >> 4) * p.hkv + h) * kPage + (slot & (kPage - 1));
-  reinterpret_cast<uint2*>((tensor ? p.v_data : p.k_data) + row * kRowBytes)[sub] = make_uint2(lo, hi);
-  uint8_t* scale = tensor ? p.v_scale : p.k_scale;
+  const int rin = (int)(slot & (kPage - 1));  // the slot's row in its page-head
   if constexpr (kVariant == NVFP4KV_VARIANT_MXFP4) {
-    if ((sub & 1) == 0) scale[row * (kHeadDim / 32) + (sub >> 1)] = (uint8_t)sbyte;
+    uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * kMxPageHeadBytes;
+    reinterpret_cast<uint2*>(ph + (tensor ? kMxOffVData : kOffKData) + rin * kRowBytes)[sub] = make_uint2(lo, hi);
+    if ((sub & 1) == 0) ph[(tensor ? kMxOffVScale : kMxOffKScale) + rin * kMxRowScales + (sub >> 1)] = (uint8_t)sbyte;
   } else {
-    scale[row * kRowScales + sub] = (uint8_t)sbyte;
+    uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * kPageHeadBytes;
+    reinterpret_cast<uint2*>(ph + (tensor ? kOffVData : kOffKData) + rin * kRowBytes)[sub] = make_uint2(lo, hi);
+    ph[(tensor ? kOffVScale : kOffKScale) + rin * kRowScales + sub] = (uint8_t)sbyte;
   }
 }
 
@@ -201,10 +201,7 @@ cudaError_t launch_quantize_variant(int variant, const nvfp4kv_cache& c, const u
   p.rows = num_tokens * c.num_kv_heads * 2;
   p.hkv = c.num_kv_heads;
   p.capacity = c.num_pages * (int64_t)c.page_size;
-  p.k_data = c.k_data;
-  p.v_data = c.v_data;
-  p.k_scale = c.k_scale;
-  p.v_scale = c.v_scale;
+  p.pages = c.pages;
   p.gk = c.k_global_scale;
   p.gv = c.v_global_scale;
   p.status = device_status;

@@ -50,17 +50,49 @@ def test_status_strings(lib):
 
 
 def test_cache_bytes_nine_sixteenths(lib):
-    d, s = kv.nvfp4kv_cache_bytes(10, 8)
-    values = 10 * 8 * 16 * 128
-    assert d == values // 2 and s == values // 16
-    assert (d + s) / values == 9 / 16
+    n = kv.nvfp4kv_cache_bytes(10, 8)
+    values = 10 * 8 * 16 * 128                    # of K, and as many of V
+    assert n == 2 * values * 9 // 16
+    assert n == 10 * 8 * kv.NVFP4KV_PAGE_HEAD_BYTES  # one 2304-byte page-head per (page, KV head)
     with pytest.raises(kv.Nvfp4kvError):
         kv.nvfp4kv_cache_bytes(0, 8)
+    with pytest.raises(kv.Nvfp4kvError):
+        kv.nvfp4kv_cache_bytes(1 << 62, 8)        # overflows size_t arithmetic
+
+
+def test_page_head_views_cover_the_pool_once(lib):
+    import torch
+
+    for mx in (False, True):
+        c = kv.Cache.empty(3, 2, device="cpu", zero=True, mxfp4=mx)
+        for i, part in enumerate((c.k_data, c.k_scale, c.v_data, c.v_scale)):
+            part.fill_(i + 1)
+        # every byte of the pool belongs to exactly one of the four views
+        counts = torch.bincount(c.pages.reshape(-1).long(), minlength=5)
+        sc = 4 if mx else 8
+        assert counts[0] == 0
+        assert counts[1] == counts[3] == 3 * 2 * 16 * 64
+        assert counts[2] == counts[4] == 3 * 2 * 16 * sc
+        # the order within a page-head: K data, K scales, V data, V scales
+        ph = c.pages[1, 1].tolist()
+        assert ph == [1] * 1024 + [2] * 16 * sc + [3] * 1024 + [4] * 16 * sc
+
+
+def test_decode_workspace_bytes_from_the_batch_shape(lib):
+    # the call the scope table names: sized from (batch, q heads, max length, SMs)
+    f = kv.nvfp4kv_decode_workspace_bytes
+    assert f(-1, 8, 100, 152) == 0 and f(4, 0, 100, 152) == 0 and f(4, 8, 100, 0) == 0
+    a = f(32, 64, 8193, 152)
+    assert a > 0
+    assert f(32, 64, 131072, 152) == a           # no length sizes the split-K scratch
+    assert f(33, 64, 8193, 152) > a              # one merge header per (sequence, head)
+    assert f(32, 64, 8193, 160) > a              # split records per CTA of the launch
+    assert f(0, 64, 0, 152) > 0                  # the records of the launch even for no sequences
 
 
 def _fake_cache(**kw):
     # aligned fake addresses: these calls are rejected before any device access
-    c = kv.Cache(0x10000, 0x20000, 0x30000, 0x40000, 4, 2)
+    c = kv.Cache(0x10000, 4, 2)
     for k, v in kw.items():
         setattr(c, k, v)
     return c
@@ -83,7 +115,7 @@ def test_host_validation_codes(lib):
     assert lib.nvfp4kv_decode_attention(P(bad), 16, 16, 4, 1, 4, 1, 2, 0.1, 256, 1 << 20, None,
                                         None) == kv.NVFP4KV_ERR_UNSUPPORTED
     # misaligned pool, bad global scale
-    bad = _fake_cache(k_data=0x10001).c_struct()
+    bad = _fake_cache(pages=0x10001).c_struct()
     assert lib.nvfp4kv_quantize_append(P(bad), 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT
     bad = _fake_cache(k_global_scale=float("nan")).c_struct()
     assert lib.nvfp4kv_quantize_append(P(bad), 16, 16, 8, 1, None, None) == kv.NVFP4KV_ERR_INVALID_ARGUMENT

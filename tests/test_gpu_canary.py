@@ -36,9 +36,10 @@ class Guarded:
 
 
 def _guarded_cache(pages, H, scale_bytes=8, gk=1.0, gv=1.0):
-    pools = [Guarded((pages, H, 16, 64), torch.uint8), Guarded((pages, H, 16, 64), torch.uint8),
-             Guarded((pages, H, 16, scale_bytes), torch.uint8), Guarded((pages, H, 16, scale_bytes), torch.uint8)]
-    return kv.Cache(*(p.t for p in pools), pages, H, gk, gv), pools
+    mx = scale_bytes == 4
+    phb = kv.NVFP4KV_MXFP4_PAGE_HEAD_BYTES if mx else kv.NVFP4KV_PAGE_HEAD_BYTES
+    pool = Guarded((pages, H, phb), torch.uint8)
+    return kv.Cache(pool.t, pages, H, gk, gv, mxfp4=mx), [pool]
 
 
 def test_decode_paths_stay_inside_their_outputs(cuda_lib):

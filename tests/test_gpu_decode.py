@@ -220,3 +220,11 @@ def test_fused_append_decode_matches_two_calls(cuda_lib, index, scale):
     assert torch.equal(out_a, out_b)
     for x, y in zip(pool_host(a), pool_host(b)):
         np.testing.assert_array_equal(x, y)
+
+
+def test_workspace_bytes_from_the_batch_shape_covers_the_call(cuda_lib):
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, hq, hkv in ((32, 64, 8), (256, 32, 8), (2, 8, 2), (7, 24, 8)):
+        cache = kv.Cache.empty(4, hkv)
+        need = kv.nvfp4kv_decode_workspace_size(cache, B, hq)
+        assert kv.nvfp4kv_decode_workspace_bytes(B, hq, 8193, nsm) >= need

@@ -31,9 +31,8 @@ def test_variant_quantize_bit_exact(cuda_lib, variant, gk, gv):
     slots[9] = pages * 16 + 1                               # outside the pool
     rk = inputs.rounding_bytes(2, n * H * 128).reshape(n, H, 128)
     rv = inputs.rounding_bytes(3, n * H * 128).reshape(n, H, 128)
-    nsc = 4 if variant == kv.NVFP4KV_VARIANT_MXFP4 else 8
-    mk = lambda c: torch.zeros((pages, H, 16, c), dtype=torch.uint8, device="cuda")
-    cache = kv.Cache(mk(64), mk(64), mk(nsc), mk(nsc), pages, H, gk, gv)
+    cache = kv.Cache.empty(pages, H, k_global_scale=gk, v_global_scale=gv, zero=True,
+                           mxfp4=variant == kv.NVFP4KV_VARIANT_MXFP4)
     st = status_word()
     kv.nvfp4kv_quantize_append_variant(variant, cache, bf16_dev(k), bf16_dev(v), dev(slots), dev(rk), dev(rv),
                                        device_status=st)

@@ -2,12 +2,16 @@
 
 Some callers cannot hand the decode a device workspace: they run inside an
 allocator hook, or they are plug-ins whose host runtime owns all device memory.
-For them the library keeps a fixed 16 MiB scratch array in its device image
-and nvfp4kv_decode_attention_static uses it instead.  These tests call the new
-entry point through the C ABI and compare it with the ordinary entry point
-(caller workspace) on the same cache, twice in a row, since the second call
-finds the first call's leftovers in the shared scratch.  This file is named to
-run last: the scratch is process-wide state.
+For them the library keeps a fixed 32 MiB scratch array in its device image
+and nvfp4kv_decode_attention_static uses it instead.
+
+The static entry point runs the same kernels, on the same split of the work,
+as nvfp4kv_decode_attention with a caller workspace, so its output must equal
+that call's bit for bit; one call is also checked against the oracle.  Between
+the two calls on the target workload the static entry point decodes another
+workload, whose (sequence, KV head) pairs are cut at other places, so the
+second call finds the scratch full of someone else's split records and
+headers.  This file is named to run last: the scratch is process-wide state.
 """
 import ctypes
 
@@ -15,9 +19,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
-from gpu_util import ATTN_TOL, bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, status_word
+from gpu_util import (ATTN_TOL, bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle,
+                      status_word)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,8 +35,27 @@ def _static(lib, cache, q_dev, out, pt_dev, lens_dev, B, Hq, scale, status):
         lens_dev.data_ptr(), B, Hq, float(scale), status.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
+def _static_decode(lib, wl, cache, q_bits):
+    """One static-entry decode of workload wl; returns the fp32 output (device)."""
+    out = torch.full((wl.batch, wl.num_q_heads, 128), float("nan"), dtype=torch.float32, device="cuda")
+    status = status_word()
+    rc = _static(lib, cache, bf16_dev(q_bits), out, dev(wl.page_table), dev(wl.seq_lens.astype(np.int32)),
+                 wl.batch, wl.num_q_heads, wl.softmax_scale, status)
+    assert rc == kv.NVFP4KV_OK, kv.nvfp4kv_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+def _other_workload():
+    """Ragged lengths, another GQA shape: cut points unlike the target's."""
+    rng = np.random.default_rng(77)
+    lens = np.array(list(rng.integers(1, 3000, 37)) + [9000], np.int64)
+    return inputs.DecodeWorkload("custom", 77, lens, True, 16, 4, inputs.KVDist("normal", 1.0), pool_factor=1.1)
+
+
 @pytest.mark.parametrize("index,scale", [(1, 1.0), (4, 1 / 16), (2, 1 / 8)])
-def test_static_scratch_matches_workspace_decode_twice(cuda_lib, index, scale):
+def test_static_scratch_equals_workspace_decode_bit_for_bit(cuda_lib, index, scale):
     lib = kv.load()
     wl = inputs.decode_config(index, scale)
     prompts = wl.all_prompt_kv()
@@ -38,25 +63,32 @@ def test_static_scratch_matches_workspace_decode_twice(cuda_lib, index, scale):
     cache = fill_workload_gpu(wl, prompts, new)
     q = wl.q()
     ref, _ = decode_gpu(wl, cache, q)                     # ordinary entry point, caller workspace
-    ref = ref.cpu().numpy().astype(np.float64)
-    q_dev, pt_dev, lens_dev = bf16_dev(q), dev(wl.page_table), dev(wl.seq_lens.astype(np.int32))
-    for call in range(2):
-        out = torch.full((wl.batch, wl.num_q_heads, 128), float("nan"), dtype=torch.float32, device="cuda")
-        status = status_word()
-        rc = _static(lib, cache, q_dev, out, pt_dev, lens_dev, wl.batch, wl.num_q_heads, wl.softmax_scale,
-                     status)
-        assert rc == kv.NVFP4KV_OK, kv.nvfp4kv_status_string(rc)
-        torch.cuda.synchronize()
-        assert int(status.item()) == 0
-        check_rows(out.cpu().numpy(), ref, tol=ATTN_TOL)
+    torch.cuda.synchronize()
+
+    first = _static_decode(lib, wl, cache, q)
+    assert torch.equal(first, ref)
+    o = fill_workload_oracle(wl, prompts, new)
+    exp, rs = oracle.decode_attention(o, q, wl.page_table, wl.seq_lens, wl.softmax_scale)
+    assert rs == 0
+    check_rows(first.cpu().numpy(), exp, tol=ATTN_TOL)
+
+    other = _other_workload()
+    oc = fill_workload_gpu(other, other.all_prompt_kv(), other.new_kv())
+    oq = other.q()
+    other_out = _static_decode(lib, other, oc, oq)
+    other_ref, _ = decode_gpu(other, oc, oq)
+    assert torch.equal(other_out, other_ref)
+
+    second = _static_decode(lib, wl, cache, q)
+    assert torch.equal(second, ref)
 
 
 def test_static_scratch_rejects_a_batch_that_does_not_fit(cuda_lib):
     lib = kv.load()
     cache = kv.Cache.empty(4, 8, zero=True)
     Hq = 8
-    B = 4096                         # grow the batch until its workspace exceeds the 16 MiB scratch
-    while kv.nvfp4kv_decode_workspace_size(cache, B, Hq) <= (16 << 20):
+    B = 4096                         # grow the batch until its workspace exceeds the 32 MiB scratch
+    while kv.nvfp4kv_decode_workspace_size(cache, B, Hq) <= (32 << 20):
         B *= 2
     q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((B, Hq, 128), dtype=torch.float32, device="cuda")
