@@ -258,6 +258,25 @@ class DecodeBench:
         return 2 if self.wl.append else 1
 
 
+def stream_probe_lines(torch, kv, b, steps, warmup, flush, hbm_peak, decode_ms):
+    """Time the library's streaming probe over a decode bench's cache: the same
+    page-heads the decode reads, with no attention math, in the decode's own
+    pattern and as whole pages by bulk copy.  The decode's time is set beside."""
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv_bytes = b.wl.kv_tokens() * b.wl.num_kv_heads * 144
+    out = {"kv_bytes": kv_bytes, "decode_kernel_ms": decode_ms,
+           "decode_gbs_kv_only": kv_bytes / (decode_ms / 1e3) / 1e9}
+    for name, mode in (("decode_pattern", kv.NVFP4KV_PROBE_DECODE_PATTERN),
+                       ("whole_pages_bulk", kv.NVFP4KV_PROBE_WHOLE_PAGES)):
+        ms, _ = time_steps(torch, steps, warmup,
+                           lambda ev=None, mode=mode: kv.nvfp4kv_stream_probe(b.cache, b.pt, b.lens, sink, mode), flush)
+        t = float(np.mean(ms))
+        gbs = kv_bytes / (t / 1e3) / 1e9
+        out[name] = {"kernel_ms": t, "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak,
+                     "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS}
+    return out
+
+
 def make_l2_flush(torch):
     """Flush L2 between timed steps: write one buffer larger than L2, then read
     another.  The write evicts every line the step could reuse; the read then
@@ -373,6 +392,10 @@ def gpu_arm(args):
     e2e_ms, _ = time_steps(torch, e2e_steps, args.warmup, e2e_step, flush)
     e2e_total = world_max(torch, float(sum(e2e_ms)), "cuda")
     e2e_value = job_throughput(world, kv_tokens, e2e_steps, e2e_total)
+    probe = None
+    if not args.skip_secondary:
+        probe = stream_probe_lines(torch, kv, bench, max(3, min(args.steps, 200)), args.warmup, flush, hbm_peak,
+                                   dec_avg_ms)
     del bench
 
     line = {
@@ -416,6 +439,7 @@ def gpu_arm(args):
     }
     if not args.skip_secondary:
         line["secondary"] = secondary(torch, kv, args, flush, hbm_peak)
+        line["secondary"]["stream_probe_b32_ctx8k"] = probe
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     if rank == 0:
@@ -435,6 +459,7 @@ def secondary(torch, kv, args, flush, hbm_peak):
     gbs = wl.algorithmic_bytes() / (t / 1e3) / 1e9
     out["decode_b4_ctx128k"] = {"kernel_ms": t, "kv_tokens_per_s": wl.kv_tokens() / (t / 1e3), "hbm_gbs": gbs,
                                 "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS, "frac_of_measured_peak": gbs / hbm_peak}
+    out["stream_probe_b4_ctx128k"] = stream_probe_lines(torch, kv, b, steps, args.warmup, flush, hbm_peak, t)
     del b
     torch.cuda.empty_cache()
     # ragged continuous batching: 256 sequences, log-uniform lengths in [512,
@@ -680,6 +705,11 @@ def only_arm(args):
     elif args.only in ("decode8k", "decode128k", "ragged"):
         b = DecodeBench(torch, kv, inputs.decode_config({"decode8k": 2, "decode128k": 3, "ragged": 4}[args.only]))
         time_steps(torch, args.steps, args.warmup, lambda ev=None: (b.append(), b.decode()), flush)
+    elif args.only == "stream-probe":
+        b = DecodeBench(torch, kv, inputs.decode_config(2))
+        peak = float(measured_peaks()[0]["hbm_gbs"])
+        print(json.dumps({"stream_probe_b32_ctx8k": stream_probe_lines(torch, kv, b, args.steps, args.warmup, flush,
+                                                                        peak, float("nan"))}))
     else:
         ew = inputs.extend_config(num_layers=1)
         cache = kv.Cache.empty(ew.num_pages, ew.num_kv_heads, zero=True)
@@ -717,7 +747,7 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--cpu-total-s", type=float, default=90.0, help="reference arm: total oracle seconds")
-    ap.add_argument("--only", choices=["decode8k", "decode128k", "ragged", "extend", "calibrate"],
+    ap.add_argument("--only", choices=["decode8k", "decode128k", "ragged", "extend", "calibrate", "stream-probe"],
                     help="run just one workload's kernels (profiler command lines); no JSON metric line")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -396,6 +396,26 @@ int nvfp4kv_tensor_amax(const void* x_bf16, int64_t n, float* amax, int accumula
                         nvfp4kv_stream_t stream);
 int nvfp4kv_calibrated_global_scale(float amax, float* g);
 
+/* Streaming probe (a measurement aid, not part of the method): reads every
+ * cached page-head of a decode batch once, with no attention math, so that the
+ * decode's time can be set against the time its bytes take to stream alone
+ * ("nvfp4-kv-cache-memory-wall", section 3, item 3: decode is bound by the KV
+ * read).  Arguments as in nvfp4kv_decode_attention; sink is a device uint32
+ * that receives an XOR of one word per page (keeps the reads alive).
+ *   NVFP4KV_PROBE_DECODE_PATTERN  the decode's grid, split over warps, per-warp
+ *                                 rings of 2304-byte page-heads copied by
+ *                                 16-byte cp.async pieces, bounded waits
+ *   NVFP4KV_PROBE_WHOLE_PAGES     every KV head of a page as one contiguous bulk
+ *                                 copy (TMA), one warp per CTA, two CTAs per SM
+ *                                 (num_kv_heads <= 16)
+ * Both split the pages statically and evenly.  A page id or length out of
+ * range is flagged as in the decode; a wait that gives up (~1 s) sets
+ * NVFP4KV_DEVERR_TIMEOUT. */
+enum { NVFP4KV_PROBE_DECODE_PATTERN = 0, NVFP4KV_PROBE_WHOLE_PAGES = 1 };
+int nvfp4kv_stream_probe(const nvfp4kv_cache* cache, const int32_t* page_table, int32_t max_pages_per_seq,
+                         const int32_t* seq_lens, int32_t batch, int mode, uint32_t* sink,
+                         int32_t* device_status, nvfp4kv_stream_t stream);
+
 /* Text of the CUDA error behind this thread's latest NVFP4KV_ERR_CUDA (the
  * runtime's own message; "no CUDA error" if there was none).  Never NULL. */
 const char* nvfp4kv_last_cuda_error(void);

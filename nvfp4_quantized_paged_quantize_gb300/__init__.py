@@ -28,6 +28,8 @@ NVFP4KV_DEVERR_PAGE = 2
 NVFP4KV_DEVERR_LENGTH = 4
 NVFP4KV_DEVERR_TIMEOUT = 8
 NVFP4KV_DEVERR_ROW = 16
+NVFP4KV_PROBE_DECODE_PATTERN = 0
+NVFP4KV_PROBE_WHOLE_PAGES = 1
 NVFP4KV_VARIANT_SR = 1
 NVFP4KV_VARIANT_HADAMARD = 2
 NVFP4KV_VARIANT_MXFP4 = 3
@@ -98,6 +100,7 @@ def load(path: str | None = None, build_if_missing: bool = True):
     L.nvfp4kv_extend_attention.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32, f32, f32, f32, vp,
                                            vp, vp]
     L.nvfp4kv_calibrated_global_scale.argtypes = [f32, ctypes.POINTER(f32)]
+    L.nvfp4kv_stream_probe.argtypes = [pc, vp, i32, vp, i32, ctypes.c_int, vp, vp, vp]
     L.nvfp4kv_last_cuda_error.argtypes = []
     L.nvfp4kv_last_cuda_error.restype = ctypes.c_char_p
     L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
@@ -106,7 +109,8 @@ def load(path: str | None = None, build_if_missing: bool = True):
                  "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
                  "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
                  "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
-                 "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant"):
+                 "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant",
+                 "nvfp4kv_stream_probe"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -361,6 +365,17 @@ def nvfp4kv_tensor_amax(x, amax, accumulate: bool = False, stream=None) -> None:
                                     int(bool(accumulate)), _stream(stream)))
 
 
+def nvfp4kv_stream_probe(cache: Cache, page_table, seq_lens, sink, mode: int = NVFP4KV_PROBE_DECODE_PATTERN,
+                         device_status=None, stream=None) -> None:
+    """Read every cached page-head of the batch once with no attention math (a measurement aid):
+    the decode's pattern, or whole pages by bulk copy; sink: a uint32 device tensor of one element."""
+    c = cache.c_struct()
+    _check("nvfp4kv_stream_probe",
+           _L().nvfp4kv_stream_probe(ctypes.byref(c), _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens),
+                                     int(seq_lens.shape[0]), int(mode), _ptr(sink), _ptr(device_status),
+                                     _stream(stream)))
+
+
 def nvfp4kv_calibrated_global_scale(amax: float) -> float:
     """The FP32 global scale that maps amax onto 6 * 448 (1.0 when amax == 0)."""
     g = ctypes.c_float()
@@ -373,4 +388,5 @@ __all__ = ["Cache", "Nvfp4kvError", "load", "NVFP4KV_PAGE_HEAD_BYTES", "NVFP4KV_
            "nvfp4kv_decode_workspace_size", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_attention", "nvfp4kv_dequant_to_fp8_workspace",
            "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
            "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
-           "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant"]
+           "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant",
+           "nvfp4kv_stream_probe", "NVFP4KV_PROBE_DECODE_PATTERN", "NVFP4KV_PROBE_WHOLE_PAGES"]

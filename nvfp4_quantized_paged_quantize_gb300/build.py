@@ -17,8 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libnvfp4kv.so")
 SOURCES = ["api.cu", "quantize_append.cu", "decode_attention.cu", "dequant_fp8.cu", "decode_no_alloc.cu",
-           "calibrate.cu", "extend_attention.cu",
-           "quantize_variants.cu"]
+           "calibrate.cu", "extend_attention.cu", "quantize_variants.cu", "stream_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
               "-I", INCLUDE, "-I", CSRC]

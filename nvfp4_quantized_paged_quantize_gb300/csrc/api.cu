@@ -318,6 +318,27 @@ int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* 
                                                  device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4kv_stream_probe(const nvfp4kv_cache* cache, const int32_t* page_table, int32_t max_pages_per_seq,
+                         const int32_t* seq_lens, int32_t batch, int mode, uint32_t* sink, int32_t* device_status,
+                         nvfp4kv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != NVFP4KV_OK) return st;
+  if (mode != NVFP4KV_PROBE_DECODE_PATTERN && mode != NVFP4KV_PROBE_WHOLE_PAGES) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (batch < 0 || max_pages_per_seq <= 0) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (mode == NVFP4KV_PROBE_WHOLE_PAGES && cache->num_kv_heads > 16) return NVFP4KV_ERR_UNSUPPORTED;
+  if (batch == 0) return NVFP4KV_OK;
+  if ((int64_t)batch * max_pages_per_seq * cache->num_kv_heads >= (int64_t(1) << 31) ||
+      (int64_t)max_pages_per_seq * kPageSize >= (int64_t(1) << 31))
+    return NVFP4KV_ERR_UNSUPPORTED;
+  if (!page_table || !seq_lens || !sink || !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(sink, 4))
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
+  return cuda_status(nvfp4kv::launch_stream_probe(*cache, page_table, max_pages_per_seq, seq_lens, batch, mode,
+                                                  sink, device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* nvfp4kv_last_cuda_error(void) {
   return last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(last_cuda_error);
 }

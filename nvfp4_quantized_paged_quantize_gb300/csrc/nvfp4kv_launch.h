@@ -88,6 +88,11 @@ size_t decode_workspace_bytes(int num_sms, int32_t batch, int32_t num_kv_heads);
 // divides num_q_heads.
 size_t decode_workspace_bound(int num_sms, int32_t batch, int32_t num_q_heads);
 
+// The decode's memory stream with no math (NVFP4KV_PROBE_* modes).
+cudaError_t launch_stream_probe(const nvfp4kv_cache& c, const int32_t* page_table, int32_t max_pages,
+                                const int32_t* seq_lens, int32_t batch, int mode, uint32_t* sink,
+                                int32_t* device_status, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                           int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
