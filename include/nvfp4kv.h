@@ -28,7 +28,8 @@
  *     [1024, 1152)  K scales  16 rows x 8 E4M3 bytes; scale j covers elements
  *                             16j..16j+15 of the row
  *     [1152, 2176)  V data    as K
- *     [2176, 2304)  V scales  as K
+ *     [2176, 2304)  V scales  block-major: 8 blocks x 16 tokens, the scale of
+ *                             block j of row r at 2176 + 16 j + r
  * A slot s is row (s % page_size) of page (s / page_size).  Supported:
  * head_dim = 128, page_size = 16.  The pool must be 16-byte aligned (256-byte
  * alignment lets every page-head start on a 128-byte line).
@@ -93,8 +94,9 @@ enum {
  * per value). */
 #define NVFP4KV_PAGE_HEAD_BYTES 2304
 /* Bytes of one page-head of the MXFP4 variant's pool (4 E8M0 scale bytes per
- * row): K data [0, 1024), K scales [1024, 1088), V data [1088, 2112),
- * V scales [2112, 2176). */
+ * row): K data [0, 1024), K scales [1024, 1088) token-major, V data
+ * [1088, 2112), V scales [2112, 2176) block-major (block j of row r at
+ * 2112 + 16 j + r). */
 #define NVFP4KV_MXFP4_PAGE_HEAD_BYTES 2176
 
 /* One layer's paged NVFP4 cache.  The struct itself is read on the host only. */

@@ -154,7 +154,9 @@ class Cache:
     variant's page-heads of 2176 bytes (4 E8M0 scale bytes per row).
 
     k_data / v_data ([num_pages, num_kv_heads, 16, 64]) and k_scale / v_scale
-    ([num_pages, num_kv_heads, 16, 8], or 4 for MXFP4) are views of the pool.
+    ([num_pages, num_kv_heads, 16, 8], or 4 for MXFP4) are views of the pool,
+    indexed [page, head, token row, block] (V scales are stored block-major;
+    their view is transposed).
     """
     pages: object
     num_pages: int
@@ -199,7 +201,9 @@ class Cache:
 
     @property
     def v_scale(self):
-        return self._view(3, HEAD_DIM // (32 if self.mxfp4 else 16))
+        lo, hi = self._parts()[3]
+        blocks = HEAD_DIM // (32 if self.mxfp4 else 16)
+        return self.pages[:, :, lo:hi].unflatten(-1, (blocks, PAGE_SIZE)).transpose(-1, -2)
 
     def c_struct(self) -> _CCache:
         return _CCache(_ptr(self.pages), int(self.num_pages), int(self.num_kv_heads), int(self.head_dim),

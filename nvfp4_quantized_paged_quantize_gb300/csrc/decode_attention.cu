@@ -143,6 +143,16 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same with a zero accumulator: d = a * b (the first MMA of a chain).
+__device__ __forceinline__ void mma16816_zero(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 __device__ __forceinline__ uint32_t dup_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
 __device__ __forceinline__ uint32_t dup_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
 
@@ -380,10 +390,6 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
     const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t));
     const uint32_t sa0 = dup_lo(sa), sa1 = dup_hi(sa), sb0 = dup_lo(sb), sb1 = dup_hi(sb);
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sc[k][h][j] = 0.0f;
-#pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t wa = word_of(ka, i >> 1), wb = word_of(kb, i >> 1);
       uint32_t a0, a1, a2, a3;
@@ -394,7 +400,12 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
       }
       const uint32_t s_g = i < 4 ? sa0 : sa1, s_g8 = i < 4 ? sb0 : sb1;
       a0 = hmul2(a0, s_g); a2 = hmul2(a2, s_g); a1 = hmul2(a1, s_g8); a3 = hmul2(a3, s_g8);
-      mma16816(sc[k][NVFP4KV_DECODE_QK_CHAINS == 2 ? (i >> 2) : 0], a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
+      // chain c = i / 4 (two chains) or 0: its first MMA starts from zero
+      const int c = NVFP4KV_DECODE_QK_CHAINS == 2 ? (i >> 2) : 0;
+      if (i == 0 || (NVFP4KV_DECODE_QK_CHAINS == 2 && i == 4))
+        mma16816_zero(sc[k][c], a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
+      else
+        mma16816(sc[k][c], a0, a1, a2, a3, s.qf[i][0], s.qf[i][1]);
     }
   }
 
@@ -460,16 +471,17 @@ __device__ __forceinline__ void pv_phase(const uint8_t* const (&stage)[NP], cons
     const uint8_t* vd = stage[k] + kOffVD;
     const uint8_t* vs = stage[k] + kOffVS;
     const int t0 = 2 * t, t1 = 2 * t + 1, t8 = 2 * t + 8, t9 = 2 * t + 9;
-    uint32_t s0 = vs[t0 * kRowScales + g], s1 = vs[t1 * kRowScales + g];
-    uint32_t s8 = vs[t8 * kRowScales + g], s9 = vs[t9 * kRowScales + g];
+    // V scales are block-major: block g's scales of tokens (2t, 2t+1) and (2t+8, 2t+9) are adjacent pairs
+    uint32_t p01 = *reinterpret_cast<const uint16_t*>(vs + g * kPage + t0);
+    uint32_t p89 = *reinterpret_cast<const uint16_t*>(vs + g * kPage + t8);
     if (!kFull && nvalid[k] < kPage) {  // tokens past the end: scale 0 keeps unwritten bytes out of the sum
-      if (t0 >= nvalid[k]) s0 = 0;
-      if (t1 >= nvalid[k]) s1 = 0;
-      if (t8 >= nvalid[k]) s8 = 0;
-      if (t9 >= nvalid[k]) s9 = 0;
+      if (t0 >= nvalid[k]) p01 &= 0xFF00u;
+      if (t1 >= nvalid[k]) p01 &= 0x00FFu;
+      if (t8 >= nvalid[k]) p89 &= 0xFF00u;
+      if (t9 >= nvalid[k]) p89 &= 0x00FFu;
     }
-    const uint32_t sv01 = e4m3x2_to_f16x2(s0 | (s1 << 8));  // (token 2t, token 2t+1)
-    const uint32_t sv89 = e4m3x2_to_f16x2(s8 | (s9 << 8));
+    const uint32_t sv01 = e4m3x2_to_f16x2(p01);  // (token 2t, token 2t+1)
+    const uint32_t sv89 = e4m3x2_to_f16x2(p89);
     const uint2 d0 = *reinterpret_cast<const uint2*>(vd + t0 * kRowBytes + 8 * g);
     const uint2 d1 = *reinterpret_cast<const uint2*>(vd + t1 * kRowBytes + 8 * g);
     const uint2 d8 = *reinterpret_cast<const uint2*>(vd + t8 * kRowBytes + 8 * g);

@@ -121,7 +121,6 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(De
   const int tensor = warp & 1;  // 0: K, 1: V
   const int r = lane >> 1, half = lane & 1;
   const int off_data = tensor ? kOffVData : kOffKData;  // within a page-head
-  const int off_scale = tensor ? kOffVScale : kOffKScale;
   uint8_t* ws = tensor ? p.ws_v : p.ws_k;
   const float g = tensor ? p.gv : p.gk, sws = tensor ? p.sv : p.sk, rs = tensor ? p.rsv : p.rsk;
   const bool fast = tensor ? p.sv_fast : p.sk_fast;
@@ -144,7 +143,15 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(De
     const uint8_t* phd = p.pages + ((int64_t)(page_ok ? page : 0) * p.hkv + h) * kPageHeadBytes;
     const uint4* src = reinterpret_cast<const uint4*>(phd + off_data + r * kRowBytes) + 2 * half;
     const uint4 d0 = __ldg(src), d1 = __ldg(src + 1);  // blocks 4 half .. 4 half + 3
-    const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(phd + off_scale + r * kRowScales) + half);
+    // the scales of blocks 4 half .. 4 half + 3 of row r (K: 4 adjacent bytes; V: block-major, 16 apart)
+    uint32_t sc4;
+    if (tensor == 0) {
+      sc4 = __ldg(reinterpret_cast<const uint32_t*>(phd + k_scale_offset(r, 4 * half)));
+    } else {
+      sc4 = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sc4 |= (uint32_t)__ldg(phd + v_scale_offset(r, 4 * half + k)) << (8 * k);
+    }
     const int t = pg * kPage + r;   // this lane's token of the prefix
     const int64_t orow = base + t;  // its workspace row
     const bool live = t < L && orow >= 0 && orow < p.total_rows;

@@ -25,6 +25,9 @@ constexpr int kDevErrTimeout = 8;                      // a bounded wait gave up
 
 // One page-head (16 tokens of one KV head) of the pool: K data, K scales,
 // V data, V scales, contiguous; the page-heads of a page follow one another.
+// K scales are token-major (the 8 scales of a token row together), V scales
+// block-major (the 16 tokens' scales of one 16-value block together): the
+// decode reads K scales by token and V scales by token pair within a block.
 constexpr int kOffKData = 0;
 constexpr int kOffKScale = kPageDataBytes;                        // 1024
 constexpr int kOffVData = kPageDataBytes + kPageScaleBytes;       // 1152
@@ -38,6 +41,12 @@ constexpr int kMxOffVData = kPageDataBytes + kPage * kMxRowScales;  // 1088
 constexpr int kMxOffVScale = 2 * kPageDataBytes + kPage * kMxRowScales;  // 2112
 constexpr int kMxPageHeadBytes = 2 * (kPageDataBytes + kPage * kMxRowScales);  // 2176
 static_assert(kMxPageHeadBytes == NVFP4KV_MXFP4_PAGE_HEAD_BYTES, "MXFP4 page-head size");
+
+// Byte offset, within a page-head, of the scale of block j of token row r.
+__host__ __device__ constexpr int k_scale_offset(int r, int j) { return kOffKScale + r * kRowScales + j; }
+__host__ __device__ constexpr int v_scale_offset(int r, int j) { return kOffVScale + j * kPage + r; }
+__host__ __device__ constexpr int mx_k_scale_offset(int r, int j) { return kMxOffKScale + r * kMxRowScales + j; }
+__host__ __device__ constexpr int mx_v_scale_offset(int r, int j) { return kMxOffVScale + j * kPage + r; }
 
 // ---------------------------------------------------------------------------
 // E2M1 / E4M3 conversions (round to nearest even, saturating, as the

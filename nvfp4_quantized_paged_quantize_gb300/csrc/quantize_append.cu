@@ -71,8 +71,7 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
   const int sub = lane & 7;      // block j = sub of the row: values [16 j, 16 j + 16)
   const int which = (lane >> 3) & 1;  // first or second row of the step
   const uint16_t* src = tensor ? p.v : p.k;
-  const int off_data = tensor ? kOffVData : kOffKData;    // within a page-head
-  const int off_scale = tensor ? kOffVScale : kOffKScale;
+  const int off_data = tensor ? kOffVData : kOffKData;  // within a page-head
   const float g = tensor ? p.gv : p.gk;
   const float t6 = __fmul_rn(6.0f, g);  // the block amax maps onto E2M1's 6
   const float r6 = __frcp_rn(t6);
@@ -172,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
       for (int k = 0; k < 4; ++k) hi |= e2m1x2_from_f32(y[8 + 2 * k], y[8 + 2 * k + 1]) << (8 * k);
     }
     reinterpret_cast<uint2*>(ph + off_data + rin * kRowBytes)[sub] = make_uint2(lo, hi);
-    ph[off_scale + rin * kRowScales + sub] = (uint8_t)sb;
+    ph[tensor ? v_scale_offset(rin, sub) : k_scale_offset(rin, sub)] = (uint8_t)sb;
   }
 }
 

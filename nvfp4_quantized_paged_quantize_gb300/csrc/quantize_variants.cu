@@ -179,11 +179,11 @@ __global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParam
   if constexpr (kVariant == NVFP4KV_VARIANT_MXFP4) {
     uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * kMxPageHeadBytes;
     reinterpret_cast<uint2*>(ph + (tensor ? kMxOffVData : kOffKData) + rin * kRowBytes)[sub] = make_uint2(lo, hi);
-    if ((sub & 1) == 0) ph[(tensor ? kMxOffVScale : kMxOffKScale) + rin * kMxRowScales + (sub >> 1)] = (uint8_t)sbyte;
+    if ((sub & 1) == 0) ph[tensor ? mx_v_scale_offset(rin, sub >> 1) : mx_k_scale_offset(rin, sub >> 1)] = (uint8_t)sbyte;
   } else {
     uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * kPageHeadBytes;
     reinterpret_cast<uint2*>(ph + (tensor ? kOffVData : kOffKData) + rin * kRowBytes)[sub] = make_uint2(lo, hi);
-    ph[(tensor ? kOffVScale : kOffKScale) + rin * kRowScales + sub] = (uint8_t)sbyte;
+    ph[tensor ? v_scale_offset(rin, sub) : k_scale_offset(rin, sub)] = (uint8_t)sbyte;
   }
 }
 

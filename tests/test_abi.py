@@ -76,6 +76,13 @@ def test_page_head_views_cover_the_pool_once(lib):
         # the order within a page-head: K data, K scales, V data, V scales
         ph = c.pages[1, 1].tolist()
         assert ph == [1] * 1024 + [2] * 16 * sc + [3] * 1024 + [4] * 16 * sc
+        # K scales token-major, V scales block-major
+        c.pages.zero_()
+        c.k_scale[0, 0, 3, 1] = 7
+        c.v_scale[0, 0, 3, 1] = 9
+        ph = c.pages[0, 0]
+        assert ph[1024 + 3 * sc + 1] == 7
+        assert ph[2048 + 16 * sc + 16 * 1 + 3] == 9
 
 
 def test_decode_workspace_bytes_from_the_batch_shape(lib):
