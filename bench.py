@@ -205,6 +205,59 @@ def _fill_cache_streaming(torch, kv, wl, threads=16):
     return cache
 
 
+def variant_decode_lines(torch, kv, args, flush, hbm_peak):
+    """Decode over each format variant's cache of the 8K workload (the pages'
+    format comparison): the cache written by the variant's append from the
+    workload's bf16 K/V, then the variant's decode timed like NVFP4's.  Bytes:
+    144 per token and KV head (NVFP4, SR, Hadamard) or 136 (MXFP4), plus q and
+    out."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    wl = inputs.decode_config(2)
+    steps = max(3, min(args.steps, 50))
+    q, pt = _bf16(torch, wl.q()), _dev(torch, wl.page_table)
+    lens = _dev(torch, wl.seq_lens.astype(np.int32))
+    out = torch.empty((wl.batch, wl.num_q_heads, 128), dtype=torch.float32, device="cuda")
+    nk, nv = wl.new_kv()
+    res = {}
+    for name, var in (("sr", kv.NVFP4KV_VARIANT_SR), ("hadamard", kv.NVFP4KV_VARIANT_HADAMARD),
+                      ("mxfp4", kv.NVFP4KV_VARIANT_MXFP4)):
+        mx = var == kv.NVFP4KV_VARIANT_MXFP4
+        cache = kv.Cache.empty(wl.num_pages, wl.num_kv_heads, zero=True, mxfp4=mx)
+
+        def draw(b):
+            k, v = wl.prompt_kv(b)
+            k = np.concatenate([k, nk[b:b + 1]])
+            v = np.concatenate([v, nv[b:b + 1]])
+            n = k.size
+            r = (inputs.rounding_bytes(100 + 2 * b, n).reshape(k.shape),
+                 inputs.rounding_bytes(101 + 2 * b, n).reshape(k.shape)) if var == kv.NVFP4KV_VARIANT_SR else None
+            return k, v, r
+
+        with ThreadPoolExecutor(max_workers=16) as ex:
+            for b, (k, v, r) in enumerate(ex.map(draw, range(wl.batch))):
+                slots = _dev(torch, wl.slots(b, 0, k.shape[0]))
+                rk = _dev(torch, r[0]) if r is not None else None
+                rv = _dev(torch, r[1]) if r is not None else None
+                kv.nvfp4kv_quantize_append_variant(var, cache, _bf16(torch, k), _bf16(torch, v), slots, rk, rv)
+        torch.cuda.synchronize()
+        ws = torch.zeros(kv.nvfp4kv_decode_workspace_size(cache, wl.batch, wl.num_q_heads), dtype=torch.uint8,
+                         device="cuda")
+        ms, _ = time_steps(torch, steps, args.warmup,
+                           lambda ev=None, c=cache, var=var: kv.nvfp4kv_decode_attention_variant(
+                               var, c, q, out, pt, lens, wl.softmax_scale, ws), flush)
+        t = float(np.mean(ms))
+        per_token_head = 136 if mx else 144
+        nbytes = wl.kv_tokens() * wl.num_kv_heads * per_token_head + q.numel() * 2 + out.numel() * 4
+        gbs = nbytes / (t / 1e3) / 1e9
+        res[f"decode_{name}_b32_ctx8k"] = {"kernel_ms": t, "kv_tokens_per_s": wl.kv_tokens() / (t / 1e3),
+                                           "hbm_gbs": gbs, "frac_of_measured_peak": gbs / hbm_peak,
+                                           "algorithmic_bytes": nbytes, "bytes_per_token_head": per_token_head}
+        del cache, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def _calibration_input(torch, wl):
     """One layer's K of a decode workload as one bf16 device tensor: the first
     sequence's prompt K drawn by the workload, repeated over the batch."""
@@ -440,6 +493,7 @@ def gpu_arm(args):
     if not args.skip_secondary:
         line["secondary"] = secondary(torch, kv, args, flush, hbm_peak)
         line["secondary"]["stream_probe_b32_ctx8k"] = probe
+        line["secondary"].update(variant_decode_lines(torch, kv, args, flush, hbm_peak))
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     if rank == 0:

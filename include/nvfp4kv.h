@@ -370,6 +370,34 @@ int nvfp4kv_quantize_append_variant(int variant, const nvfp4kv_cache* cache, con
                                     const int64_t* slot_mapping, int64_t num_tokens, const uint8_t* rand_k,
                                     const uint8_t* rand_v, int32_t* device_status, nvfp4kv_stream_t stream);
 
+/* Decode attention over a format variant's cache, so that each variant's
+ * accuracy and decode throughput can be set beside NVFP4's ("NVFP4: breaking
+ * the memory wall" (cloud.tencent.com), quantisation techniques; "NVIDIA
+ * NVFP4: LLM memory doubled, inference 3x" (nmedialink), figure 6).  The same
+ * attention as nvfp4kv_decode_attention, over the rows the variant's append
+ * wrote:
+ *   NVFP4KV_VARIANT_SR        the pool is NVFP4 (stochastically rounded codes):
+ *                             exactly nvfp4kv_decode_attention
+ *   NVFP4KV_VARIANT_HADAMARD  the pool holds NVFP4 of H k and H v (H the
+ *                             orthonormal 128-point Walsh-Hadamard transform,
+ *                             its own inverse): the keys and values are
+ *                             H Khat and H Vhat.  q is rotated once (q . H k =
+ *                             H q . k) and the output rotated back, in fp32
+ *   NVFP4KV_VARIANT_MXFP4     the pool holds MXFP4 page-heads
+ *                             (NVFP4KV_MXFP4_PAGE_HEAD_BYTES): values
+ *                             e2m1 * 2^(s - 127), global scales not used.
+ *                             Within a page-head, blocks more than 24 binades
+ *                             below the page's largest scale of K (or V)
+ *                             read as zero (their weight is < 2^-21 of it)
+ * Arguments, workspace (nvfp4kv_decode_workspace_size), layout and errors as
+ * in nvfp4kv_decode_attention.  Unknown variants return
+ * NVFP4KV_ERR_INVALID_ARGUMENT. */
+int nvfp4kv_decode_attention_variant(int variant, const nvfp4kv_cache* cache, const void* q, float* out,
+                                     const int32_t* page_table, int32_t max_pages_per_seq,
+                                     const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                     float softmax_scale, void* workspace, size_t workspace_bytes,
+                                     int32_t* device_status, nvfp4kv_stream_t stream);
+
 /* Global-scale calibration ("nvfp4-kv-cache-memory-wall", section 2: the
  * FP32 per-tensor scale is 1 in the uncalibrated public setting; a calibrated
  * scale maps the tensor's largest magnitude onto the largest NVFP4 magnitude,

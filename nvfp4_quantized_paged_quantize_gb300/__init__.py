@@ -101,6 +101,8 @@ def load(path: str | None = None, build_if_missing: bool = True):
                                            vp, vp]
     L.nvfp4kv_calibrated_global_scale.argtypes = [f32, ctypes.POINTER(f32)]
     L.nvfp4kv_stream_probe.argtypes = [pc, vp, i32, vp, i32, ctypes.c_int, vp, vp, vp]
+    L.nvfp4kv_decode_attention_variant.argtypes = [ctypes.c_int, pc, vp, vp, vp, i32, vp, i32, i32, f32, vp, sz, vp,
+                                                   vp]
     L.nvfp4kv_last_cuda_error.argtypes = []
     L.nvfp4kv_last_cuda_error.restype = ctypes.c_char_p
     L.nvfp4kv_status_string.argtypes = [ctypes.c_int]
@@ -110,7 +112,7 @@ def load(path: str | None = None, build_if_missing: bool = True):
                  "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
                  "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
                  "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant",
-                 "nvfp4kv_stream_probe"):
+                 "nvfp4kv_stream_probe", "nvfp4kv_decode_attention_variant"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -260,6 +262,22 @@ def nvfp4kv_decode_attention(cache: Cache, q, out, page_table, seq_lens, softmax
                                          workspace_bytes, _ptr(device_status), _stream(stream)))
 
 
+def nvfp4kv_decode_attention_variant(variant: int, cache: Cache, q, out, page_table, seq_lens, softmax_scale: float,
+                                     workspace, device_status=None, stream=None,
+                                     workspace_bytes: int | None = None) -> None:
+    """Decode attention over a format variant's cache (NVFP4KV_VARIANT_SR / _HADAMARD / _MXFP4; see
+    include/nvfp4kv.h); arguments as nvfp4kv_decode_attention."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    maxp = int(page_table.shape[1])
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    c = cache.c_struct()
+    _check("nvfp4kv_decode_attention_variant",
+           _L().nvfp4kv_decode_attention_variant(int(variant), ctypes.byref(c), _ptr(q), _ptr(out), _ptr(page_table),
+                                                 maxp, _ptr(seq_lens), B, Hq, float(softmax_scale), _ptr(workspace),
+                                                 workspace_bytes, _ptr(device_status), _stream(stream)))
+
+
 def nvfp4kv_append_decode_attention(cache: Cache, k, v, slot_mapping, q, out, page_table, seq_lens,
                                     softmax_scale: float, workspace, device_status=None, stream=None,
                                     workspace_bytes: int | None = None) -> None:
@@ -393,4 +411,5 @@ __all__ = ["Cache", "Nvfp4kvError", "load", "NVFP4KV_PAGE_HEAD_BYTES", "NVFP4KV_
            "nvfp4kv_status_string", "nvfp4kv_decode_attention_static", "nvfp4kv_append_decode_attention",
            "nvfp4kv_tensor_amax", "nvfp4kv_calibrated_global_scale", "nvfp4kv_bf16_to_fp8_workspace",
            "nvfp4kv_extend_attention", "nvfp4kv_quantize_append_fp8", "nvfp4kv_quantize_append_variant",
-           "nvfp4kv_stream_probe", "NVFP4KV_PROBE_DECODE_PATTERN", "NVFP4KV_PROBE_WHOLE_PAGES"]
+           "nvfp4kv_stream_probe", "NVFP4KV_PROBE_DECODE_PATTERN", "NVFP4KV_PROBE_WHOLE_PAGES",
+           "nvfp4kv_decode_attention_variant"]

@@ -199,6 +199,22 @@ int nvfp4kv_decode_attention(const nvfp4kv_cache* cache, const void* q, float* o
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4kv_decode_attention_variant(int variant, const nvfp4kv_cache* cache, const void* q, float* out,
+                                     const int32_t* page_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                     int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
+                                     size_t workspace_bytes, int32_t* device_status, nvfp4kv_stream_t stream) {
+  if (variant != NVFP4KV_VARIANT_SR && variant != NVFP4KV_VARIANT_HADAMARD && variant != NVFP4KV_VARIANT_MXFP4)
+    return NVFP4KV_ERR_INVALID_ARGUMENT;
+  int nsm = 0;
+  const int st = check_decode(cache, q, out, page_table, max_pages_per_seq, seq_lens, batch, num_q_heads,
+                              softmax_scale, workspace, workspace_bytes, device_status, &nsm);
+  if (st != NVFP4KV_OK || batch == 0) return st;
+  return cuda_status(nvfp4kv::launch_decode_variant(variant, *cache, static_cast<const uint16_t*>(q), out, page_table,
+                                                    max_pages_per_seq, seq_lens, batch, num_q_heads, softmax_scale,
+                                                    workspace, device_status, nsm,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, const void* v,
                                     const int64_t* slot_mapping, int64_t num_tokens, const void* q, float* out,
                                     const int32_t* page_table, int32_t max_pages_per_seq,

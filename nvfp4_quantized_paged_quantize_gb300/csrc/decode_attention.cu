@@ -61,13 +61,18 @@ constexpr int kCtasPerSm = NVFP4KV_DECODE_CTAS_PER_SM; // resident CTAs per SM t
 constexpr int kGMax = 8;        // query heads per KV head (one MMA n-tile)
 constexpr float kLazy = 8.0f;   // running-max slack (log2 units): P <= 2^8 in f16
 
+// Cache formats the decode reads: NVFP4; NVFP4 of Hadamard-rotated rows (q is
+// rotated on the way in and the output rotated back, both exact orthonormal
+// transforms); MXFP4 (blocks of 32 with E8M0 scales, 4 per row).
+enum : int { kFmtNvfp4 = 0, kFmtHadamard = 1, kFmtMxfp4 = 2 };
+
 // stage layout: the page-head as stored (K data | K scales | V data | V scales)
 constexpr int kOffKD = kOffKData;
-constexpr int kOffVD = kOffVData;
-constexpr int kOffKS = kOffKScale;
-constexpr int kOffVS = kOffVScale;
-constexpr int kStageBytes = kPageHeadBytes;  // 2304
-constexpr int kCopyChunks = kStageBytes / 16;  // 144 16-byte pieces per page-head
+__host__ __device__ constexpr int ph_bytes(int F) { return F == kFmtMxfp4 ? kMxPageHeadBytes : kPageHeadBytes; }
+__host__ __device__ constexpr int off_vd(int F) { return F == kFmtMxfp4 ? kMxOffVData : kOffVData; }
+__host__ __device__ constexpr int off_ks(int F) { return F == kFmtMxfp4 ? kMxOffKScale : kOffKScale; }
+__host__ __device__ constexpr int off_vs(int F) { return F == kFmtMxfp4 ? kMxOffVScale : kOffVScale; }
+constexpr int kStageBytes = kPageHeadBytes;  // stage stride: the larger page-head (2304)
 
 // a (partial) result record: O[kGMax][128] unnormalised, m[kGMax] (base 2), l[kGMax]
 constexpr int kRecFloats = kGMax * kHeadDim + 2 * kGMax;
@@ -268,20 +273,22 @@ __device__ __forceinline__ int item_row(const ItemMap& cur, const ItemMap& nxt, 
 }
 
 // cp.async staging: lane l copies the 16-byte pieces l, l + 32, ... of the
-// page-head (lanes 0-15 five of the 144, the others four), then arrives
-// (no-increment) on the stage's mbarrier, which expects 32 arrivals.  The
-// lane's source base and shared-memory offset are set up once.
+// page-head (NVFP4: lanes 0-15 five of the 144, the others four; MXFP4: lanes
+// 0-7 five of the 136), then arrives (no-increment) on the stage's mbarrier,
+// which expects 32 arrivals.  The lane's source base and shared-memory offset
+// are set up once.
 struct LaneCopy {
   const uint8_t* src;  // pages + 16 * lane
   uint32_t off;        // 16 * lane
-  bool fifth;          // lanes 0-15: a fifth piece at 16 * (lane + 128)
+  bool fifth;          // a fifth piece at 16 * (lane + 128)
 };
 
+template <int F>
 __device__ __forceinline__ LaneCopy lane_copy(const DecodeParams& p, int lane) {
   LaneCopy c;
   c.src = p.pages + 16 * lane;
   c.off = 16u * lane;
-  c.fifth = lane + 128 < kCopyChunks;
+  c.fifth = lane + 128 < ph_bytes(F) / 16;
   return c;
 }
 
@@ -289,10 +296,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+template <int F>
 __device__ __forceinline__ void issue_page_cpasync(const LaneCopy& c, int row, uint32_t st, uint32_t bar,
                                                    int lane) {
   if (row >= 0) {
-    const uint8_t* src = c.src + (size_t)row * kPageHeadBytes;
+    const uint8_t* src = c.src + (size_t)row * ph_bytes(F);
     const uint32_t dst = st + c.off;
 #pragma unroll
     for (int k = 0; k < 4; ++k) cp_async16(dst + 512 * k, src + 512 * k);
@@ -312,6 +320,50 @@ struct WarpState {
   float l0, l1;     // this lane's partial sums of P over its tokens
   float c0, c1;     // score multipliers of heads 2t, 2t+1
 };
+
+// Orthonormal Walsh-Hadamard transform (Sylvester order) of the 128 values of
+// a row held by a group of lanes: each lane holds N consecutive values (index
+// bits below log2 N); passes across lanes pair the lane with lane ^ x for
+// each lane mask x in `xs` (index bits above, lowest first), the lower lane
+// keeping a + b and the upper a - b.  Then one product with RN(1 / sqrt(128)).
+template <int N, int NX>
+__device__ __forceinline__ void hadamard_lanes(float (&v)[N], const int (&xs)[NX], int lane) {
+#pragma unroll
+  for (int h = 1; h < N; h *= 2)
+#pragma unroll
+    for (int i = 0; i < N; i += 2 * h)
+#pragma unroll
+      for (int j = i; j < i + h; ++j) {
+        const float a = v[j], b = v[j + h];
+        v[j] = a + b;
+        v[j + h] = a - b;
+      }
+#pragma unroll
+  for (int k = 0; k < NX; ++k) {
+    const bool upper = (lane & xs[k]) != 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], xs[k]);
+      v[i] = upper ? o - v[i] : v[i] + o;
+    }
+  }
+  const float c = 0x1.6a09e6p-4f;  // RN(1 / sqrt(128))
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] *= c;
+}
+
+// 2^d as an f16 for an integer d <= 0 (0 below f16's range): the relative
+// weight of an MXFP4 block whose E8M0 exponent is d below the page's largest.
+__device__ __forceinline__ uint32_t exp2_f16_bits(int d) {
+  if (d >= -14) return (uint32_t)(d + 15) << 10;   // normal
+  if (d >= -24) return 1u << (d + 24);             // subnormal
+  return 0u;
+}
+
+// 2^e as an fp32 for an E8M0 exponent e in [-127, 127].
+__device__ __forceinline__ float exp2_f32(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
 
 // The bf16 q elements lane (g, t) needs for pair b * hkv + h: head h * G + g,
 // elements 32t .. 32t + 31 (zeros for g >= G).  Query heads of pair P start at
@@ -335,6 +387,7 @@ __device__ __forceinline__ QRaw fetch_q(const DecodeParams& p, int pair, int g, 
 
 // Turn fetched q into B-fragments with a per-head power-of-two prescale and
 // reset the pair's softmax state.
+template <int F>
 __device__ __forceinline__ void load_q(const DecodeParams& p, const QRaw& raw, WarpState& s, int g, int t) {
   float qv[32];
 #pragma unroll
@@ -344,6 +397,13 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const QRaw& raw, W
     qv[8 * j + 2] = bf16_to_f32(w.y & 0xFFFFu); qv[8 * j + 3] = bf16_to_f32(w.y >> 16);
     qv[8 * j + 4] = bf16_to_f32(w.z & 0xFFFFu); qv[8 * j + 5] = bf16_to_f32(w.z >> 16);
     qv[8 * j + 6] = bf16_to_f32(w.w & 0xFFFFu); qv[8 * j + 7] = bf16_to_f32(w.w >> 16);
+  }
+  if constexpr (F == kFmtHadamard) {
+    // the cache holds NVFP4 of H k for each key k: q . k = (H q) . (H k), so q
+    // is rotated once here (lane t holds elements 32t .. 32t + 31: passes 1-16
+    // inside the lane, 32 and 64 across lanes t ^ 1 and t ^ 2)
+    const int xs[2] = {1, 2};
+    hadamard_lanes<32, 2>(qv, xs, (g << 2) | t);
   }
   float amax = 0.0f;
 #pragma unroll
@@ -377,18 +437,51 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const QRaw& raw, W
 
 // Phase 1 of a step: S^T = Khat q^T for NP pages (16 tokens x G heads each),
 // two independent accumulator chains per page (tiles 0-3 and 4-7).
-template <int NP>
-__device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], const WarpState& s,
-                                         float (&sc)[NP][2][4], int g, int t) {
+// MXFP4 pages carry their scales relative to the page's largest exponent (per
+// K and per V, so every product stays inside f16): kx[k] = 2^(K's largest)
+// multiplies the page's scores, ve[k] (V's largest) enters the softmax exponent.
+struct PageExp {
+  float kx;  // 2^ek
+  int ve;    // ev
+};
+
+template <int NP, int F>
+__device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], const int (&nvalid)[NP],
+                                         const WarpState& s, float (&sc)[NP][2][4], PageExp (&pe)[NP], int g,
+                                         int t) {
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     const uint8_t* kd = stage[k] + kOffKD;
-    const uint8_t* ks = stage[k] + kOffKS;
+    const uint8_t* ks = stage[k] + off_ks(F);
     const uint4 ka = *reinterpret_cast<const uint4*>(kd + g * kRowBytes + 16 * t);
     const uint4 kb = *reinterpret_cast<const uint4*>(kd + (g + 8) * kRowBytes + 16 * t);
-    const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t));
-    const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t));
-    const uint32_t sa0 = dup_lo(sa), sa1 = dup_hi(sa), sb0 = dup_lo(sb), sb1 = dup_hi(sb);
+    uint32_t sa0, sa1, sb0, sb1;
+    if constexpr (F == kFmtMxfp4) {
+      // the lane's 32 values of rows g and g + 8 are one block (t); the 64 K
+      // scale bytes of the page are read once over the warp, as are V's
+      // (rows at or past the page's valid tokens hold other data: they count as 0)
+      const int nv = nvalid[k];
+      const int ea = g < nv ? ks[g * kMxRowScales + t] : 0, eb = g + 8 < nv ? ks[(g + 8) * kMxRowScales + t] : 0;
+      int ek = max(ea, eb);
+      const uint8_t* vsc = stage[k] + off_vs(F) + (g >> 1) * kPage;
+      int ev = max(max(2 * t < nv ? vsc[2 * t] : 0, 2 * t + 1 < nv ? vsc[2 * t + 1] : 0),
+                   max(2 * t + 8 < nv ? vsc[2 * t + 8] : 0, 2 * t + 9 < nv ? vsc[2 * t + 9] : 0));
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        ek = max(ek, __shfl_xor_sync(0xFFFFFFFFu, ek, off));
+        ev = max(ev, __shfl_xor_sync(0xFFFFFFFFu, ev, off));
+      }
+      pe[k].kx = exp2_f32(ek - 127);
+      pe[k].ve = ev - 127;
+      sa0 = sa1 = dup_lo(exp2_f16_bits(ea - ek));
+      sb0 = sb1 = dup_lo(exp2_f16_bits(eb - ek));
+    } else {
+      const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t));
+      const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t));
+      sa0 = dup_lo(sa); sa1 = dup_hi(sa); sb0 = dup_lo(sb); sb1 = dup_hi(sb);
+      pe[k].kx = 1.0f;
+      pe[k].ve = 0;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t wa = word_of(ka, i >> 1), wb = word_of(kb, i >> 1);
@@ -413,24 +506,34 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
 
 // Phase 2: online softmax (base 2) over the NP pages' scores, one running-max
 // check for all of them; returns P^T as mma B fragments (k = tokens, n = heads).
-template <int NP, bool kFull>
-__device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const int (&nvalid)[NP], WarpState& s,
-                                              uint32_t (&pb)[NP][2], int g) {
-  // raw scores; the running max is kept in scaled (base-2) units: max(S c) = c max(S), c > 0
+template <int NP, bool kFull, int F>
+__device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const PageExp (&pe)[NP],
+                                              const int (&nvalid)[NP], WarpState& s, uint32_t (&pb)[NP][2], int g) {
+  // raw scores; the running max is kept in scaled (base-2) units: max(S c) = c max(S), c > 0.
+  // MXFP4: page k's weights carry 2^ve[k] (its V exponent), folded into the
+  // exponent so that P stays within f16; the sums l take it out again.
   float S[NP][4];
-  float ms0 = -INFINITY, ms1 = -INFINITY;
+  float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) S[k][j] = NVFP4KV_DECODE_QK_CHAINS == 2 ? sc[k][0][j] + sc[k][1][j] : sc[k][0][j];
+    if constexpr (F == kFmtMxfp4) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) S[k][j] *= pe[k].kx;
+    }
     if (!kFull && nvalid[k] < kPage) {
       if (g >= nvalid[k]) S[k][0] = S[k][1] = -INFINITY;
       if (g + 8 >= nvalid[k]) S[k][2] = S[k][3] = -INFINITY;
     }
-    ms0 = fmaxf(ms0, fmaxf(S[k][0], S[k][2]));
-    ms1 = fmaxf(ms1, fmaxf(S[k][1], S[k][3]));
+    float a0 = fmaxf(S[k][0], S[k][2]) * s.c0, a1 = fmaxf(S[k][1], S[k][3]) * s.c1;
+    if constexpr (F == kFmtMxfp4) {
+      a0 += (float)pe[k].ve;
+      a1 += (float)pe[k].ve;
+    }
+    mx0 = fmaxf(mx0, a0);
+    mx1 = fmaxf(mx1, a1);
   }
-  float mx0 = ms0 * s.c0, mx1 = ms1 * s.c1;
   const bool need = (mx0 > s.m0 + kLazy) || (mx1 > s.m1 + kLazy);
   if (__any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
@@ -452,10 +555,21 @@ __device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const
   const float nm0 = -s.m0, nm1 = -s.m1;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
-    const float p0 = ex2(fmaf(S[k][0], s.c0, nm0)), p1 = ex2(fmaf(S[k][1], s.c1, nm1));
-    const float p2 = ex2(fmaf(S[k][2], s.c0, nm0)), p3 = ex2(fmaf(S[k][3], s.c1, nm1));
-    s.l0 += p0 + p2;
-    s.l1 += p1 + p3;
+    float o0 = nm0, o1 = nm1;
+    if constexpr (F == kFmtMxfp4) {
+      o0 += (float)pe[k].ve;
+      o1 += (float)pe[k].ve;
+    }
+    const float p0 = ex2(fmaf(S[k][0], s.c0, o0)), p1 = ex2(fmaf(S[k][1], s.c1, o1));
+    const float p2 = ex2(fmaf(S[k][2], s.c0, o0)), p3 = ex2(fmaf(S[k][3], s.c1, o1));
+    if constexpr (F == kFmtMxfp4) {
+      const float un = exp2_f32(-pe[k].ve);  // 2^-ve: the sum counts the plain weights
+      s.l0 += (p0 + p2) * un;
+      s.l1 += (p1 + p3) * un;
+    } else {
+      s.l0 += p0 + p2;
+      s.l1 += p1 + p3;
+    }
     // P^T (tokens x heads) in the accumulator layout -> B fragments (k = tokens, n = heads)
     pb[k][0] = movmatrix_trans(pack_f16x2(p0, p1));
     pb[k][1] = movmatrix_trans(pack_f16x2(p2, p3));
@@ -463,25 +577,40 @@ __device__ __forceinline__ void softmax_phase(const float (&sc)[NP][2][4], const
 }
 
 // Phase 3: O^T += Vhat^T P^T for the NP pages.
-template <int NP, bool kFull>
+template <int NP, bool kFull, int F>
 __device__ __forceinline__ void pv_phase(const uint8_t* const (&stage)[NP], const int (&nvalid)[NP],
-                                         const uint32_t (&pb)[NP][2], WarpState& s, int g, int t) {
+                                         const PageExp (&pe)[NP], const uint32_t (&pb)[NP][2], WarpState& s, int g,
+                                         int t) {
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
-    const uint8_t* vd = stage[k] + kOffVD;
-    const uint8_t* vs = stage[k] + kOffVS;
+    const uint8_t* vd = stage[k] + off_vd(F);
+    const uint8_t* vs = stage[k] + off_vs(F);
     const int t0 = 2 * t, t1 = 2 * t + 1, t8 = 2 * t + 8, t9 = 2 * t + 9;
-    // V scales are block-major: block g's scales of tokens (2t, 2t+1) and (2t+8, 2t+9) are adjacent pairs
-    uint32_t p01 = *reinterpret_cast<const uint16_t*>(vs + g * kPage + t0);
-    uint32_t p89 = *reinterpret_cast<const uint16_t*>(vs + g * kPage + t8);
-    if (!kFull && nvalid[k] < kPage) {  // tokens past the end: scale 0 keeps unwritten bytes out of the sum
-      if (t0 >= nvalid[k]) p01 &= 0xFF00u;
-      if (t1 >= nvalid[k]) p01 &= 0x00FFu;
-      if (t8 >= nvalid[k]) p89 &= 0xFF00u;
-      if (t9 >= nvalid[k]) p89 &= 0x00FFu;
+    uint32_t sv01, sv89;  // (token 2t, token 2t+1) and (2t+8, 2t+9) scales of the lane's block, f16x2
+    if constexpr (F == kFmtMxfp4) {
+      // the lane's 16 values are in block g / 2; its E8M0 exponents relative to the page's largest
+      const uint8_t* b = vs + (g >> 1) * kPage;
+      const bool full = kFull || nvalid[k] >= kPage;
+      const int ve = pe[k].ve + 127;
+      const uint32_t e0 = (full || t0 < nvalid[k]) ? exp2_f16_bits(b[t0] - ve) : 0u;
+      const uint32_t e1 = (full || t1 < nvalid[k]) ? exp2_f16_bits(b[t1] - ve) : 0u;
+      const uint32_t e8 = (full || t8 < nvalid[k]) ? exp2_f16_bits(b[t8] - ve) : 0u;
+      const uint32_t e9 = (full || t9 < nvalid[k]) ? exp2_f16_bits(b[t9] - ve) : 0u;
+      sv01 = e0 | (e1 << 16);
+      sv89 = e8 | (e9 << 16);
+    } else {
+      // V scales are block-major: block g's scales of tokens (2t, 2t+1) and (2t+8, 2t+9) are adjacent pairs
+      uint32_t p01 = *reinterpret_cast<const uint16_t*>(vs + g * kPage + t0);
+      uint32_t p89 = *reinterpret_cast<const uint16_t*>(vs + g * kPage + t8);
+      if (!kFull && nvalid[k] < kPage) {  // tokens past the end: scale 0 keeps unwritten bytes out of the sum
+        if (t0 >= nvalid[k]) p01 &= 0xFF00u;
+        if (t1 >= nvalid[k]) p01 &= 0x00FFu;
+        if (t8 >= nvalid[k]) p89 &= 0xFF00u;
+        if (t9 >= nvalid[k]) p89 &= 0x00FFu;
+      }
+      sv01 = e4m3x2_to_f16x2(p01);
+      sv89 = e4m3x2_to_f16x2(p89);
     }
-    const uint32_t sv01 = e4m3x2_to_f16x2(p01);  // (token 2t, token 2t+1)
-    const uint32_t sv89 = e4m3x2_to_f16x2(p89);
     const uint2 d0 = *reinterpret_cast<const uint2*>(vd + t0 * kRowBytes + 8 * g);
     const uint2 d1 = *reinterpret_cast<const uint2*>(vd + t1 * kRowBytes + 8 * g);
     const uint2 d8 = *reinterpret_cast<const uint2*>(vd + t8 * kRowBytes + 8 * g);
@@ -519,18 +648,20 @@ __device__ __forceinline__ void pv_phase(const uint8_t* const (&stage)[NP], cons
 // NP pages of one KV head (16 tokens each, nvalid[k] of them valid) from ring
 // stages, folded into the warp's running softmax state with one max update.
 // kFull: every page has all 16 tokens (no masking code).
-template <int NP, bool kFull>
+template <int NP, bool kFull, int F>
 __device__ __forceinline__ void process_pages(const uint8_t* const (&stage)[NP], const int (&nvalid)[NP],
                                               WarpState& s, int g, int t) {
   float sc[NP][2][4];
   uint32_t pb[NP][2];
-  qk_phase<NP>(stage, s, sc, g, t);
-  softmax_phase<NP, kFull>(sc, nvalid, s, pb, g);
-  pv_phase<NP, kFull>(stage, nvalid, pb, s, g, t);
+  PageExp pe[NP];
+  qk_phase<NP, F>(stage, nvalid, s, sc, pe, g, t);
+  softmax_phase<NP, kFull, F>(sc, pe, nvalid, s, pb, g);
+  pv_phase<NP, kFull, F>(stage, nvalid, pe, pb, s, g, t);
 }
 
 // Finish a warp's piece of a pair: total l over the lanes, then either write
 // the final output (complete pair) or store the piece's record at `slot`.
+template <int F>
 __device__ __forceinline__ void finish_piece(const DecodeParams& p, WarpState& s, int pair, bool complete,
                                              float* slot, int g, int t) {
 #pragma unroll
@@ -544,17 +675,28 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, WarpState& s
     float* base = p.out + ((long long)b * p.hq + (long long)h * p.group) * kHeadDim;
     const float r0 = s.l0 > 0.0f ? p.v_gscale / s.l0 : 0.0f;
     const float r1 = s.l1 > 0.0f ? p.v_gscale / s.l1 : 0.0f;
+    // the lane's values of heads 2t and 2t + 1: d = 16 g + k, k = 0 .. 15
+    float v0[16], v1[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v0[2 * i] = s.o[i][0] * r0; v0[2 * i + 1] = s.o[i][2] * r0;
+      v1[2 * i] = s.o[i][1] * r1; v1[2 * i + 1] = s.o[i][3] * r1;
+    }
+    if constexpr (F == kFmtHadamard) {
+      // rotate the output back (d bits 0-3 in the lane, 4-6 across lanes g: lane ^ 4, 8, 16)
+      const int xs[3] = {4, 8, 16};
+      hadamard_lanes<16, 3>(v0, xs, (g << 2) | t);
+      hadamard_lanes<16, 3>(v1, xs, (g << 2) | t);
+    }
     if (h0 < p.group) {
       float4* dst = reinterpret_cast<float4*>(base + h0 * kHeadDim + 16 * g);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_float4(s.o[2 * j][0] * r0, s.o[2 * j][2] * r0, s.o[2 * j + 1][0] * r0, s.o[2 * j + 1][2] * r0);
+      for (int j = 0; j < 4; ++j) dst[j] = make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
     }
     if (h1 < p.group) {
       float4* dst = reinterpret_cast<float4*>(base + h1 * kHeadDim + 16 * g);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_float4(s.o[2 * j][1] * r1, s.o[2 * j][3] * r1, s.o[2 * j + 1][1] * r1, s.o[2 * j + 1][3] * r1);
+      for (int j = 0; j < 4; ++j) dst[j] = make_float4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
     }
   } else {
     float4* d0 = reinterpret_cast<float4*>(slot + h0 * kHeadDim + 16 * g);
@@ -585,6 +727,7 @@ __device__ __forceinline__ long long block_sum_ll(long long v, long long* red, i
   return total;
 }
 
+template <int F>
 __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -755,18 +898,18 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // producer: prefill the ring (all within the first chunk: kStages < 32)
     const int pre = n < kStages ? n : kStages;
-    const LaneCopy lc = lane_copy(p, lane);
+    const LaneCopy lc = lane_copy<F>(p, lane);
     const uint32_t wring_u32 = smem_u32(wring);
     for (int j = 0; j < pre; ++j) {
       const int row = __shfl_sync(0xFFFFFFFFu, cur.row, j);
-      issue_page_cpasync(lc, row, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
+      issue_page_cpasync<F>(lc, row, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
     }
     int issued = pre;
     int chunk = 0;   // the chunk `cur` maps
     int st = 0;      // ring stage of the next item
     uint32_t ph = 0; // its mbarrier phase parity
     WarpState s;
-    load_q(p, q_first, s, g, t);  // the first piece's q, fetched before the prefill
+    load_q<F>(p, q_first, s, g, t);  // the first piece's q, fetched before the prefill
     int nseg = 0;
     int i = 0;
     while (i < n) {
@@ -790,7 +933,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       const int iend = min(n, i + (np - page0));
       const long long piece_r = wr0 + i;
       ++nseg;
-      if (nseg > 1) load_q(p, fetch_q(p, pair, g, t), s, g, t);
+      if (nseg > 1) load_q<F>(p, fetch_q(p, pair, g, t), s, g, t);
       for (int j = i; j < iend;) {
         if ((j >> 5) != chunk) {
           if (!nres) vnxt = resolve_chunk(p, nxt);
@@ -831,20 +974,20 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
           const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + (two ? st1 : st) * kStageBytes};
           const int nvs[2] = {nv0, nv1};
           if ((nv0 & nv1) == kPage)
-            process_pages<2, true>(stg, nvs, s, g, t);
+            process_pages<2, true, F>(stg, nvs, s, g, t);
           else if (nv0 | nv1)
-            process_pages<2, false>(stg, nvs, s, g, t);
+            process_pages<2, false, F>(stg, nvs, s, g, t);
           __syncwarp();
           // refill the freed stages with items j + kStages (and j + 1 + kStages)
           const int ja = j + kStages, jb = j + 1 + kStages;
           if (ja < n) {
             const int ra = item_row(cur, nxt, ja, chunk);
-            issue_page_cpasync(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            issue_page_cpasync<F>(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
             issued = ja + 1;
           }
           if (two && jb < n) {
             const int rb = item_row(cur, nxt, jb, chunk);
-            issue_page_cpasync(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
+            issue_page_cpasync<F>(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
             issued = jb + 1;
           }
         }
@@ -872,7 +1015,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       const int last_page = page0 + (iend - i) - 1;
       const bool complete = page0 == 0 && last_page == np - 1;
       const int slot = (iend == n && nseg > 1) ? 1 : 0;
-      finish_piece(p, s, pair, complete, p.part + (2 * gwarp + slot) * kRecFloats, g, t);
+      finish_piece<F>(p, s, pair, complete, p.part + (2 * gwarp + slot) * kRecFloats, g, t);
       if (page0 == 0 && lane == 0) {
         // the pair's first piece writes the pair's header on every call: where
         // its pieces are if it was cut, else the no-op header (0, 0)
@@ -908,6 +1051,7 @@ __device__ __forceinline__ void online_merge(float& M, float& L, float4& acc, fl
   M = Mn;
 }
 
+template <int F>
 __global__ void __launch_bounds__(kCombineMaxGroups * 32) combine_kernel(const DecodeParams p) {
   __shared__ float s_m[kCombineMaxGroups][32], s_l[kCombineMaxGroups][32];
   __shared__ float4 s_o[kCombineMaxGroups][32];
@@ -937,8 +1081,14 @@ __global__ void __launch_bounds__(kCombineMaxGroups * 32) combine_kernel(const D
   if (grp != 0) return;
   for (int k = 1; k < groups; ++k) online_merge(M, L, acc, s_m[k][col], s_l[k][col], s_o[k][col]);
   const float sc = L > 0.0f ? p.v_gscale / L : 0.0f;
+  float v[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
+  if constexpr (F == kFmtHadamard) {
+    // rotate the merged output back (d bits 0-1 in the thread, 2-6 across the warp's 32 columns)
+    const int xs[5] = {1, 2, 4, 8, 16};
+    hadamard_lanes<4, 5>(v, xs, col);
+  }
   reinterpret_cast<float4*>(p.out + ((long long)pair * p.group + head) * kHeadDim)[col] =
-      make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+      make_float4(v[0], v[1], v[2], v[3]);
 }
 
 }  // namespace
@@ -956,14 +1106,17 @@ size_t decode_workspace_bound(int num_sms, int32_t batch, int32_t num_q_heads) {
   return decode_workspace_bytes(num_sms, batch, num_q_heads);
 }
 
-cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
-                          int32_t max_pages, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
-                          float softmax_scale, void* workspace, int32_t* device_status, int num_sms,
-                          cudaStream_t stream, bool after_kernel) {
+namespace {
+
+template <int F>
+cudaError_t launch_decode_fmt(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
+                              int32_t max_pages, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                              float softmax_scale, void* workspace, int32_t* device_status, int num_sms,
+                              cudaStream_t stream, bool after_kernel) {
   // the shared-memory limit is an attribute of the function on each device
   static PerDeviceOnce attr_once;
   const cudaError_t ae = attr_once.run([] {
-    return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (ae != cudaSuccess) return ae;
   const int num_ctas = decode_num_ctas(num_sms);
@@ -979,8 +1132,10 @@ cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
   p.batch = batch;
   p.hq = num_q_heads;
   p.group = num_q_heads / c.num_kv_heads;
-  p.score_scale = softmax_scale * 1.4426950408889634f * c.k_global_scale;
-  p.v_gscale = c.v_global_scale;
+  // MXFP4 has no global scales: its blocks carry power-of-two scales alone
+  const float gk = F == kFmtMxfp4 ? 1.0f : c.k_global_scale, gv = F == kFmtMxfp4 ? 1.0f : c.v_global_scale;
+  p.score_scale = softmax_scale * 1.4426950408889634f * gk;
+  p.v_gscale = gv;
   const size_t pairs = (size_t)batch * (size_t)c.num_kv_heads;
   size_t rec = 2 * (size_t)num_ctas * kNW * kRecFloats * sizeof(float);
   rec = (rec + 255) / 256 * 256;
@@ -1000,9 +1155,9 @@ cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
     da[0].val.programmaticStreamSerializationAllowed = 1;
     dc.attrs = da;
     dc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&dc, decode_kernel, p);
+    e = cudaLaunchKernelEx(&dc, decode_kernel<F>, p);
   } else {
-    decode_kernel<<<num_ctas, kNW * 32, kSmemBytes, stream>>>(p);
+    decode_kernel<F><<<num_ctas, kNW * 32, kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess || pairs == 0) return e;
@@ -1022,8 +1177,33 @@ cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, combine_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, combine_kernel<F>, p);
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out, const int32_t* page_table,
+                          int32_t max_pages, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                          float softmax_scale, void* workspace, int32_t* device_status, int num_sms,
+                          cudaStream_t stream, bool after_kernel) {
+  return launch_decode_fmt<kFmtNvfp4>(c, q, out, page_table, max_pages, seq_lens, batch, num_q_heads, softmax_scale,
+                                      workspace, device_status, num_sms, stream, after_kernel);
+}
+
+cudaError_t launch_decode_variant(int variant, const nvfp4kv_cache& c, const uint16_t* q, float* out,
+                                  const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                                  int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
+                                  int32_t* device_status, int num_sms, cudaStream_t stream) {
+  if (variant == NVFP4KV_VARIANT_HADAMARD)
+    return launch_decode_fmt<kFmtHadamard>(c, q, out, page_table, max_pages, seq_lens, batch, num_q_heads,
+                                           softmax_scale, workspace, device_status, num_sms, stream, false);
+  if (variant == NVFP4KV_VARIANT_MXFP4)
+    return launch_decode_fmt<kFmtMxfp4>(c, q, out, page_table, max_pages, seq_lens, batch, num_q_heads,
+                                        softmax_scale, workspace, device_status, num_sms, stream, false);
+  // stochastic rounding writes the plain NVFP4 format
+  return launch_decode_fmt<kFmtNvfp4>(c, q, out, page_table, max_pages, seq_lens, batch, num_q_heads, softmax_scale,
+                                      workspace, device_status, num_sms, stream, false);
 }
 
 }  // namespace nvfp4kv

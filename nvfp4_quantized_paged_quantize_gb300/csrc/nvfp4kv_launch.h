@@ -93,6 +93,13 @@ cudaError_t launch_stream_probe(const nvfp4kv_cache& c, const int32_t* page_tabl
                                 const int32_t* seq_lens, int32_t batch, int mode, uint32_t* sink,
                                 int32_t* device_status, int num_sms, cudaStream_t stream);
 
+// The decode over a format variant's cache (NVFP4KV_VARIANT_*): SR pages are
+// NVFP4; Hadamard pages hold NVFP4 of rotated rows; MXFP4 its own page-heads.
+cudaError_t launch_decode_variant(int variant, const nvfp4kv_cache& c, const uint16_t* q, float* out,
+                                  const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                                  int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
+                                  int32_t* device_status, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_decode(const nvfp4kv_cache& c, const uint16_t* q, float* out,
                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                           int32_t batch, int32_t num_q_heads, float softmax_scale, void* workspace,
