@@ -12,7 +12,7 @@ import oracle
 import nvfp4_quantized_paged_quantize_gb300 as kv
 from nvfp4_quantized_paged_quantize_gb300 import inputs
 from gpu_util import (bf16_dev, check_rows, decode_gpu, dev, fill_workload_gpu, fill_workload_oracle, gpu_append,
-                      gpu_cache, gpu_global_scales, oracle_global_scales, oracle_pair, pool_host, status_word)
+                      gpu_cache, gpu_global_scales, pool_host, status_word)
 
 pytestmark = pytest.mark.gpu
 
@@ -104,77 +104,6 @@ def test_bad_page_ids_and_lengths_are_flagged_and_skipped(cuda_lib):
                                 device_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & kv.NVFP4KV_DEVERR_LENGTH
-
-
-def _full_size_sampled(index, samples):
-    """Full-size workload through the launch configuration the benchmark times;
-    oracle on sampled (sequence, KV head) pairs, filled from the same inputs."""
-    wl = inputs.decode_config(index)
-    prompts = wl.all_prompt_kv(threads=16)
-    new = wl.new_kv() if wl.append else None
-    q = wl.q()
-    gk, gv = oracle_global_scales(wl, prompts, new)
-    g = fill_workload_gpu(wl, prompts, new)
-    out, _ = decode_gpu(wl, g, q)
-    out = out.cpu().numpy()
-    kd, vd, ks, vs = pool_host(g)
-    G = wl.num_q_heads // wl.num_kv_heads
-    worst = 0.0
-    for b, h in samples:
-        k_seq, v_seq = prompts[b]
-        if wl.append:
-            k_seq = np.concatenate([k_seq, new[0][b:b + 1]])
-            v_seq = np.concatenate([v_seq, new[1][b:b + 1]])
-        ref, oc, npg = oracle_pair(wl, b, h, k_seq, v_seq, q, gk, gv)
-        worst = max(worst, check_rows(out[b, h * G:(h + 1) * G], ref))
-        # the pool rows of this pair are bit-exact too
-        pages = wl.page_table[b, :npg].astype(np.int64)
-        rows = ((pages[:, None] * wl.num_kv_heads + h) * 16 + np.arange(16)[None, :]).reshape(-1)
-        L = k_seq.shape[0]
-        rows = rows[:L]
-        np.testing.assert_array_equal(kd[rows], oc.k_data[:L])
-        np.testing.assert_array_equal(vd[rows], oc.v_data[:L])
-        np.testing.assert_array_equal(ks[rows], oc.k_scale[:L])
-        np.testing.assert_array_equal(vs[rows], oc.v_scale[:L])
-    return worst
-
-
-def test_full_size_decode_b32_ctx8k(cuda_lib):
-    _full_size_sampled(2, [(0, 0), (13, 5), (31, 7)])
-
-
-def test_full_size_decode_b4_ctx128k(cuda_lib):
-    _full_size_sampled(3, [(2, 3)])
-
-
-def test_full_size_ragged_b256(cuda_lib):
-    # 256 sequences of 512..32768 tokens, 32 q / 8 KV heads, a fragmented pool:
-    # the cache is filled one sequence at a time (its bf16 source would not
-    # fit comfortably on the host at once); sampled pairs go to the oracle
-    wl = inputs.decode_config(4)
-    lens = wl.seq_lens
-    samples = [(0, 0), (int(np.argmax(lens)), 3), (int(np.argmin(lens)), 5), (200, 7), (255, 1)]
-    keep = {b for b, _ in samples}
-    new = wl.new_kv()
-    q = wl.q()
-    g = gpu_cache(wl.num_pages, wl.num_kv_heads)
-    kept = {}
-    for b in range(wl.batch):
-        k, v = wl.prompt_kv(b)
-        gpu_append(g, k, v, wl.slots(b, 0, k.shape[0]))
-        if b in keep:
-            kept[b] = (np.concatenate([k, new[0][b:b + 1]]), np.concatenate([v, new[1][b:b + 1]]))
-    gpu_append(g, new[0], new[1], wl.append_slots())
-    st = status_word()
-    out, _ = decode_gpu(wl, g, q, st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
-    out = out.cpu().numpy()
-    G = wl.num_q_heads // wl.num_kv_heads
-    for b, h in samples:
-        k_seq, v_seq = kept[b]
-        ref, _, _ = oracle_pair(wl, b, h, k_seq, v_seq, q, 1.0, 1.0)
-        check_rows(out[b, h * G:(h + 1) * G], ref)
 
 
 @pytest.mark.parametrize("index,scale", [(1, 1.0), (2, 1 / 32), (4, 1 / 32), (3, 1 / 256)])
