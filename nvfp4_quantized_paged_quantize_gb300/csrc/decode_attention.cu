@@ -159,7 +159,21 @@ __device__ __forceinline__ void mma16816_zero(float d[4], uint32_t a0, uint32_t 
 }
 
 __device__ __forceinline__ uint32_t dup_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
-__device__ __forceinline__ uint32_t dup_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
+
+// a * (the low or the high half of s, in both halves): the broadcast is left to
+// the multiply's operand selection
+union H2U {
+  uint32_t u;
+  __half2 h;
+};
+template <bool kHi>
+__device__ __forceinline__ uint32_t hmul2_bcast(uint32_t a, uint32_t s) {
+  H2U x, y, r;
+  x.u = a;
+  y.u = s;
+  r.h = __hmul2(x.h, kHi ? __high2half2(y.h) : __low2half2(y.h));
+  return r.u;
+}
 
 template <int K>
 __device__ __forceinline__ uint32_t cvt_sel(uint32_t w) { return e2m1x2_to_f16x2<K>(w); }
@@ -200,6 +214,7 @@ struct ItemMap {
   int page;    // page index within the sequence
   int np;      // pages of the pair
   int lastnv;  // valid tokens in the pair's last page (1..16)
+  int nv;      // after resolve_chunk: valid tokens of the item's page (0 for an invalid id or past the range)
 };
 
 // The sequence a chunk walk starts from: its index, its first page (in units
@@ -224,6 +239,7 @@ __device__ __forceinline__ ItemMap map_chunk(const DecodeParams& p, long long wr
   m.page = 0;
   m.np = 1;
   m.lastnv = kPage;
+  m.nv = 0;
   const int i = i0 + lane;
   int b = sc.b, cu = sc.cu, L = sc.L;
   if (i < n) {
@@ -259,6 +275,7 @@ __device__ __forceinline__ uint32_t resolve_chunk(const DecodeParams& p, ItemMap
   const bool valid = real && m.row >= 0 && m.row < p.num_pages;
   if (real && !valid) flag_error(p.status, NVFP4KV_DEVERR_PAGE);
   m.row = valid ? m.row * p.hkv + m.h : -1;
+  m.nv = valid ? (m.page == m.np - 1 ? m.lastnv : kPage) : 0;
   return __ballot_sync(0xFFFFFFFFu, valid);
 }
 
@@ -299,17 +316,59 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 template <int F>
 __device__ __forceinline__ void issue_page_cpasync(const LaneCopy& c, int row, uint32_t st, uint32_t bar,
                                                    int lane) {
-  if (row >= 0) {
-    const uint8_t* src = c.src + (size_t)row * ph_bytes(F);
-    const uint32_t dst = st + c.off;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) cp_async16(dst + 512 * k, src + 512 * k);
-    if (c.fifth) cp_async16(dst + 2048, src + 2048);
-  }
-  // fires once all of this lane's earlier copies have landed (also for an
-  // invalid page, which copies nothing): a stage's barrier therefore covers
-  // every stage issued before it as well
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+  // predicated copies (no branch): nothing is copied for an invalid page (row < 0)
+  const uint8_t* src = c.src + (size_t)(row < 0 ? 0 : row) * ph_bytes(F);
+  const uint32_t dst = st + c.off;
+  const uint32_t v5 = (row >= 0 && c.fifth) ? 1u : 0u;
+  asm volatile(
+      "{\n .reg .pred p, q;\n"
+      " setp.ge.s32 p, %2, 0;\n"
+      " setp.ne.u32 q, %3, 0;\n"
+      " @p cp.async.cg.shared.global [%0], [%1], 16;\n"
+      " @p cp.async.cg.shared.global [%0+512], [%1+512], 16;\n"
+      " @p cp.async.cg.shared.global [%0+1024], [%1+1024], 16;\n"
+      " @p cp.async.cg.shared.global [%0+1536], [%1+1536], 16;\n"
+      " @q cp.async.cg.shared.global [%0+2048], [%1+2048], 16;\n"
+      // fires once all of this lane's earlier copies have landed (also for an
+      // invalid page, which copies nothing): a stage's barrier therefore covers
+      // every stage issued before it as well
+      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%4];\n"
+      "}\n" ::"r"(dst), "l"(src), "r"(row), "r"(v5), "r"(bar)
+      : "memory");
+}
+
+// Two NVFP4 page-heads (288 pieces of 16 bytes: 9 per lane), into stages a and
+// b: lane l copies pieces l + 32 k of the pair of page-heads, i.e. a's pieces
+// l, l + 32, l + 64, l + 96, then a's l + 128 (l < 16) or b's l - 16 (l >= 16),
+// then b's l + 16, l + 48, l + 80, l + 112; then arrives on both barriers.
+__device__ __forceinline__ void issue_two_pages(const LaneCopy& c, int ra, int rb, uint32_t sta, uint32_t stb,
+                                                uint32_t bara, uint32_t barb, int lane) {
+  const uint8_t* srca = c.src + (size_t)(ra < 0 ? 0 : ra) * kPageHeadBytes;
+  const uint8_t* srcb = c.src + (size_t)(rb < 0 ? 0 : rb) * kPageHeadBytes;
+  const uint32_t dsta = sta + c.off, dstb = stb + c.off;
+  const bool lo = lane < 16;
+  const uint32_t dst4 = lo ? dsta + 2048 : dstb - 256;
+  const uint8_t* src4 = lo ? srca + 2048 : srcb - 256;
+  const uint32_t v4 = (lo ? ra : rb) >= 0 ? 1u : 0u;
+  asm volatile(
+      "{\n .reg .pred pa, pb, p4;\n"
+      " setp.ge.s32 pa, %4, 0;\n"
+      " setp.ge.s32 pb, %5, 0;\n"
+      " setp.ne.u32 p4, %6, 0;\n"
+      " @pa cp.async.cg.shared.global [%0], [%2], 16;\n"
+      " @pa cp.async.cg.shared.global [%0+512], [%2+512], 16;\n"
+      " @pa cp.async.cg.shared.global [%0+1024], [%2+1024], 16;\n"
+      " @pa cp.async.cg.shared.global [%0+1536], [%2+1536], 16;\n"
+      " @p4 cp.async.cg.shared.global [%7], [%8], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+256], [%3+256], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+768], [%3+768], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+1280], [%3+1280], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+1792], [%3+1792], 16;\n"
+      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%9];\n"
+      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%10];\n"
+      "}\n" ::"r"(dsta), "r"(dstb), "l"(srca), "l"(srcb), "r"(ra), "r"(rb), "r"(v4), "r"(dst4), "l"(src4),
+      "r"(bara), "r"(barb)
+      : "memory");
 }
 
 // Per-warp attention state of the current pair.
@@ -455,7 +514,7 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
     const uint8_t* ks = stage[k] + off_ks(F);
     const uint4 ka = *reinterpret_cast<const uint4*>(kd + g * kRowBytes + 16 * t);
     const uint4 kb = *reinterpret_cast<const uint4*>(kd + (g + 8) * kRowBytes + 16 * t);
-    uint32_t sa0, sa1, sb0, sb1;
+    uint32_t sa, sb;  // f16x2: the scales of blocks 2t (low half) and 2t + 1 (high half) of rows g, g + 8
     if constexpr (F == kFmtMxfp4) {
       // the lane's 32 values of rows g and g + 8 are one block (t); the 64 K
       // scale bytes of the page are read once over the warp, as are V's
@@ -473,12 +532,11 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
       }
       pe[k].kx = exp2_f32(ek - 127);
       pe[k].ve = ev - 127;
-      sa0 = sa1 = dup_lo(exp2_f16_bits(ea - ek));
-      sb0 = sb1 = dup_lo(exp2_f16_bits(eb - ek));
+      sa = dup_lo(exp2_f16_bits(ea - ek));
+      sb = dup_lo(exp2_f16_bits(eb - ek));
     } else {
-      const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t));
-      const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t));
-      sa0 = dup_lo(sa); sa1 = dup_hi(sa); sb0 = dup_lo(sb); sb1 = dup_hi(sb);
+      sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + g * kRowScales + 2 * t));
+      sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + (g + 8) * kRowScales + 2 * t));
       pe[k].kx = 1.0f;
       pe[k].ve = 0;
     }
@@ -491,8 +549,13 @@ __device__ __forceinline__ void qk_phase(const uint8_t* const (&stage)[NP], cons
       } else {
         a0 = cvt_sel<0>(wa); a1 = cvt_sel<0>(wb); a2 = cvt_sel<1>(wa); a3 = cvt_sel<1>(wb);
       }
-      const uint32_t s_g = i < 4 ? sa0 : sa1, s_g8 = i < 4 ? sb0 : sb1;
-      a0 = hmul2(a0, s_g); a2 = hmul2(a2, s_g); a1 = hmul2(a1, s_g8); a3 = hmul2(a3, s_g8);
+      if (i < 4) {
+        a0 = hmul2_bcast<false>(a0, sa); a2 = hmul2_bcast<false>(a2, sa);
+        a1 = hmul2_bcast<false>(a1, sb); a3 = hmul2_bcast<false>(a3, sb);
+      } else {
+        a0 = hmul2_bcast<true>(a0, sa); a2 = hmul2_bcast<true>(a2, sa);
+        a1 = hmul2_bcast<true>(a1, sb); a3 = hmul2_bcast<true>(a3, sb);
+      }
       // chain c = i / 4 (two chains) or 0: its first MMA starts from zero
       const int c = NVFP4KV_DECODE_QK_CHAINS == 2 ? (i >> 2) : 0;
       if (i == 0 || (NVFP4KV_DECODE_QK_CHAINS == 2 && i == 4))
@@ -912,100 +975,120 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     load_q<F>(p, q_first, s, g, t);  // the first piece's q, fetched before the prefill
     int nseg = 0;
     int i = 0;
+    // the chunk maps hold items [32 chunk, 32 chunk + 64): move them up to item k
+#define NVFP4KV_ADVANCE_TO(k)                                   \
+  while (((k) >> 5) != chunk) {                                 \
+    if (!nres) vnxt = resolve_chunk(p, nxt);                    \
+    cur = nxt;                                                  \
+    vcur = vnxt;                                                \
+    ++chunk;                                                    \
+    nres = true;                                                \
+    if ((chunk + 1) * 32 < n) {                                 \
+      nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, seq, lane);  \
+      nres = false;                                             \
+    }                                                           \
+  }
+    // a field of item k (k in the two mapped chunks)
+#define NVFP4KV_ITEM(field, k) __shfl_sync(0xFFFFFFFFu, ((k) >> 5) == chunk ? cur.field : nxt.field, (k) & 31)
     while (i < n) {
       // ---- one piece: items [i, iend) of one (sequence, KV head) pair -------------
-      while ((i >> 5) != chunk) {
-        if (!nres) vnxt = resolve_chunk(p, nxt);
-        cur = nxt;
-        vcur = vnxt;
-        ++chunk;
-        nres = true;
-        if ((chunk + 1) * 32 < n) {
-          nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, seq, lane);
-          nres = false;
-        }
-      }
+      NVFP4KV_ADVANCE_TO(i)
       const int li = i & 31;
       const int pair = __shfl_sync(0xFFFFFFFFu, cur.pair, li);
       const int page0 = __shfl_sync(0xFFFFFFFFu, cur.page, li);
       const int np = __shfl_sync(0xFFFFFFFFu, cur.np, li);
-      const int lastnv = __shfl_sync(0xFFFFFFFFu, cur.lastnv, li);
       const int iend = min(n, i + (np - page0));
       const long long piece_r = wr0 + i;
       ++nseg;
       if (nseg > 1) load_q<F>(p, fetch_q(p, pair, g, t), s, g, t);
-      for (int j = i; j < iend;) {
-        if ((j >> 5) != chunk) {
-          if (!nres) vnxt = resolve_chunk(p, nxt);
-          cur = nxt;
-          vcur = vnxt;
-          ++chunk;
-          nres = true;
-          if ((chunk + 1) * 32 < n) {
-            nxt = map_chunk(p, wr0, (chunk + 1) * 32, n, seq, lane);
-            nres = false;
-          }
-        }
+      int j = i;
+      // two pages per step
+      for (; j + 1 < iend; j += 2) {
+        NVFP4KV_ADVANCE_TO(j)
         // the next chunk's rows are first needed at item 32 chunk + 32 - kStages - 1;
         // resolving them half way through the chunk leaves their loads time to land
         if (!nres && (j & 31) >= 16) {
           vnxt = resolve_chunk(p, nxt);
           nres = true;
         }
-        const bool two = j + 1 < iend;
         const int st1 = st + 1 == kStages ? 0 : st + 1;
-        const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
+        const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
         if (ok) {
           // every lane waits; the outcome is made warp-uniform before it is used.
           // The second stage's barrier fires only after each lane's earlier copies
           // (those of the first stage) have landed too, so one wait covers both.
-          const bool done = two ? mbar_wait(wbar + 8 * st1, ph1) : mbar_wait(wbar + 8 * st, ph);
-          if (!__all_sync(0xFFFFFFFFu, done)) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(wbar + 8 * st1, ph1))) {
             ok = false;
             if (lane == 0) flag_error(p.status, kDevErrTimeout);
           }
         }
         if (ok) {
-          // a page with an invalid id, or a missing second page, has no valid tokens
-          const int pg = page0 + (j - i);
-          const uint32_t vm0 = vcur, vm1 = ((j + 1) >> 5) == chunk ? vcur : vnxt;
-          const int nv0 = ((vm0 >> (j & 31)) & 1u) ? (pg == np - 1 ? lastnv : kPage) : 0;
-          const int nv1 = (two && ((vm1 >> ((j + 1) & 31)) & 1u)) ? (pg + 1 == np - 1 ? lastnv : kPage) : 0;
-          const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + (two ? st1 : st) * kStageBytes};
+          const int nv0 = __shfl_sync(0xFFFFFFFFu, cur.nv, j & 31);
+          const int nv1 = NVFP4KV_ITEM(nv, j + 1);
+          const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + st1 * kStageBytes};
           const int nvs[2] = {nv0, nv1};
           if ((nv0 & nv1) == kPage)
             process_pages<2, true, F>(stg, nvs, s, g, t);
           else if (nv0 | nv1)
             process_pages<2, false, F>(stg, nvs, s, g, t);
           __syncwarp();
-          // refill the freed stages with items j + kStages (and j + 1 + kStages)
-          const int ja = j + kStages, jb = j + 1 + kStages;
-          if (ja < n) {
-            const int ra = item_row(cur, nxt, ja, chunk);
-            issue_page_cpasync<F>(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+          // refill the freed stages with items j + kStages and j + 1 + kStages
+          const int ja = j + kStages, jb = ja + 1;
+          if (jb < n) {
+            const int ra = NVFP4KV_ITEM(row, ja);
+            const int rb = NVFP4KV_ITEM(row, jb);
+            if constexpr (F == kFmtMxfp4) {
+              issue_page_cpasync<F>(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+              issue_page_cpasync<F>(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
+            } else {
+              issue_two_pages(lc, ra, rb, wring_u32 + st * kStageBytes, wring_u32 + st1 * kStageBytes,
+                              wbar + 8 * st, wbar + 8 * st1, lane);
+            }
+            issued = jb + 1;
+          } else if (ja < n) {
+            issue_page_cpasync<F>(lc, NVFP4KV_ITEM(row, ja), wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
             issued = ja + 1;
           }
-          if (two && jb < n) {
-            const int rb = item_row(cur, nxt, jb, chunk);
-            issue_page_cpasync<F>(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
-            issued = jb + 1;
+        }
+        st = st1 + 1 == kStages ? 0 : st1 + 1;
+        ph = st == 0 ? ph1 ^ 1u : ph1;
+      }
+      if (j < iend) {
+        // the piece's last page on its own
+        NVFP4KV_ADVANCE_TO(j)
+        if (!nres && (j & 31) >= 16) {
+          vnxt = resolve_chunk(p, nxt);
+          nres = true;
+        }
+        if (ok) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(wbar + 8 * st, ph))) {
+            ok = false;
+            if (lane == 0) flag_error(p.status, kDevErrTimeout);
           }
         }
-        if (two) {
-          st = st1 + 1 == kStages ? 0 : st1 + 1;
-          ph = st1 + 1 == kStages ? ph1 ^ 1u : ph1;
-          j += 2;
-        } else {
-          st = st1;
-          ph = ph1;
-          j += 1;
+        if (ok) {
+          const int nv0 = __shfl_sync(0xFFFFFFFFu, cur.nv, j & 31);
+          const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + st * kStageBytes};
+          const int nvs[2] = {nv0, 0};
+          if (nv0) process_pages<2, false, F>(stg, nvs, s, g, t);
+          __syncwarp();
+          const int ja = j + kStages;
+          if (ja < n) {
+            issue_page_cpasync<F>(lc, NVFP4KV_ITEM(row, ja), wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            issued = ja + 1;
+          }
         }
+        st = st + 1 == kStages ? 0 : st + 1;
+        ph = st == 0 ? ph ^ 1u : ph;
+        ++j;
       }
+#undef NVFP4KV_ITEM
+#undef NVFP4KV_ADVANCE_TO
       if (iend == n && !ok) {
         // drain: wait (bounded) for every copy still in flight before the ring is reused
-        for (int j = issued - kStages; j < issued; ++j) {
-          if (j < 0) continue;
-          mbar_wait(wbar + 8 * (j % kStages), (uint32_t)((j / kStages) & 1));
+        for (int jj = issued - kStages; jj < issued; ++jj) {
+          if (jj < 0) continue;
+          mbar_wait(wbar + 8 * (jj % kStages), (uint32_t)((jj / kStages) & 1));
         }
       }
       __syncwarp();
