@@ -27,7 +27,11 @@
  *                             low nibble of byte i
  *     [1024, 1152)  K scales  16 rows x 8 E4M3 bytes; scale j covers elements
  *                             16j..16j+15 of the row
- *     [1152, 2176)  V data    as K
+ *     [1152, 2176)  V data    by token pair: 8 rows x 128 bytes; byte d of
+ *                             row p holds element d of token 2p in its low
+ *                             nibble and element d of token 2p + 1 in its
+ *                             high nibble (the decode's P.V product pairs
+ *                             two tokens of one element)
  *     [2176, 2304)  V scales  block-major: 8 blocks x 16 tokens, the scale of
  *                             block j of row r at 2176 + 16 j + r
  * A slot s is row (s % page_size) of page (s / page_size).  Supported:
@@ -95,8 +99,8 @@ enum {
 #define NVFP4KV_PAGE_HEAD_BYTES 2304
 /* Bytes of one page-head of the MXFP4 variant's pool (4 E8M0 scale bytes per
  * row): K data [0, 1024), K scales [1024, 1088) token-major, V data
- * [1088, 2112), V scales [2112, 2176) block-major (block j of row r at
- * 2112 + 16 j + r). */
+ * [1088, 2112) by token pair as in the NVFP4 page-head, V scales
+ * [2112, 2176) block-major (block j of row r at 2112 + 16 j + r). */
 #define NVFP4KV_MXFP4_PAGE_HEAD_BYTES 2176
 
 /* One layer's paged NVFP4 cache.  The struct itself is read on the host only. */
@@ -132,7 +136,10 @@ int nvfp4kv_cache_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t head_di
  *                 pool skips the token and raises NVFP4KV_DEVERR_SLOT
  *   num_tokens    >= 0 (0 enqueues nothing)
  * K uses cache->k_global_scale and V uses cache->v_global_scale.  Two tokens
- * mapped to one slot race (unspecified which one lands).
+ * mapped to one slot race: that row's bytes are unspecified (they may mix
+ * the two tokens).  Any other slot mapping is exact, including the two tokens
+ * of a pair of rows (2m, 2m + 1) written by different calls or in any order
+ * within one call.
  */
 int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const void* v,
                             const int64_t* slot_mapping, int64_t num_tokens,

@@ -155,10 +155,14 @@ class Cache:
     order (include/nvfp4kv.h).  With mxfp4=True the pool holds the MXFP4
     variant's page-heads of 2176 bytes (4 E8M0 scale bytes per row).
 
-    k_data / v_data ([num_pages, num_kv_heads, 16, 64]) and k_scale / v_scale
+    k_data ([num_pages, num_kv_heads, 16, 64]) and k_scale / v_scale
     ([num_pages, num_kv_heads, 16, 8], or 4 for MXFP4) are views of the pool,
     indexed [page, head, token row, block] (V scales are stored block-major;
-    their view is transposed).
+    their view is transposed).  V data is stored by token pair: v_pairs
+    ([num_pages, num_kv_heads, 8, 128]) is the view of it, byte d of pair row p
+    holding dimension d of token 2p (low nibble) and of token 2p + 1 (high
+    nibble).  v_data is a copy in K's row layout ([..., 16, 64], value 2j of a
+    row in the low nibble of byte j), and set_v_data writes one.
     """
     pages: object
     num_pages: int
@@ -185,9 +189,9 @@ class Cache:
         sc = PAGE_SIZE * (HEAD_DIM // (32 if self.mxfp4 else 16))
         return (0, d), (d, d + sc), (d + sc, 2 * d + sc), (2 * d + sc, 2 * d + 2 * sc)
 
-    def _view(self, part, row_bytes):
+    def _view(self, part, row_bytes, rows=PAGE_SIZE):
         lo, hi = self._parts()[part]
-        return self.pages[:, :, lo:hi].unflatten(-1, (PAGE_SIZE, row_bytes))
+        return self.pages[:, :, lo:hi].unflatten(-1, (rows, row_bytes))
 
     @property
     def k_data(self):
@@ -198,8 +202,25 @@ class Cache:
         return self._view(1, HEAD_DIM // (32 if self.mxfp4 else 16))
 
     @property
+    def v_pairs(self):
+        return self._view(2, HEAD_DIM, PAGE_SIZE // 2)
+
+    @property
     def v_data(self):
-        return self._view(2, HEAD_DIM // 2)
+        import torch
+
+        raw = self.v_pairs                                     # [P, H, 8, 128]: tokens 2p, 2p + 1
+        nib = torch.stack((raw & 15, raw >> 4), dim=-2)         # [P, H, 8, 2, 128]
+        nib = nib.reshape(*raw.shape[:2], PAGE_SIZE, HEAD_DIM)  # [P, H, 16, 128]: token, dimension
+        return nib[..., 0::2] | (nib[..., 1::2] << 4)
+
+    def set_v_data(self, rows):
+        """Write V data given in K's row layout ([P, H, 16, 64] uint8, on the pool's device)."""
+        import torch
+
+        nib = torch.stack((rows & 15, rows >> 4), dim=-1)       # [P, H, 16, 64, 2]
+        nib = nib.reshape(*rows.shape[:2], PAGE_SIZE // 2, 2, HEAD_DIM)
+        self.v_pairs.copy_(nib[..., 0, :] | (nib[..., 1, :] << 4))
 
     @property
     def v_scale(self):

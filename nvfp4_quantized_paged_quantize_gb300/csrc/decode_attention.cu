@@ -22,7 +22,8 @@
 //      raised when a score exceeds it by more than 8, so the rescale of the
 //      accumulators is rare;
 //   3. transposes P (f16) with movmatrix and accumulates O^T += Vhat^T P^T,
-//      Vhat^T built from nibble-interleaved V bytes and scaled per token.
+//      Vhat^T converted straight from V's token-pair bytes (each byte one
+//      dimension of two tokens) and scaled per token.
 // A (sequence, KV head) pair that lies inside one warp range is finished by
 // that warp.  A piece of a pair cut by a warp boundary is written to the
 // workspace as a record (unnormalised O, running max m, sum l) and the warp
@@ -279,16 +280,6 @@ __device__ __forceinline__ uint32_t resolve_chunk(const DecodeParams& p, ItemMap
   return __ballot_sync(0xFFFFFFFFu, valid);
 }
 
-// The row (physical page-head) of item j, from the chunk map that holds it.
-__device__ __forceinline__ int item_row(const ItemMap& cur, const ItemMap& nxt, int j, int i_chunk) {
-  int r;
-  if ((j >> 5) == i_chunk)
-    r = __shfl_sync(0xFFFFFFFFu, cur.row, j & 31);
-  else
-    r = __shfl_sync(0xFFFFFFFFu, nxt.row, j & 31);
-  return r;
-}
-
 // cp.async staging: lane l copies the 16-byte pieces l, l + 32, ... of the
 // page-head (NVFP4: lanes 0-15 five of the 144, the others four; MXFP4: lanes
 // 0-7 five of the 136), then arrives (no-increment) on the stage's mbarrier,
@@ -307,10 +298,6 @@ __device__ __forceinline__ LaneCopy lane_copy(const DecodeParams& p, int lane) {
   c.off = 16u * lane;
   c.fifth = lane + 128 < ph_bytes(F) / 16;
   return c;
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 template <int F>
@@ -674,36 +661,31 @@ __device__ __forceinline__ void pv_phase(const uint8_t* const (&stage)[NP], cons
       sv01 = e4m3x2_to_f16x2(p01);
       sv89 = e4m3x2_to_f16x2(p89);
     }
-    const uint2 d0 = *reinterpret_cast<const uint2*>(vd + t0 * kRowBytes + 8 * g);
-    const uint2 d1 = *reinterpret_cast<const uint2*>(vd + t1 * kRowBytes + 8 * g);
-    const uint2 d8 = *reinterpret_cast<const uint2*>(vd + t8 * kRowBytes + 8 * g);
-    const uint2 d9 = *reinterpret_cast<const uint2*>(vd + t9 * kRowBytes + 8 * g);
-    // interleave nibbles of two tokens: byte j of lo = (even d of token a, even d of token b)
-    const uint32_t lo01a = (d0.x & 0x0F0F0F0Fu) | ((d1.x << 4) & 0xF0F0F0F0u);
-    const uint32_t hi01a = ((d0.x >> 4) & 0x0F0F0F0Fu) | (d1.x & 0xF0F0F0F0u);
-    const uint32_t lo01b = (d0.y & 0x0F0F0F0Fu) | ((d1.y << 4) & 0xF0F0F0F0u);
-    const uint32_t hi01b = ((d0.y >> 4) & 0x0F0F0F0Fu) | (d1.y & 0xF0F0F0F0u);
-    const uint32_t lo89a = (d8.x & 0x0F0F0F0Fu) | ((d9.x << 4) & 0xF0F0F0F0u);
-    const uint32_t hi89a = ((d8.x >> 4) & 0x0F0F0F0Fu) | (d9.x & 0xF0F0F0F0u);
-    const uint32_t lo89b = (d8.y & 0x0F0F0F0Fu) | ((d9.y << 4) & 0xF0F0F0F0u);
-    const uint32_t hi89b = ((d8.y >> 4) & 0x0F0F0F0Fu) | (d9.y & 0xF0F0F0F0u);
+    // V data by token pair: pair t holds tokens (2t, 2t+1), pair t + 4 tokens
+    // (2t+8, 2t+9); bytes 16g .. 16g + 15 of a pair row are dimensions 16g ..
+    // 16g + 15, each byte the two tokens' codes of one dimension: one E2M1
+    // conversion gives an A-operand register (k = the two tokens) as it is
+    const uint4 w01 = *reinterpret_cast<const uint4*>(vd + t * kVPairBytes + 16 * g);
+    const uint4 w89 = *reinterpret_cast<const uint4*>(vd + (t + 4) * kVPairBytes + 16 * g);
     const uint32_t pb0 = pb[k][0], pb1 = pb[k][1];
-#define NVFP4KV_PV_TILE(I, LO01, HI01, LO89, HI89, K)                                   \
-  {                                                                                     \
-    const uint32_t a0 = hmul2(cvt_sel<K>(LO01), sv01);                                  \
-    const uint32_t a1 = hmul2(cvt_sel<K>(HI01), sv01);                                  \
-    const uint32_t a2 = hmul2(cvt_sel<K>(LO89), sv89);                                  \
-    const uint32_t a3 = hmul2(cvt_sel<K>(HI89), sv89);                                  \
-    mma16816(s.o[I], a0, a1, a2, a3, pb0, pb1);                                         \
+    // tile I: rows g and g + 8 are dimensions 16g + 2I and 16g + 2I + 1, bytes
+    // 2I and 2I + 1 of the lane's 16
+#define NVFP4KV_PV_TILE(I, W01, W89, K0, K1)                                    \
+  {                                                                             \
+    const uint32_t a0 = hmul2(cvt_sel<K0>(W01), sv01);                          \
+    const uint32_t a1 = hmul2(cvt_sel<K1>(W01), sv01);                          \
+    const uint32_t a2 = hmul2(cvt_sel<K0>(W89), sv89);                          \
+    const uint32_t a3 = hmul2(cvt_sel<K1>(W89), sv89);                          \
+    mma16816(s.o[I], a0, a1, a2, a3, pb0, pb1);                                 \
   }
-    NVFP4KV_PV_TILE(0, lo01a, hi01a, lo89a, hi89a, 0)
-    NVFP4KV_PV_TILE(1, lo01a, hi01a, lo89a, hi89a, 1)
-    NVFP4KV_PV_TILE(2, lo01a, hi01a, lo89a, hi89a, 2)
-    NVFP4KV_PV_TILE(3, lo01a, hi01a, lo89a, hi89a, 3)
-    NVFP4KV_PV_TILE(4, lo01b, hi01b, lo89b, hi89b, 0)
-    NVFP4KV_PV_TILE(5, lo01b, hi01b, lo89b, hi89b, 1)
-    NVFP4KV_PV_TILE(6, lo01b, hi01b, lo89b, hi89b, 2)
-    NVFP4KV_PV_TILE(7, lo01b, hi01b, lo89b, hi89b, 3)
+    NVFP4KV_PV_TILE(0, w01.x, w89.x, 0, 1)
+    NVFP4KV_PV_TILE(1, w01.x, w89.x, 2, 3)
+    NVFP4KV_PV_TILE(2, w01.y, w89.y, 0, 1)
+    NVFP4KV_PV_TILE(3, w01.y, w89.y, 2, 3)
+    NVFP4KV_PV_TILE(4, w01.z, w89.z, 0, 1)
+    NVFP4KV_PV_TILE(5, w01.z, w89.z, 2, 3)
+    NVFP4KV_PV_TILE(6, w01.w, w89.w, 0, 1)
+    NVFP4KV_PV_TILE(7, w01.w, w89.w, 2, 3)
 #undef NVFP4KV_PV_TILE
   }
 }

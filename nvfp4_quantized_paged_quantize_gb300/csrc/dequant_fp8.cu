@@ -5,10 +5,15 @@
 //   ws[cu_prefix[b] + t][h][d] = E4M3(fp32(fp32(e2m1 * E4M3val(sb)) * g) / s_ws)
 //
 // One warp converts one page-head (16 rows of one KV head of one sequence) of
-// K or of V: lane l loads row l / 2, values [64 (l % 2), 64 (l % 2) + 64) --
-// two 16-byte data loads and one 4-byte scale load, the warp reading the
-// page-head's 1 KiB of data contiguously -- then trades blocks with the row's
-// other lane so that each store of the pair fills a 32-byte sector.
+// K or of V, reading its 1 KiB of data contiguously.  K: lane l loads row
+// l / 2, values [64 (l % 2), 64 (l % 2) + 64) -- two 16-byte data loads and
+// one 4-byte scale load -- then trades blocks with the row's other lane so
+// that each store of the pair fills a 32-byte sector.  V (stored by token
+// pair): lane l loads dimensions [32 (l % 4), 32 (l % 4) + 32) of token pair
+// l / 4, each byte one dimension of both tokens, which one conversion turns
+// into the two tokens' values (lane l takes blocks l % 4 and l % 4 + 4, so
+// that the four lanes of a pair fill 64 contiguous bytes of each output row
+// with each store); the two tokens' scales of a block are one 16-bit load.
 // The page-table lookup and the row arithmetic are done once per page-head; a
 // block takes four page-heads (K and V warps), and the grid holds every block,
 // so the block scheduler keeps each SM full of independent loads.  With g = s_ws = 1 the product e2m1 * E4M3val(sb) is exact
@@ -114,13 +119,13 @@ __device__ __forceinline__ void convert_half_row(const uint4& d0, const uint4& d
   }
 }
 
-// Unit scales fit 32 registers (full occupancy); the general path keeps 40.
+// Unit scales fit 32 registers (full occupancy); the general path takes up to 48
+// (no spills).
 template <bool kUnit>
-__global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(DequantParams p) {
+__global__ void __launch_bounds__(kThreads, kUnit ? 8 : 5) dequant_fp8_kernel(DequantParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tensor = warp & 1;  // 0: K, 1: V
   const int r = lane >> 1, half = lane & 1;
-  const int off_data = tensor ? kOffVData : kOffKData;  // within a page-head
   uint8_t* ws = tensor ? p.ws_v : p.ws_k;
   const float g = tensor ? p.gv : p.gk, sws = tensor ? p.sv : p.sk, rs = tensor ? p.rsv : p.rsk;
   const bool fast = tensor ? p.sv_fast : p.sk_fast;
@@ -141,17 +146,59 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(De
     if (pg * kPage >= L) continue;  // a page past this prefix
     const bool page_ok = page >= 0 && page < p.num_pages;
     const uint8_t* phd = p.pages + ((int64_t)(page_ok ? page : 0) * p.hkv + h) * kPageHeadBytes;
-    const uint4* src = reinterpret_cast<const uint4*>(phd + off_data + r * kRowBytes) + 2 * half;
-    const uint4 d0 = __ldg(src), d1 = __ldg(src + 1);  // blocks 4 half .. 4 half + 3
-    // the scales of blocks 4 half .. 4 half + 3 of row r (K: 4 adjacent bytes; V: block-major, 16 apart)
-    uint32_t sc4;
-    if (tensor == 0) {
-      sc4 = __ldg(reinterpret_cast<const uint32_t*>(phd + k_scale_offset(r, 4 * half)));
-    } else {
-      sc4 = 0;
+    if (tensor == 1) {
+      // V: token pair q = lane / 4, blocks c and c + 4 (dimensions 16 c .., 64 + 16 c ..)
+      const int q = lane >> 2, c = lane & 3;
+      const int te = pg * kPage + 2 * q;  // the pair's tokens te, te + 1 of the prefix
+      const int64_t orow = base + te;
+      const bool live_e = te < L && orow >= 0 && orow < p.total_rows;
+      const bool live_o = te + 1 < L && orow + 1 >= 0 && orow + 1 < p.total_rows;
+      uint4* dst_e = reinterpret_cast<uint4*>(ws + (orow * p.hkv + h) * kHeadDim) + c;
+      uint4* dst_o = reinterpret_cast<uint4*>(ws + ((orow + 1) * p.hkv + h) * kHeadDim) + c;
+      if (!page_ok) {
+        if (lane == 0) flag_error(p.status, NVFP4KV_DEVERR_PAGE);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        if (live_e) dst_e[0] = dst_e[4] = z;
+        if (live_o) dst_o[0] = dst_o[4] = z;
+        continue;
+      }
+      if (!live_e && !live_o) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(phd + kOffVData + q * kVPairBytes) + c;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) sc4 |= (uint32_t)__ldg(phd + v_scale_offset(r, 4 * half + k)) << (8 * k);
+      for (int hb = 0; hb < 2; ++hb) {
+        // block c + 4 hb: 16 bytes, and the (token te, token te + 1) scales as f16x2
+        const uint4 d = __ldg(src + 4 * hb);
+        const uint32_t sc =
+            e4m3x2_to_f16x2(__ldg(reinterpret_cast<const uint16_t*>(phd + v_scale_offset(2 * q, c + 4 * hb))));
+        const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+        uint32_t oe[4], oo[4];  // the two tokens' output bytes, 4 dimensions per word
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t r[4];  // dimension 4k + i of the block: low byte token te, high byte token te + 1
+          if constexpr (kUnit) {
+            r[0] = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<0>(w[k]), sc));
+            r[1] = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<1>(w[k]), sc));
+            r[2] = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<2>(w[k]), sc));
+            r[3] = e4m3x2_from_f16x2(hmul2(e2m1x2_to_f16x2<3>(w[k]), sc));
+          } else {
+            r[0] = convert_pair_general<0>(w[k], sc, g, sws, rs, fast);
+            r[1] = convert_pair_general<1>(w[k], sc, g, sws, rs, fast);
+            r[2] = convert_pair_general<2>(w[k], sc, g, sws, rs, fast);
+            r[3] = convert_pair_general<3>(w[k], sc, g, sws, rs, fast);
+          }
+          const uint32_t x01 = r[0] | (r[1] << 16), x23 = r[2] | (r[3] << 16);
+          oe[k] = __byte_perm(x01, x23, 0x6420);
+          oo[k] = __byte_perm(x01, x23, 0x7531);
+        }
+        if (live_e) dst_e[4 * hb] = make_uint4(oe[0], oe[1], oe[2], oe[3]);
+        if (live_o) dst_o[4 * hb] = make_uint4(oo[0], oo[1], oo[2], oo[3]);
+      }
+      continue;
     }
+    const uint4* src = reinterpret_cast<const uint4*>(phd + kOffKData + r * kRowBytes) + 2 * half;
+    const uint4 d0 = __ldg(src), d1 = __ldg(src + 1);  // blocks 4 half .. 4 half + 3
+    // the scales of blocks 4 half .. 4 half + 3 of row r: 4 adjacent bytes
+    const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(phd + k_scale_offset(r, 4 * half)));
     const int t = pg * kPage + r;   // this lane's token of the prefix
     const int64_t orow = base + t;  // its workspace row
     const bool live = t < L && orow >= 0 && orow < p.total_rows;
@@ -159,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 6) dequant_fp8_kernel(De
     // two lanes of a row fill whole 32-byte sectors with each store
     uint4* dst = reinterpret_cast<uint4*>(ws + (orow * p.hkv + h) * kHeadDim) + half;
     if (!page_ok) {
-      if (lane == 0 && tensor == 0) flag_error(p.status, NVFP4KV_DEVERR_PAGE);
+      if (lane == 0) flag_error(p.status, NVFP4KV_DEVERR_PAGE);
       if (live) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll

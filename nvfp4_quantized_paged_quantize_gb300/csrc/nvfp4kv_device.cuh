@@ -25,9 +25,15 @@ constexpr int kDevErrTimeout = 8;                      // a bounded wait gave up
 
 // One page-head (16 tokens of one KV head) of the pool: K data, K scales,
 // V data, V scales, contiguous; the page-heads of a page follow one another.
-// K scales are token-major (the 8 scales of a token row together), V scales
-// block-major (the 16 tokens' scales of one 16-value block together): the
-// decode reads K scales by token and V scales by token pair within a block.
+// K data is token-major: 16 rows of 64 bytes, value 2k of a row in the low
+// nibble of its byte k.  V data is stored by token pair: 8 rows of 128
+// bytes, byte d of row p holding dimension d of token 2p (low nibble) and of
+// token 2p + 1 (high nibble) -- the decode's P.V product contracts over
+// tokens, and its f16 operands pair two tokens of one dimension, which one
+// E2M1 conversion of such a byte gives directly.  K scales are token-major
+// (the 8 scales of a token row together), V scales block-major (the 16
+// tokens' scales of one 16-value block together): the decode reads K scales
+// by token and V scales by token pair within a block.
 constexpr int kOffKData = 0;
 constexpr int kOffKScale = kPageDataBytes;                        // 1024
 constexpr int kOffVData = kPageDataBytes + kPageScaleBytes;       // 1152
@@ -41,6 +47,8 @@ constexpr int kMxOffVData = kPageDataBytes + kPage * kMxRowScales;  // 1088
 constexpr int kMxOffVScale = 2 * kPageDataBytes + kPage * kMxRowScales;  // 2112
 constexpr int kMxPageHeadBytes = 2 * (kPageDataBytes + kPage * kMxRowScales);  // 2176
 static_assert(kMxPageHeadBytes == NVFP4KV_MXFP4_PAGE_HEAD_BYTES, "MXFP4 page-head size");
+
+constexpr int kVPairBytes = 2 * kRowBytes;  // 128: one token pair of V data
 
 // Byte offset, within a page-head, of the scale of block j of token row r.
 __host__ __device__ constexpr int k_scale_offset(int r, int j) { return kOffKScale + r * kRowScales + j; }
@@ -119,6 +127,47 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// ---------------------------------------------------------------------------
+// V data by token pair
+// ---------------------------------------------------------------------------
+
+// Eight E2M1 codes of token 2p (e: value i in nibble i) and the same eight
+// values of token 2p + 1 (o) -> the 8 bytes of the pair row, in value order
+// (byte i: value i of e in the low nibble, of o in the high one).
+__device__ __forceinline__ uint2 v_pair_bytes(uint32_t e, uint32_t o) {
+  const uint32_t ev = (e & 0x0F0F0F0Fu) | ((o << 4) & 0xF0F0F0F0u);         // byte k: values 2k
+  const uint32_t od = ((e >> 4) & 0x0F0F0F0Fu) | (o & 0xF0F0F0F0u);         // byte k: values 2k + 1
+  return make_uint2(__byte_perm(ev, od, 0x5140), __byte_perm(ev, od, 0x7362));
+}
+
+// Store one 16-value block (codes lo: values 0-7, hi: 8-15) of both tokens of
+// a pair (e: token 2p, o: token 2p + 1) at block j of pair row p of V data.
+__device__ __forceinline__ void v_store_block_pair(uint8_t* vdata, int p, int j, uint32_t elo, uint32_t ehi,
+                                                   uint32_t olo, uint32_t ohi) {
+  const uint2 a = v_pair_bytes(elo, olo), b = v_pair_bytes(ehi, ohi);
+  reinterpret_cast<uint4*>(vdata + p * kVPairBytes)[j] = make_uint4(a.x, a.y, b.x, b.y);
+}
+
+// Store one 16-value block of token row r alone: its nibbles of the 16 bytes,
+// leaving the other token's (which another thread may be writing in the same
+// launch) untouched.  Each word gets XORed with the difference between the
+// codes it holds and the new ones, restricted to this token's nibbles, so
+// concurrent updates of the two tokens of a pair commute.
+__device__ __forceinline__ void v_store_block_one(uint8_t* vdata, int r, int j, uint32_t lo, uint32_t hi) {
+  const bool odd = r & 1;
+  const uint2 a = odd ? v_pair_bytes(0u, lo) : v_pair_bytes(lo, 0u);
+  const uint2 b = odd ? v_pair_bytes(0u, hi) : v_pair_bytes(hi, 0u);
+  const uint32_t mask = odd ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+  uint32_t* w = reinterpret_cast<uint32_t*>(vdata + (r >> 1) * kVPairBytes + 16 * j);
+  const uint4 old = __ldcg(reinterpret_cast<const uint4*>(w));
+  const uint32_t nw[4] = {a.x, a.y, b.x, b.y}, ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t d = (nw[k] ^ ow[k]) & mask;
+    if (d) atomicXor(w + k, d);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // shared memory and mbarriers

@@ -2,17 +2,22 @@
 // paged cache ("nvfp4-kv-cache-memory-wall", section 3: new K/V are quantised
 // to NVFP4 on the way into the cache; section 2: two-level scaling).
 //
-// One lane quantises one 16-value block (two 16-byte loads): a warp takes two
-// (token, KV head) rows of K (lanes 0-7 and 8-15) and the same two rows of V
-// (lanes 16-23 and 24-31) per step, so the per-block work (amax, the scale's
-// division, the reciprocal) is done once per block.  Per block:
+// One lane quantises one 16-value block (two 16-byte loads).  Per step a warp
+// takes two (token, KV head) rows of K (lanes 0-7 and 8-15) and the two
+// tokens of a token pair of one KV head of V (lanes 16-23: token 2q, lanes
+// 24-31: token 2q + 1), so the per-block work (amax, the scale's division,
+// the reciprocal) is done once per block.  Per block:
 //   amax = max |x|                       (exact; inputs are bf16)
 //   sb   = E4M3(amax / (6 g))            (correctly rounded quotient, RNE, saturating)
 //   den  = E4M3val(sb) * g
 //   code = E2M1(x / den)                 (correctly rounded quotient, RNE, saturating)
-// A block with den == 0 stores signed zeros.  The row's 64 data bytes and 8
-// scale bytes go to slot slot_mapping[token]: row slot % 16 of the K (or V)
-// part of the page-head (slot / 16, head).  HBM-bound: 2 B read and 9/16 B
+// A block with den == 0 stores signed zeros.  A token's codes and scales go
+// to slot slot_mapping[token]: row slot % 16 of the page-head (slot / 16,
+// head).  V data is stored by token pair (byte d of pair row p: dimension d of
+// tokens 2p and 2p + 1): when the two tokens of a step land in the two rows
+// of one pair row (the usual case: consecutive slots from an even one), one
+// lane writes both tokens' bytes; otherwise each token's nibbles are merged
+// into their bytes with atomic XORs.  HBM-bound: 2 B read and 9/16 B
 // written per value.
 #include "fp8_quotient.cuh"
 #include "nvfp4kv_device.cuh"
@@ -26,6 +31,7 @@ struct QuantParams {
   const uint16_t* v;
   const int64_t* slots;
   int32_t rows;  // num_tokens * num_kv_heads (< 2^31, checked on the host)
+  int32_t ntok;  // num_tokens
   int32_t hkv;
   int64_t capacity;  // num_pages * page_size
   uint8_t* pages;  // [num_pages][hkv][kPageHeadBytes]
@@ -42,6 +48,32 @@ struct QuantParams {
 
 constexpr int kThreads = 256;
 constexpr int kRowsPerWarp = 2;  // (token, head) rows of K and of V per warp and step
+
+// The (token, KV head) a lane quantises, walked without a division per step:
+// K lanes walk the rows r = token * hkv + head, V lanes the token pairs
+// u = q * hkv + head (their token is 2q or 2q + 1), both by a fixed stride.
+struct RowWalk {
+  int32_t major;  // K: token; V: token pair q
+  int32_t head;
+  int32_t dmajor, dhead;  // the stride as (major, head) steps
+  int32_t hkv;
+
+  __device__ __forceinline__ void init(int32_t start, int32_t stride, int32_t h) {
+    hkv = h;
+    major = start / h;
+    head = start - major * h;
+    dmajor = stride / h;
+    dhead = stride - dmajor * h;
+  }
+  __device__ __forceinline__ void next() {
+    major += dmajor;
+    head += dhead;
+    if (head >= hkv) {
+      head -= hkv;
+      ++major;
+    }
+  }
+};
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
   f[0] = bf16_to_f32(x.x & 0xFFFFu); f[1] = bf16_to_f32(x.x >> 16);
@@ -71,45 +103,64 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
   const int sub = lane & 7;      // block j = sub of the row: values [16 j, 16 j + 16)
   const int which = (lane >> 3) & 1;  // first or second row of the step
   const uint16_t* src = tensor ? p.v : p.k;
-  const int off_data = tensor ? kOffVData : kOffKData;  // within a page-head
   const float g = tensor ? p.gv : p.gk;
   const float t6 = __fmul_rn(6.0f, g);  // the block amax maps onto E2M1's 6
   const float r6 = __frcp_rn(t6);
   const bool t6_ok = t6 >= 0x1p-100f && t6 <= 0x1p+100f;  // t6 and 1/t6 well inside the normal range
   const int warp = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
   const int nwarps = (int)((gridDim.x * (unsigned)blockDim.x) >> 5);
+  // steps cover the K rows and the V token pairs: (ntok rounded up to even) * hkv,
+  // an even count, so the two halves of a warp run the same number of steps
+  const int64_t steps_end = (int64_t)(p.ntok + (p.ntok & 1)) * p.hkv;
 
-  // software pipeline: the next step's row (two 16-byte loads and its slot) is
-  // in flight while this step's block is quantised
+  // software pipeline: the next step's row (two 16-byte loads, its slot and,
+  // for V, the slot of the pair's other token) is in flight while this step's
+  // block is quantised
   const int64_t stride = (int64_t)nwarps * kRowsPerWarp;
   int64_t r = (int64_t)warp * kRowsPerWarp + which;
+  RowWalk walk;
+  if (tensor == 0)
+    walk.init(warp * kRowsPerWarp + which, nwarps * kRowsPerWarp, p.hkv);
+  else
+    walk.init(warp, nwarps, p.hkv);
+  // the lane's token at the walk's position (V: 2q + which)
+  auto token_of = [&](const RowWalk& w) { return tensor == 0 ? w.major : 2 * w.major + which; };
   uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
-  int64_t slot = -1, wrow = -1;
-  if (r < p.rows) {
-    const uint4* xs = reinterpret_cast<const uint4*>(src + (int64_t)r * kHeadDim) + 2 * sub;
+  int64_t slot = -1, pslot = -1, wrow = -1;
+  int tok = token_of(walk), head = walk.head;
+  if (r < steps_end && tok < p.ntok) {
+    const uint4* xs = reinterpret_cast<const uint4*>(src + ((int64_t)tok * p.hkv + head) * kHeadDim) + 2 * sub;
     xa = __ldg(xs);
     xb = __ldg(xs + 1);
-    slot = __ldg(p.slots + (int)r / p.hkv);  // r < rows < 2^31
-    if constexpr (kWs) wrow = __ldg(p.ws_rows + (int)r / p.hkv);
+    slot = __ldg(p.slots + tok);
+    if (tensor && (tok ^ 1) < p.ntok) pslot = __ldg(p.slots + (tok ^ 1));
+    if constexpr (kWs) wrow = __ldg(p.ws_rows + tok);
   }
-  for (; r < p.rows; r += stride) {
+  for (; r < steps_end; r += stride) {
     const int64_t rn = r + stride;
+    const int ctok = tok, h = head;
+    walk.next();
+    tok = token_of(walk);
+    head = walk.head;
     uint4 na = make_uint4(0, 0, 0, 0), nb = na;
-    int64_t nslot = -1, nwrow = -1;
-    if (rn < p.rows) {
-      const uint4* xs = reinterpret_cast<const uint4*>(src + (int64_t)rn * kHeadDim) + 2 * sub;
+    int64_t nslot = -1, npslot = -1, nwrow = -1;
+    if (rn < steps_end && tok < p.ntok) {
+      const uint4* xs = reinterpret_cast<const uint4*>(src + ((int64_t)tok * p.hkv + head) * kHeadDim) + 2 * sub;
       na = __ldg(xs);
       nb = __ldg(xs + 1);
-      nslot = __ldg(p.slots + (int)rn / p.hkv);
-      if constexpr (kWs) nwrow = __ldg(p.ws_rows + (int)rn / p.hkv);
+      nslot = __ldg(p.slots + tok);
+      if (tensor && (tok ^ 1) < p.ntok) npslot = __ldg(p.slots + (tok ^ 1));
+      if constexpr (kWs) nwrow = __ldg(p.ws_rows + tok);
     }
     const uint4 ca = xa, cb = xb;
-    const int64_t cslot = slot;
+    const bool cvalid = ctok < p.ntok;
+    const int64_t cslot = cvalid ? slot : -1, cpslot = pslot;
     xa = na;
     xb = nb;
     slot = nslot;
+    pslot = npslot;
     if constexpr (kWs) {
-      const int64_t cw = wrow;
+      const int64_t cw = cvalid ? wrow : -1;
       wrow = nwrow;
       if (cw >= p.ws_total_rows) {
         flag_error(p.status, NVFP4KV_DEVERR_ROW);
@@ -123,18 +174,10 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
         for (int i = 0; i < 8; ++i)
           e[i] = e4m3x2_from_quotients(bf16_to_f32(w[i] & 0xFFFFu), bf16_to_f32(w[i] >> 16), s, rs, fast, p.ws_unit);
         uint8_t* ws = tensor ? p.ws_v : p.ws_k;
-        reinterpret_cast<uint4*>(ws + (cw * p.hkv + (int)r % p.hkv) * kHeadDim)[sub] =
+        reinterpret_cast<uint4*>(ws + (cw * p.hkv + h) * kHeadDim)[sub] =
             make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
       }
     }
-    if (cslot < 0) continue;  // padding
-    if (cslot >= p.capacity) {
-      flag_error(p.status, NVFP4KV_DEVERR_SLOT);
-      continue;
-    }
-    const int h = (int)r % p.hkv;
-    uint8_t* ph = p.pages + ((cslot >> 4) * p.hkv + h) * kPageHeadBytes;  // the slot's page-head
-    const int rin = (int)(cslot & (kPage - 1));                            // its row there
     float f[16];
     unpack_bf16x8(ca, f);
     unpack_bf16x8(cb, f + 8);
@@ -170,8 +213,31 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(QuantParams p
 #pragma unroll
       for (int k = 0; k < 4; ++k) hi |= e2m1x2_from_f32(y[8 + 2 * k], y[8 + 2 * k + 1]) << (8 * k);
     }
-    reinterpret_cast<uint2*>(ph + off_data + rin * kRowBytes)[sub] = make_uint2(lo, hi);
-    ph[tensor ? v_scale_offset(rin, sub) : k_scale_offset(rin, sub)] = (uint8_t)sb;
+    // V: the other token of the pair (lane ^ 8 holds the same block of it);
+    // every lane takes part in the exchange
+    const uint32_t plo = __shfl_xor_sync(0xFFFFFFFFu, lo, 8);
+    const uint32_t phi = __shfl_xor_sync(0xFFFFFFFFu, hi, 8);
+    if (cslot < 0) continue;  // padding, or no such row
+    if (cslot >= p.capacity) {
+      flag_error(p.status, NVFP4KV_DEVERR_SLOT);
+      continue;
+    }
+    uint8_t* ph = p.pages + ((cslot >> 4) * p.hkv + h) * kPageHeadBytes;  // the slot's page-head
+    const int rin = (int)(cslot & (kPage - 1));                            // its row there
+    if (tensor == 0) {
+      reinterpret_cast<uint2*>(ph + kOffKData + rin * kRowBytes)[sub] = make_uint2(lo, hi);
+      ph[k_scale_offset(rin, sub)] = (uint8_t)sb;
+    } else {
+      // the step's two tokens fill one pair row when their slots are 2m and 2m + 1
+      const int64_t se = which ? cpslot : cslot, so = which ? cslot : cpslot;
+      const bool paired = (se & 1) == 0 && so == se + 1;
+      if (paired) {
+        if (which == 0) v_store_block_pair(ph + kOffVData, rin >> 1, sub, lo, hi, plo, phi);
+      } else {
+        v_store_block_one(ph + kOffVData, rin, sub, lo, hi);
+      }
+      ph[v_scale_offset(rin, sub)] = (uint8_t)sb;
+    }
   }
 }
 
@@ -181,7 +247,7 @@ namespace {
 
 template <bool kWs>
 cudaError_t launch_quantize(QuantParams& p, int num_sms, cudaStream_t stream) {
-  const int warps_needed = (p.rows + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int warps_needed = (int)(((int64_t)(p.ntok + (p.ntok & 1)) * p.hkv) / kRowsPerWarp);
   const int warps_per_block = kThreads / 32;
   int blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
   // a persistent grid: as many blocks as fit on the device at once (more
@@ -207,6 +273,7 @@ QuantParams cache_params(const nvfp4kv_cache& c, const uint16_t* k, const uint16
   p.v = v;
   p.slots = slot_mapping;
   p.rows = (int32_t)(num_tokens * c.num_kv_heads);
+  p.ntok = (int32_t)num_tokens;
   p.hkv = c.num_kv_heads;
   p.capacity = c.num_pages * (int64_t)c.page_size;
   p.pages = c.pages;

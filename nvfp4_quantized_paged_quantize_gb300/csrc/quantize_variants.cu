@@ -15,8 +15,10 @@
 // (the same 64 data bytes per row, 4 scale bytes per row).
 //
 // Eight lanes own one (token, head) row of K or of V, 16 values each; a warp
-// takes four rows.  Block scales divide exactly (IEEE); these are comparison
-// paths, not the tuned one.
+// takes the rows of one token pair (2q, 2q + 1) of one KV head: K of token 2q,
+// K of token 2q + 1, V of token 2q, V of token 2q + 1, so that V's token-pair
+// bytes can be written whole when the two slots are 2m and 2m + 1.  Block
+// scales divide exactly (IEEE); these are comparison paths, not the tuned one.
 #include "nvfp4kv_device.cuh"
 #include "nvfp4kv_launch.h"
 
@@ -29,7 +31,8 @@ struct VariantParams {
   const int64_t* slots;
   const uint8_t* rand_k;  // stochastic rounding: one byte per value, [tokens][hkv][128]
   const uint8_t* rand_v;
-  int64_t rows;  // num_tokens * hkv * 2 (K rows then V rows of each (token, head))
+  int64_t units;  // token pairs * hkv: one warp each
+  int64_t ntok;
   int32_t hkv;
   int64_t capacity;
   uint8_t* pages;  // [num_pages][hkv][page-head bytes of the variant's layout]
@@ -72,16 +75,18 @@ template <int kVariant>
 __global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParams p) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & 7;  // values [16 sub, 16 sub + 16) of the row
+  const int tensor = lane >> 4, which = (lane >> 3) & 1;
   // every lane stays to the end (the rotation and MXFP4 exchange values across
-  // the row's lanes with full-warp shuffles); lanes past the last row work on
-  // row 0 and store nothing
-  const int64_t gid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
-  const bool live = gid < p.rows;
-  const int64_t row_id = live ? gid : 0;
-  const int tensor = (int)(row_id & 1);
-  const int64_t th = row_id >> 1;  // token * hkv + h
-  const int64_t token = th / p.hkv;
-  const int h = (int)(th - token * p.hkv);
+  // the row's lanes with full-warp shuffles, and V's two tokens meet); lanes
+  // without a row work on row 0 and store nothing
+  const int64_t unit = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t q = unit / p.hkv;
+  const int h0 = (int)(unit - q * p.hkv);
+  const int64_t token0 = 2 * q + which;
+  const bool live = unit < p.units && token0 < p.ntok;
+  const int64_t token = live ? token0 : 0;
+  const int h = live ? h0 : 0;
+  const int64_t th = token * p.hkv + h;  // the input row
   const uint16_t* src = (tensor ? p.v : p.k) + th * kHeadDim + 16 * sub;
   const uint4 xa = __ldg(reinterpret_cast<const uint4*>(src));
   const uint4 xb = __ldg(reinterpret_cast<const uint4*>(src) + 1);
@@ -168,21 +173,34 @@ __global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParam
         hi |= e2m1x2_from_f32(__fdiv_rn(f[8 + 2 * k], den), __fdiv_rn(f[8 + 2 * k + 1], den)) << (8 * k);
     }
   }
-  if (!live) return;
-  const int64_t slot = __ldg(p.slots + token);
-  if (slot < 0) return;  // padding
+  const int64_t slot = live ? __ldg(p.slots + token) : -1;
+  // V: the other token of the pair (lane ^ 8 holds the same block of it)
+  const uint32_t plo = __shfl_xor_sync(0xFFFFFFFFu, lo, 8);
+  const uint32_t phi = __shfl_xor_sync(0xFFFFFFFFu, hi, 8);
+  const int64_t pslot = __shfl_xor_sync(0xFFFFFFFFu, slot, 8);
+  if (slot < 0) return;  // padding, or no row
   if (slot >= p.capacity) {
     if (sub == 0) flag_error(p.status, NVFP4KV_DEVERR_SLOT);
     return;
   }
   const int rin = (int)(slot & (kPage - 1));  // the slot's row in its page-head
+  const int64_t se = which ? pslot : slot, so = which ? slot : pslot;
+  const bool paired = (se & 1) == 0 && so == se + 1;  // the two tokens fill one V pair row
+  const bool mx = kVariant == NVFP4KV_VARIANT_MXFP4;
+  uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * (mx ? kMxPageHeadBytes : kPageHeadBytes);
+  if (tensor == 0) {
+    reinterpret_cast<uint2*>(ph + kOffKData + rin * kRowBytes)[sub] = make_uint2(lo, hi);
+  } else {
+    uint8_t* vdata = ph + (mx ? kMxOffVData : kOffVData);
+    if (paired) {
+      if (which == 0) v_store_block_pair(vdata, rin >> 1, sub, lo, hi, plo, phi);
+    } else {
+      v_store_block_one(vdata, rin, sub, lo, hi);
+    }
+  }
   if constexpr (kVariant == NVFP4KV_VARIANT_MXFP4) {
-    uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * kMxPageHeadBytes;
-    reinterpret_cast<uint2*>(ph + (tensor ? kMxOffVData : kOffKData) + rin * kRowBytes)[sub] = make_uint2(lo, hi);
     if ((sub & 1) == 0) ph[tensor ? mx_v_scale_offset(rin, sub >> 1) : mx_k_scale_offset(rin, sub >> 1)] = (uint8_t)sbyte;
   } else {
-    uint8_t* ph = p.pages + ((slot >> 4) * p.hkv + h) * kPageHeadBytes;
-    reinterpret_cast<uint2*>(ph + (tensor ? kOffVData : kOffKData) + rin * kRowBytes)[sub] = make_uint2(lo, hi);
     ph[tensor ? v_scale_offset(rin, sub) : k_scale_offset(rin, sub)] = (uint8_t)sbyte;
   }
 }
@@ -198,14 +216,16 @@ cudaError_t launch_quantize_variant(int variant, const nvfp4kv_cache& c, const u
   p.slots = slot_mapping;
   p.rand_k = rand_k;
   p.rand_v = rand_v;
-  p.rows = num_tokens * c.num_kv_heads * 2;
+  p.units = (num_tokens + 1) / 2 * c.num_kv_heads;
+  p.ntok = num_tokens;
   p.hkv = c.num_kv_heads;
   p.capacity = c.num_pages * (int64_t)c.page_size;
   p.pages = c.pages;
   p.gk = c.k_global_scale;
   p.gv = c.v_global_scale;
   p.status = device_status;
-  const int64_t blocks = (p.rows * 8 + kThreads - 1) / kThreads;
+  const int64_t blocks = (p.units * 32 + kThreads - 1) / kThreads;
+  if (blocks == 0) return cudaSuccess;
   if (variant == NVFP4KV_VARIANT_SR)
     quantize_variant_kernel<NVFP4KV_VARIANT_SR><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
   else if (variant == NVFP4KV_VARIANT_HADAMARD)

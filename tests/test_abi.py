@@ -65,7 +65,7 @@ def test_page_head_views_cover_the_pool_once(lib):
 
     for mx in (False, True):
         c = kv.Cache.empty(3, 2, device="cpu", zero=True, mxfp4=mx)
-        for i, part in enumerate((c.k_data, c.k_scale, c.v_data, c.v_scale)):
+        for i, part in enumerate((c.k_data, c.k_scale, c.v_pairs, c.v_scale)):
             part.fill_(i + 1)
         # every byte of the pool belongs to exactly one of the four views
         counts = torch.bincount(c.pages.reshape(-1).long(), minlength=5)
@@ -83,6 +83,14 @@ def test_page_head_views_cover_the_pool_once(lib):
         ph = c.pages[0, 0]
         assert ph[1024 + 3 * sc + 1] == 7
         assert ph[2048 + 16 * sc + 16 * 1 + 3] == 9
+        # V data by token pair: dimension d of tokens 2p (low nibble) and 2p + 1 (high)
+        rows = torch.zeros((3, 2, 16, 64), dtype=torch.uint8)
+        rows[2, 1, 5, 3] = 0xA0                     # token 5, dimension 7 = 0xA (high nibble of byte 3)
+        rows[2, 1, 4, 3] = 0x0B                     # token 4, dimension 6 = 0xB
+        c.set_v_data(rows)
+        pr = c.pages[2, 1, 1024 + 16 * sc: 2048 + 16 * sc].reshape(8, 128)
+        assert pr[2, 7] == 0xA0 and pr[2, 6] == 0x0B and int(pr.sum()) == 0xA0 + 0x0B
+        assert torch.equal(c.v_data, rows)
 
 
 def test_decode_workspace_bytes_from_the_batch_shape(lib):

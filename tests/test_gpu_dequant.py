@@ -134,7 +134,7 @@ def test_every_code_and_scale_bit_exact(cuda_lib, gk, gv, sk, sv):
     vd = np.tile(rev, (2, 16, 8))
     g = gpu_cache(2, 1, gk, gv)
     g.k_data.copy_(torch.from_numpy(kd.reshape(2, 1, 16, 64)))
-    g.v_data.copy_(torch.from_numpy(vd.reshape(2, 1, 16, 64)))
+    g.set_v_data(torch.from_numpy(vd.reshape(2, 1, 16, 64)).cuda())
     g.k_scale.copy_(torch.from_numpy(sc.reshape(2, 1, 16, 8)))
     g.v_scale.copy_(torch.from_numpy(sc[::-1].copy().reshape(2, 1, 16, 8)))
     o = oracle.Cache(2, 1, 128, 16, gk, gv, arrays=(kd, vd, sc, sc[::-1].copy()))

@@ -127,6 +127,52 @@ def test_padding_and_out_of_range_slots(cuda_lib):
     _assert_pool_equal(g, o)
 
 
+@pytest.mark.parametrize("variant", [None, "sr", "hadamard", "mxfp4"])
+def test_v_token_pairs_any_slot_order(cuda_lib, variant):
+    # V data is stored by token pair (slots 2m, 2m + 1 share bytes): a call's two
+    # tokens of a step fill a pair row whole only when their slots are 2m, 2m + 1;
+    # every other case merges nibbles.  Cover: consecutive slots from an even
+    # and from an odd start, a shuffled order, a pair split between two calls
+    # (in both orders), pairs whose partner is padding, and the last token of an
+    # odd count; the final pool must equal the oracle's after the same calls.
+    from variant_util import MXFP4, SR, HADAMARD, oracle_variant_pools
+
+    rng = np.random.default_rng(17)
+    H, pages = 3, 12                                          # 192 slots
+    calls = []
+    calls.append(np.arange(10, 10 + 21, dtype=np.int64))      # even start, odd count
+    calls.append(np.arange(35, 35 + 20, dtype=np.int64))      # odd start: every step straddles two pair rows
+    calls.append(rng.permutation(np.arange(60, 100, dtype=np.int64)))  # shuffled
+    calls.append(np.array([101, 130, 103, 102, -1, 100, 131], np.int64))  # mixed, partners in this call or none
+    calls.append(np.array([104, 150, 107], np.int64))         # halves of pairs (104, 105), (106, 107), (150, 151)
+    calls.append(np.array([105, 106, 151, -1, 152], np.int64))  # ... completed later, in the other order
+    xs = [inputs.bf16_bits(rng.normal(0, 1, (len(c), H, 128)).astype(np.float32)) for c in calls]
+    vs = [inputs.bf16_bits(rng.standard_t(4, (len(c), H, 128)).astype(np.float32)) for c in calls]
+    if variant is None:
+        g = gpu_cache(pages, H)
+        o = oracle.Cache(pages, H)
+        for c, x, v in zip(calls, xs, vs):
+            gpu_append(g, x, v, c)
+            assert oracle.quantize_append(o, x, v, c) == 0
+        _assert_pool_equal(g, o)
+        return
+    var = {"sr": SR, "hadamard": HADAMARD, "mxfp4": MXFP4}[variant]
+    g = kv.Cache.empty(pages, H, zero=True, mxfp4=variant == "mxfp4")
+    rk = [rng.integers(0, 256, x.shape, dtype=np.uint8) for x in xs]
+    rv = [rng.integers(0, 256, x.shape, dtype=np.uint8) for x in xs]
+    for c, x, v, a, b in zip(calls, xs, vs, rk, rv):
+        kv.nvfp4kv_quantize_append_variant(var, g, bf16_dev(x), bf16_dev(v), dev(c), dev(a), dev(b))
+    # the oracle's pools after the same calls, one by one
+    want = oracle_variant_pools(var, np.concatenate(xs), np.concatenate(vs), np.concatenate(calls), pages, H,
+                                1.0, 1.0, np.concatenate(rk), np.concatenate(rv))
+    rows = pages * H * 16
+    for name, (data, scale) in want.items():
+        gd = (g.k_data if name == "k" else g.v_data).reshape(rows, -1).cpu().numpy()
+        gs = (g.k_scale if name == "k" else g.v_scale).reshape(rows, -1).cpu().numpy()
+        assert np.array_equal(gd, data), f"{name} data"
+        assert np.array_equal(gs, scale), f"{name} scales"
+
+
 def test_extend_chunk_full_size_bit_exact(cuda_lib):
     # one layer of the extend workload: 16 sequences x 2048 new tokens x 8 KV heads
     wl = inputs.extend_config()
