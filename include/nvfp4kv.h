@@ -147,9 +147,10 @@ int nvfp4kv_quantize_append(const nvfp4kv_cache* cache, const void* k, const voi
 
 /*
  * Bytes of device workspace nvfp4kv_decode_attention needs for this batch
- * shape on the current CUDA device (split-K partial results and per-(sequence,
- * KV head) merge headers).  Host only; query it with the device current
- * that will run the decode.
+ * shape on the current CUDA device: split-K partial results, two per warp of
+ * the launch (so they depend on the device's SM count, not on the batch), and
+ * one 4-byte page prefix per sequence.  Host only; query it with the device
+ * current that will run the decode.
  */
 int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int32_t num_q_heads,
                                   size_t* bytes);
@@ -158,11 +159,11 @@ int nvfp4kv_decode_workspace_size(const nvfp4kv_cache* cache, int32_t batch, int
  * The same size from the batch shape alone, for callers that size the
  * workspace before a cache exists: bytes enough for any cache with
  * num_q_heads / G KV heads, on a device with num_sms SMs (pass that device's
- * cudaDevAttrMultiProcessorCount).  max_seq_len is accepted and ignored: the
- * split-K partition cuts the pages of all sequences together into as many
- * ranges as the device runs at once, so the scratch depends on the SM count
- * and the number of (sequence, KV head) pairs, not on any length.  Host only;
- * returns 0 for batch < 0, num_q_heads <= 0 or num_sms <= 0.
+ * cudaDevAttrMultiProcessorCount).  num_q_heads and max_seq_len are checked
+ * and otherwise unused: the split-K partition cuts the pages of all sequences
+ * together into as many ranges as the device runs at once, so the scratch
+ * depends on the SM count and the batch, not on any length or head count.
+ * Host only; returns 0 for batch < 0, num_q_heads <= 0 or num_sms <= 0.
  */
 size_t nvfp4kv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
                                       int32_t num_sms);
@@ -251,8 +252,9 @@ int nvfp4kv_append_decode_attention(const nvfp4kv_cache* cache, const void* k, c
  *
  * Arguments, layout and errors are those of nvfp4kv_decode_attention without
  * `workspace` / `workspace_bytes`.  A batch whose workspace would exceed the
- * fixed scratch (see nvfp4kv_decode_workspace_size) returns
- * NVFP4KV_ERR_WORKSPACE before anything is enqueued.
+ * fixed scratch (see nvfp4kv_decode_workspace_size: about 4.59 million
+ * sequences on 152 SMs) returns NVFP4KV_ERR_WORKSPACE before anything is
+ * enqueued.
  */
 int nvfp4kv_decode_attention_static(const nvfp4kv_cache* cache, const void* q, float* out,
                                     const int32_t* page_table, int32_t max_pages_per_seq,

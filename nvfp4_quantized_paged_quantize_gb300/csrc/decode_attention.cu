@@ -30,7 +30,9 @@
 // is done: no CTA-wide barrier or merge sits at the end of the decode, where
 // it would wait on the slowest warp and run cold code under full memory load.
 // combine_kernel, launched right behind the decode as a programmatic
-// dependent, merges each cut pair's records (the flash-decoding combine).
+// dependent, merges each cut pair's records (the flash-decoding combine); it
+// finds them from the split itself, which it rederives from the lengths while
+// the decode still runs.
 //
 // Exactness: e2m1 * E4M3 has at most 6 significant bits in [2^-10, 2688], so
 // Khat and Vhat are exact in f16.  q is bf16; it is multiplied by a power of
@@ -99,9 +101,10 @@ struct DecodeParams {
   float score_scale;  // softmax_scale * log2(e) * g_K
   float v_gscale;     // g_V
   float* part;        // [2 * num_ctas * kNW] records: warp w's first (2w) and last (2w + 1) cut piece
-  int2* hdr;          // [batch * hkv], written every call: a pair cut by warp ranges gets (record of its
-                      // first piece, last warp), any other pair (0, 0)
   int32_t* status;
+  int32_t* cu_pages;  // [batch + 1], written by CTA 0: pages of the sequences before each, then of all
+  int32_t ncta;       // CTAs of the decode grid (its split, rederived by the combine)
+  int32_t comb_heads; // query heads per combine block
 };
 
 // ---------------------------------------------------------------------------
@@ -191,20 +194,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 __device__ __forceinline__ long long cta_start(long long c, long long W, long long N) {
   const long long q = W / N, rem = W % N;
   return c * q + (c < rem ? c : rem);
-}
-
-// The CTA whose range holds global page-head r (0 <= r < W).
-__device__ __forceinline__ long long cta_of(long long r, long long W, long long N) {
-  const long long q = W / N, rem = W % N, big = rem * (q + 1);
-  return r < big ? r / (q + 1) : rem + (r - big) / q;
-}
-
-// The global warp (CTA * kNW + warp) whose range holds page-head r: CTA c's
-// range [r0, r0 + len) gives warp w the items [r0 + len w / kNW, r0 + len (w + 1) / kNW).
-__device__ __forceinline__ int warp_of_item(long long r, long long W, long long N) {
-  const long long c = cta_of(r, W, N);
-  const long long r0 = cta_start(c, W, N), len = cta_start(c + 1, W, N) - r0;
-  return (int)(c * kNW + ((r - r0 + 1) * kNW - 1) / len);
 }
 
 // Where each item of a 32-item chunk of a warp's range lives (one per lane).
@@ -778,7 +767,6 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   uint8_t* ring = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
   __shared__ long long red[kNW];
-  __shared__ long long s_W;  // total page-heads, reread by the merge
   __shared__ int wstart_b[kNW], wstart_cu[kNW];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -813,7 +801,6 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
         float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
         for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int h = 0; h < p.hkv; ++h) p.hdr[(long long)b * p.hkv + h] = make_int2(0, 0);  // nothing to combine
       }
     }
     int incl = np;
@@ -835,6 +822,8 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     r0 = cta_start(blockIdx.x, W, N);
     r1 = cta_start((long long)blockIdx.x + 1, W, N);
     const int excl = (int)before + incl - np;
+    if (blockIdx.x == 0 && b < p.batch) p.cu_pages[b] = excl;
+    if (blockIdx.x == 0 && tid == 0) p.cu_pages[p.batch] = (int)total;
     if (np > 0) {
       for (int w2 = 0; w2 < kNW; ++w2) {
         const long long ws = r0 + (r1 - r0) * w2 / kNW, we = r0 + (r1 - r0) * (w2 + 1) / kNW;
@@ -844,7 +833,6 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         }
       }
     }
-    if (tid == 0) s_W = W;
     __syncthreads();
   } else {
     long long pages_local = 0;
@@ -854,11 +842,9 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       if (L == 0 && (b % (int)gridDim.x) == (int)blockIdx.x) {
         float4* o = reinterpret_cast<float4*>(p.out + (long long)b * p.hq * kHeadDim);
         for (int j = 0; j < p.hq * kHeadDim / 4; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int h = 0; h < p.hkv; ++h) p.hdr[(long long)b * p.hkv + h] = make_int2(0, 0);  // nothing to combine
       }
     }
     W = block_sum_ll(pages_local, red, warp, lane) * p.hkv;
-    if (tid == 0) s_W = W;
     if (W == 0) return;
     r0 = cta_start(blockIdx.x, W, N);
     r1 = cta_start((long long)blockIdx.x + 1, W, N);
@@ -883,6 +869,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         chunk += (int)red[w];
       }
       const int excl = before + incl - np;
+      if (blockIdx.x == 0 && b < p.batch) p.cu_pages[b] = excl;
       if (np > 0) {
         for (int w2 = 0; w2 < kNW; ++w2) {
           const long long ws = r0 + (r1 - r0) * w2 / kNW, we = r0 + (r1 - r0) * (w2 + 1) / kNW;
@@ -895,6 +882,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       carry += chunk;
       __syncthreads();
     }
+    if (blockIdx.x == 0 && tid == 0) p.cu_pages[p.batch] = carry;
   }
 
   // ---- per-warp streaming over its page-heads ----------------------------------
@@ -980,7 +968,6 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       const int page0 = __shfl_sync(0xFFFFFFFFu, cur.page, li);
       const int np = __shfl_sync(0xFFFFFFFFu, cur.np, li);
       const int iend = min(n, i + (np - page0));
-      const long long piece_r = wr0 + i;
       ++nseg;
       if (nseg > 1) load_q<F>(p, fetch_q(p, pair, g, t), s, g, t);
       int j = i;
@@ -1081,27 +1068,18 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       const bool complete = page0 == 0 && last_page == np - 1;
       const int slot = (iend == n && nseg > 1) ? 1 : 0;
       finish_piece<F>(p, s, pair, complete, p.part + (2 * gwarp + slot) * kRecFloats, g, t);
-      if (page0 == 0 && lane == 0) {
-        // the pair's first piece writes the pair's header on every call: where
-        // its pieces are if it was cut, else the no-op header (0, 0)
-        int2 hd = make_int2(0, 0);
-        if (!complete) {
-          const long long Wt = s_W, Nt = gridDim.x;
-          hd = make_int2((int)(2 * gwarp + slot), warp_of_item(piece_r + np - 1, Wt, Nt));
-        }
-        p.hdr[pair] = hd;
-      }
       i = iend;
     }
   }
 }
 
-// Merge the records of every pair the warp ranges cut: block = (pair, query
-// head), thread = (record group, 4-column group).  Group k takes records k,
-// k + groups, ... with an online rescale (the loads of a group are
-// independent), then group 0 merges the groups' partial results.  Launched as
-// a programmatic dependent of decode_kernel: griddepcontrol.wait returns once
-// the decode grid has finished and its writes are visible.
+// Merge the records of every pair the warp ranges cut: block = (pair, a chunk
+// of its query heads), warp = (query head, record group), thread = 4 columns.
+// Group k of a head takes records k, k + groups, ... with an online rescale,
+// then group 0 merges the groups' partial results.  Launched as a
+// programmatic dependent of decode_kernel: griddepcontrol.wait returns once
+// the decode grid has finished and its writes are visible; what comes before
+// it reads only the call's inputs.
 constexpr int kCombineMaxGroups = 16;
 
 __device__ __forceinline__ void online_merge(float& M, float& L, float4& acc, float m, float l, float4 v) {
@@ -1116,35 +1094,129 @@ __device__ __forceinline__ void online_merge(float& M, float& L, float4& acc, fl
   M = Mn;
 }
 
+// The split's arithmetic in 32 bits, for W < 2^31 page-heads (the combine's use).
+__device__ __forceinline__ int cta_start32(int c, int W, int N) {
+  const int q = W / N, rem = W - q * N;
+  return c * q + (c < rem ? c : rem);
+}
+__device__ __forceinline__ int warp_of_item32(int r, int W, int N) {
+  const int q = W / N, rem = W - q * N, big = rem * (q + 1);
+  const int c = r < big ? r / (q + 1) : rem + (r - big) / q;
+  const int r0 = cta_start32(c, W, N), len = cta_start32(c + 1, W, N) - r0;
+  return c * kNW + (int)(((long long)(r - r0 + 1) * kNW - 1) / len);
+}
+
+// A sequence's length as the decode clamps it (without flagging: the decode does).
+__device__ __forceinline__ int clamped_len(const DecodeParams& p, int b) {
+  const int L = __ldg(p.seq_lens + b), lmax = p.max_pages * kPage;
+  return L < 0 ? 0 : (L > lmax ? lmax : L);
+}
+
+// Block = (pair, chunk of its query heads); warp = (head, record group).
+constexpr int kCombineMaxWarps = 32;
+constexpr int kCombineScanMax = 1024;  // batches up to this size: the combine sums the lengths itself
+
 template <int F>
-__global__ void __launch_bounds__(kCombineMaxGroups * 32) combine_kernel(const DecodeParams p) {
-  __shared__ float s_m[kCombineMaxGroups][32], s_l[kCombineMaxGroups][32];
-  __shared__ float4 s_o[kCombineMaxGroups][32];
+__global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const DecodeParams p) {
+  __shared__ float s_m[kCombineMaxWarps][32], s_l[kCombineMaxWarps][32];
+  __shared__ float4 s_o[kCombineMaxWarps][32];
+  __shared__ int s_info[3];  // first record, first warp, record count (0: nothing to merge)
+  const int pair = blockIdx.x;
+  const int b = pair / p.hkv, hh = pair - b * p.hkv;
+  const int warp = threadIdx.x >> 5, col = threadIdx.x & 31;
+  const int hb = p.comb_heads;                 // query heads per block
+  const int groups = (blockDim.x >> 5) / hb;   // record groups per head
+  const int hl = warp % hb, grp = warp / hb;
+  const int head = blockIdx.y * hb + hl;
+  // Where the pair lies in the decode's split, worked out by warp 0 in 32-bit
+  // arithmetic (page-head indices stay below 2^31): the pages of the sequences
+  // before b and of all sequences, then the warps holding the pair's first and
+  // last page-heads.  For up to kCombineScanMax sequences the pages come from
+  // the lengths, inputs of the call, so this runs while the decode is still
+  // streaming; for more, from the prefix the decode's CTA 0 wrote (after the
+  // wait), which keeps the work per block independent of the batch.
+  const bool scan = p.batch <= kCombineScanMax;
+  if (warp == 0) {
+    int before = 0, total = 0;
+    if (scan) {
+      for (int i = col; i < p.batch; i += 32) {
+        const int npi = (clamped_len(p, i) + kPage - 1) / kPage;
+        total += npi;
+        before += i < b ? npi : 0;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
+        before += __shfl_xor_sync(0xFFFFFFFFu, before, off);
+      }
+    }
+    if (col == 0) {
+      const int np = (clamped_len(p, b) + kPage - 1) / kPage;
+      int rec0 = 0, wf = 0, cnt = 0;
+      if (np > 0) {
+        if (!scan) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          before = __ldcg(p.cu_pages + b);
+          total = __ldcg(p.cu_pages + p.batch);
+        }
+        const int W = total * p.hkv, N = p.ncta;
+        const int P0 = before * p.hkv + hh * np;  // the pair's first page-head
+        wf = warp_of_item32(P0, W, N);
+        const int wl = warp_of_item32(P0 + np - 1, W, N);
+        if (wl != wf) {
+          // the first piece is warp wf's last piece (record 2 wf + 1), or its
+          // only one when the pair starts wf's range (record 2 wf); every later
+          // warp up to wl holds one piece as its first (record 2 w)
+          const int cf = wf / kNW, r0c = cta_start32(cf, W, N), r1c = cta_start32(cf + 1, W, N);
+          const int wr0 = r0c + (int)((long long)(r1c - r0c) * (wf - cf * kNW) / kNW);
+          rec0 = 2 * wf + (P0 > wr0 ? 1 : 0);
+          cnt = wl - wf + 1;
+        }
+      }
+      s_info[0] = rec0;
+      s_info[1] = wf;
+      s_info[2] = cnt;
+    }
+  }
+  __syncthreads();
+  const int rec0 = s_info[0], wf = s_info[1], cnt = s_info[2];
+  if (cnt == 0) return;  // an empty sequence (the decode wrote its zeros) or one warp held the whole pair
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int pair = blockIdx.x, head = blockIdx.y;
-  const int2 h = __ldcg(p.hdr + pair);
-  const int gw_first = h.x >> 1;
-  if (h.y <= gw_first) return;  // the pair was not cut
-  const int groups = blockDim.x >> 5, grp = threadIdx.x >> 5, col = threadIdx.x & 31;
-  const int cnt = h.y - gw_first + 1;  // records: h.x, then 2 (gw_first + c) for c = 1 .. cnt - 1
+  // warp (head, grp) merges the head's records grp, grp + groups, ...: four at
+  // a time, all loads issued before any is used (a warp of the decode with no
+  // items marked its record m = -inf)
   float M = -INFINITY, L = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int c = grp; c < cnt; c += groups) {
-    const long long ri = c == 0 ? (long long)h.x : 2LL * (gw_first + c);
-    const float* r = p.part + ri * kRecFloats;
-    const float m = __ldcg(r + kOffM + head);
-    if (m == -INFINITY) continue;  // a warp with no items (or no valid page): nothing to merge
-    const float l = __ldcg(r + kOffL + head);
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(r + head * kHeadDim) + col);
-    online_merge(M, L, acc, m, l, v);
+  if (head < p.group) {
+    for (int c0 = grp; c0 < cnt; c0 += 4 * groups) {
+      float m[4], l[4];
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + i * groups;
+        m[i] = -INFINITY;
+        l[i] = 0.0f;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < cnt) {
+          const float* r = p.part + (c == 0 ? (long long)rec0 : 2LL * (wf + c)) * kRecFloats;
+          m[i] = __ldcg(r + kOffM + head);
+          l[i] = __ldcg(r + kOffL + head);
+          v[i] = __ldcg(reinterpret_cast<const float4*>(r + head * kHeadDim) + col);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) online_merge(M, L, acc, m[i], l[i], v[i]);
+    }
   }
-  s_m[grp][col] = M;
-  s_l[grp][col] = L;
-  s_o[grp][col] = acc;
+  s_m[warp][col] = M;
+  s_l[warp][col] = L;
+  s_o[warp][col] = acc;
   __syncthreads();
-  if (grp != 0) return;
-  for (int k = 1; k < groups; ++k) online_merge(M, L, acc, s_m[k][col], s_l[k][col], s_o[k][col]);
+  if (grp != 0 || head >= p.group) return;
+  for (int k = 1; k < groups; ++k) {
+    const int w2 = k * hb + hl;
+    online_merge(M, L, acc, s_m[w2][col], s_l[w2][col], s_o[w2][col]);
+  }
   const float sc = L > 0.0f ? p.v_gscale / L : 0.0f;
   float v[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
   if constexpr (F == kFmtHadamard) {
@@ -1162,12 +1234,12 @@ int decode_num_ctas(int num_sms) { return num_sms * kCtasPerSm; }
 
 size_t decode_workspace_bytes(int num_sms, int32_t batch, int32_t num_kv_heads) {
   size_t rec = 2 * (size_t)decode_num_ctas(num_sms) * kNW * kRecFloats * sizeof(float);
+  (void)num_kv_heads;
   rec = (rec + 255) / 256 * 256;
-  return rec + (size_t)batch * (size_t)num_kv_heads * sizeof(int2);
+  return rec + ((size_t)batch + 1) * sizeof(int32_t);
 }
 
 size_t decode_workspace_bound(int num_sms, int32_t batch, int32_t num_q_heads) {
-  // the headers grow with the KV-head count, which is at most num_q_heads
   return decode_workspace_bytes(num_sms, batch, num_q_heads);
 }
 
@@ -1205,8 +1277,9 @@ cudaError_t launch_decode_fmt(const nvfp4kv_cache& c, const uint16_t* q, float* 
   size_t rec = 2 * (size_t)num_ctas * kNW * kRecFloats * sizeof(float);
   rec = (rec + 255) / 256 * 256;
   p.part = static_cast<float*>(workspace);
-  p.hdr = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + rec);
+  p.cu_pages = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + rec);
   p.status = device_status;
+  p.ncta = num_ctas;
   cudaError_t e;
   if (after_kernel) {
     // a programmatic dependent of the kernel before it on the stream
@@ -1229,12 +1302,17 @@ cudaError_t launch_decode_fmt(const nvfp4kv_cache& c, const uint16_t* q, float* 
   // the combine, as a programmatic dependent of the decode on the same stream
   // records per cut pair are about (warps / pairs) when the sequences are
   // alike: give each thread a handful of them
+  // records per cut pair are about (warps / pairs) when the sequences are
+  // alike: a record group per four to eight of them, up to 16 groups per head,
+  // and as many of the pair's query heads per block as fit 32 warps
   const long long per_pair = (2LL * num_ctas * kNW) / (long long)pairs;
   int groups = 1;
-  while (groups < kCombineMaxGroups && groups * 4 < per_pair) groups *= 2;
+  while (groups < kCombineMaxGroups && groups * 8 < per_pair) groups *= 2;
+  const int hb = p.group < kCombineMaxWarps / groups ? p.group : kCombineMaxWarps / groups;
+  p.comb_heads = hb;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)pairs, (unsigned)p.group);
-  cfg.blockDim = dim3(32 * groups);
+  cfg.gridDim = dim3((unsigned)pairs, (unsigned)((p.group + hb - 1) / hb));
+  cfg.blockDim = dim3(32 * hb * groups);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

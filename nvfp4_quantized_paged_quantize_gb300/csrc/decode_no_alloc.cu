@@ -2,7 +2,7 @@
 // allocate device memory.
 //
 // nvfp4kv_decode_attention needs a caller-provided device workspace for its
-// split-K pieces and the per-(sequence, KV head) merge headers.  Some callers cannot provide one: code
+// split-K pieces.  Some callers cannot provide one: code
 // running inside a host allocator hook, a plug-in loaded by a runtime that
 // owns all device memory, or a process that must never call cudaMalloc on its
 // hot path.  nvfp4kv_decode_attention_static serves them by using a fixed

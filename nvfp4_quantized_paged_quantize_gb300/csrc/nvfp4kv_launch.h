@@ -81,7 +81,7 @@ cudaError_t launch_tensor_amax(const uint16_t* x, int64_t n, float* amax, bool a
 
 // Split-K decode: how many CTAs the decode launches on a device with num_sms
 // SMs, and the workspace it needs there (two split records per warp of the
-// launch, a merge header per (sequence, KV head)).
+// launch, whatever the batch).
 int decode_num_ctas(int num_sms);
 size_t decode_workspace_bytes(int num_sms, int32_t batch, int32_t num_kv_heads);
 // An upper bound of decode_workspace_bytes over every KV-head count that

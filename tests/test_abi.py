@@ -100,9 +100,11 @@ def test_decode_workspace_bytes_from_the_batch_shape(lib):
     a = f(32, 64, 8193, 152)
     assert a > 0
     assert f(32, 64, 131072, 152) == a           # no length sizes the split-K scratch
-    assert f(33, 64, 8193, 152) > a              # one merge header per (sequence, head)
+    records = 2 * (152 * 3 * 4) * (8 * 128 + 16) * 4   # two per warp of the launch
+    assert a == records + 33 * 4                 # and each sequence's page prefix
+    assert f(33, 8, 8193, 152) == a + 4          # neither the query nor the KV heads count
     assert f(32, 64, 8193, 160) > a              # split records per CTA of the launch
-    assert f(0, 64, 0, 152) > 0                  # the records of the launch even for no sequences
+    assert f(0, 64, 0, 152) == records + 4       # the records of the launch even for no sequences
 
 
 def _fake_cache(**kw):

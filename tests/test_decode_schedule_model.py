@@ -6,10 +6,11 @@ each CTA range into kNW balanced contiguous warp ranges.  Inside a warp range
 a maximal run of one (sequence, KV head) pair's items is a piece.  A piece
 that does not cover its pair from the first page to the last becomes a record:
 slot 1 if it is the last of two or more pieces of the warp's range, else slot
-0.  The pair's first piece writes the pair's header (its record, the warp that
-holds the pair's last page).  A warp whose range is empty marks its slot-0
-record empty.  The combine takes the header's record, then slot 0 of every
-later warp up to the last, skipping empty records.
+0.  A warp whose range is empty marks its slot-0 record empty.  The combine
+rederives, from the lengths alone, the warps holding a pair's first and last
+page-heads, takes the first warp's record (slot 1 unless the pair starts that
+warp's range), then slot 0 of every later warp up to the last, skipping empty
+records.
 
 This model replays that arithmetic (restated from the kernel's description,
 in Python) for many ragged batches and checks that each cut pair's records
@@ -49,7 +50,6 @@ def simulate(lens, hkv, nsm):
     items = [(b, h, pg) for b, n in enumerate(npg) for h in range(hkv) for pg in range(n)]
     W = len(items)
     records = {}      # record index -> (b, h, first page, last page) or "empty"
-    headers = {}      # (b, h) -> (record, last warp)
     outputs = set()
     if W == 0:
         return
@@ -75,33 +75,35 @@ def simulate(lens, hkv, nsm):
                 else:
                     assert 2 * gw + slot not in records
                     records[2 * gw + slot] = (b, h, page0, last_page)
-                if page0 == 0:
-                    hd = (0, 0)
-                    if not complete:
-                        hd = (2 * gw + slot, warp_of_item(wr0 + i + npg[b] - 1, W, N))
-                    headers[(b, h)] = hd
                 i = iend
+    before = 0
     for b, n in enumerate(npg):
         for h in range(hkv):
             if n == 0:
                 continue
-            x, y = headers[(b, h)]
-            gw_first = x >> 1
-            if y <= gw_first:
+            # the combine's view: from the lengths alone
+            p0 = before * hkv + h * n
+            wf, wl = warp_of_item(p0, W, N), warp_of_item(p0 + n - 1, W, N)
+            if wl == wf:
                 assert (b, h) in outputs
                 continue
             assert (b, h) not in outputs
+            cf = wf // NW
+            r0c, r1c = cta_start(cf, W, N), cta_start(cf + 1, W, N)
+            wr0 = r0c + (r1c - r0c) * (wf - cf * NW) // NW
+            first = 2 * wf + (1 if p0 > wr0 else 0)
             pages = []
-            for c in range(y - gw_first + 1):
-                ri = x if c == 0 else 2 * (gw_first + c)
+            for c in range(wl - wf + 1):
+                ri = first if c == 0 else 2 * (wf + c)
                 assert ri < 2 * N * NW                   # inside the workspace's records
                 rec = records[ri]
                 if rec == "empty":
                     continue
-                rb, rh, p0, p1 = rec
+                rb, rh, q0, q1 = rec
                 assert (rb, rh) == (b, h)
-                pages.extend(range(p0, p1 + 1))
+                pages.extend(range(q0, q1 + 1))
             assert pages == list(range(n))               # each page once, in order
+        before += n
 
 
 @pytest.mark.parametrize("seed", range(40))

@@ -64,6 +64,15 @@ def test_ragged_tails_empty_and_many_tiny_sequences(cuda_lib):
     _full_compare(_custom(lens, 32, 8, seed=5, pool_factor=1.3))
 
 
+@pytest.mark.parametrize("batch", [1024, 1025, 3000])
+def test_batches_past_the_combines_length_scan(cuda_lib, batch):
+    # up to 1024 sequences the combine works out where a cut pair's records
+    # are from the lengths; past that, from the page prefix the decode wrote
+    rng = np.random.default_rng(batch)
+    lens = list(rng.integers(0, 120, batch - 2)) + [3000, 0]
+    _full_compare(_custom(lens, 4, 2, seed=batch, pool_factor=1.2))
+
+
 def test_long_single_sequence_across_many_ctas(cuda_lib):
     _full_compare(_custom([65536 + 7], 8, 1, seed=11, append=True,
                           dist=inputs.KVDist("normal", 0.02, outlier=6.0, per_chunk=8)))

@@ -11,7 +11,7 @@ that call's bit for bit; one call is also checked against the oracle.  Between
 the two calls on the target workload the static entry point decodes another
 workload, whose (sequence, KV head) pairs are cut at other places, so the
 second call finds the scratch full of someone else's split records and
-headers.  This file is named to run last: the scratch is process-wide state.
+page prefixes.  This file is named to run last: the scratch is process-wide state.
 """
 import ctypes
 
@@ -85,11 +85,20 @@ def test_static_scratch_equals_workspace_decode_bit_for_bit(cuda_lib, index, sca
 
 def test_static_scratch_rejects_a_batch_that_does_not_fit(cuda_lib):
     lib = kv.load()
-    cache = kv.Cache.empty(4, 8, zero=True)
-    Hq = 8
-    B = 4096                         # grow the batch until its workspace exceeds the 32 MiB scratch
+    cache = kv.Cache.empty(4, 1, zero=True)
+    Hq = 1
+    # the scratch holds the split records and one page-prefix word per sequence:
+    # the smallest batch past 32 MiB
+    B = 1
     while kv.nvfp4kv_decode_workspace_size(cache, B, Hq) <= (32 << 20):
         B *= 2
+    lo = B // 2
+    while lo + 1 < B:
+        mid = (lo + B) // 2
+        if kv.nvfp4kv_decode_workspace_size(cache, mid, Hq) <= (32 << 20):
+            lo = mid
+        else:
+            B = mid
     q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((B, Hq, 128), dtype=torch.float32, device="cuda")
     pt = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
