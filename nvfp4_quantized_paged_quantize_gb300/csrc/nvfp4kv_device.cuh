@@ -128,6 +128,15 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// Correctly rounded a / b from r = RN(1 / b): q0 = RN(a r), then Markstein's
+// correction RN(q0 + r RN(a - b q0)) (two FMAs).  Valid while b, 1 / b and
+// the quotient stay well inside the normal range; the caller checks.
+__device__ __forceinline__ float div_markstein(float a, float b, float r) {
+  const float q0 = __fmul_rn(a, r);
+  const float rem = __fmaf_rn(-q0, b, a);
+  return __fmaf_rn(rem, r, q0);
+}
+
 // ---------------------------------------------------------------------------
 // V data by token pair
 // ---------------------------------------------------------------------------

@@ -82,15 +82,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
   f[6] = bf16_to_f32(x.w & 0xFFFFu); f[7] = bf16_to_f32(x.w >> 16);
 }
 
-// Correctly rounded a / b from r = RN(1 / b): q0 = RN(a r), then Markstein's
-// correction RN(q0 + r RN(a - b q0)) (two FMAs).  Valid while b, 1 / b and
-// the quotient stay well inside the normal range; the caller checks.
-__device__ __forceinline__ float div_markstein(float a, float b, float r) {
-  const float q0 = __fmul_rn(a, r);
-  const float rem = __fmaf_rn(-q0, b, a);
-  return __fmaf_rn(rem, r, q0);
-}
-
 // kWs: also write each row's FP8 workspace row, E4M3(fp32(x) / s_ws), at
 // ws_rows[token] (< 0: none) from the same registers.
 template <bool kWs>

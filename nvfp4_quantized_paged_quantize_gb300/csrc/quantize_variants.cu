@@ -18,7 +18,8 @@
 // takes the rows of one token pair (2q, 2q + 1) of one KV head: K of token 2q,
 // K of token 2q + 1, V of token 2q, V of token 2q + 1, so that V's token-pair
 // bytes can be written whole when the two slots are 2m and 2m + 1.  Block
-// scales divide exactly (IEEE); these are comparison paths, not the tuned one.
+// scales and quotients are correctly rounded (a reciprocal and one Markstein
+// correction, IEEE division outside its range), as in the NVFP4 append.
 #include "nvfp4kv_device.cuh"
 #include "nvfp4kv_launch.h"
 
@@ -44,30 +45,19 @@ constexpr int kThreads = 256;
 
 // E2M1 code of |y| < 6 (grid neighbours a <= |y| < b) rounded up with
 // probability (|y| - a) / (b - a): up iff 2 r + 1 < 512 (|y| - a) / (b - a).
-// Every gap is a power of two, so the scaled fraction is exact.
+// The grid's segments [0, 2), [2, 4), [4, 6) have gaps 0.5, 1, 2: with t =
+// (|y| - segment start) / gap, a is the segment start plus floor(t) gaps and
+// the scaled fraction is 512 (t - floor(t)), every step exact.  No branches.
 __device__ __forceinline__ uint32_t e2m1_code_sr(float y, uint32_t r) {
   const float m = fabsf(y);
-  uint32_t c;
-  if (m >= 6.0f) {
-    c = 7;
-  } else {
-    float a, inv_gap;  // lower neighbour and 1 / gap
-    if (m < 2.0f) {
-      c = (uint32_t)(m * 2.0f);  // 0 .. 3, exact
-      a = (float)c * 0.5f;
-      inv_gap = 2.0f;
-    } else if (m < 4.0f) {
-      c = m < 3.0f ? 4u : 5u;
-      a = m < 3.0f ? 2.0f : 3.0f;
-      inv_gap = 1.0f;
-    } else {
-      c = 6;
-      a = 4.0f;
-      inv_gap = 0.5f;
-    }
-    const float frac512 = (m - a) * inv_gap * 512.0f;  // exact
-    if ((float)(2 * r + 1) < frac512) ++c;
-  }
+  const bool s1 = m >= 2.0f, s2 = m >= 4.0f;
+  const float inv_gap = s2 ? 0.5f : (s1 ? 1.0f : 2.0f);
+  const float start = s2 ? 4.0f : (s1 ? 2.0f : 0.0f);
+  const uint32_t c0 = s2 ? 6u : (s1 ? 4u : 0u);
+  const float t = (m - start) * inv_gap;
+  const float k = floorf(t);
+  uint32_t c = c0 + (uint32_t)k + (((float)(2 * r + 1) < (t - k) * 512.0f) ? 1u : 0u);
+  c = m >= 6.0f ? 7u : c;
   return c | (__float_as_uint(y) >> 31 << 3);
 }
 
@@ -147,8 +137,17 @@ __global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParam
       hi |= e2m1x2_from_f32(__fmul_rn(f[8 + 2 * k], sc), __fmul_rn(f[8 + 2 * k + 1], sc)) << (8 * k);
   } else {
     const float g = tensor ? p.gv : p.gk;
-    sbyte = e4m3_from_f32(__fdiv_rn(amax, __fmul_rn(6.0f, g)));
+    const float t6 = __fmul_rn(6.0f, g), r6 = __frcp_rn(t6);
+    // Markstein while t6 and the first product stay well inside the normal range
+    // (a quotient below 2^-11 encodes as 0 either way)
+    const bool t6_ok = t6 >= 0x1p-100f && t6 <= 0x1p+100f && __fmul_rn(amax, r6) < 0x1p+64f;
+    sbyte = e4m3_from_f32(t6_ok ? div_markstein(amax, t6, r6) : __fdiv_rn(amax, t6));
     const float den = __fmul_rn(e4m3_to_f32(sbyte), g);
+    const float rcp = __frcp_rn(den);
+    // the sign of x / den is the sign of x (den > 0): restored where a quotient
+    // rounding to zero came out as +0
+    const bool fast = den >= 0x1p-100f && den <= 0x1p+100f && __fmul_rn(amax, rcp) < 0x1p+64f;
+    auto quot = [&](float x) { return fast ? copysignf(div_markstein(x, den, rcp), x) : __fdiv_rn(x, den); };
     if (den == 0.0f) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) lo |= (__float_as_uint(f[i]) >> 31) << (4 * i + 3);
@@ -160,17 +159,17 @@ __global__ void __launch_bounds__(kThreads) quantize_variant_kernel(VariantParam
       const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        lo |= e2m1_code_sr(__fdiv_rn(f[i], den), (rw[i >> 2] >> (8 * (i & 3))) & 0xFFu) << (4 * i);
+        lo |= e2m1_code_sr(quot(f[i]), (rw[i >> 2] >> (8 * (i & 3))) & 0xFFu) << (4 * i);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        hi |= e2m1_code_sr(__fdiv_rn(f[8 + i], den), (rw[2 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu) << (4 * i);
+        hi |= e2m1_code_sr(quot(f[8 + i]), (rw[2 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu) << (4 * i);
     } else {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        lo |= e2m1x2_from_f32(__fdiv_rn(f[2 * k], den), __fdiv_rn(f[2 * k + 1], den)) << (8 * k);
+        lo |= e2m1x2_from_f32(quot(f[2 * k]), quot(f[2 * k + 1])) << (8 * k);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        hi |= e2m1x2_from_f32(__fdiv_rn(f[8 + 2 * k], den), __fdiv_rn(f[8 + 2 * k + 1], den)) << (8 * k);
+        hi |= e2m1x2_from_f32(quot(f[8 + 2 * k]), quot(f[8 + 2 * k + 1])) << (8 * k);
     }
   }
   const int64_t slot = live ? __ldg(p.slots + token) : -1;
