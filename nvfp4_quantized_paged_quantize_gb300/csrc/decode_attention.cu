@@ -347,6 +347,25 @@ __device__ __forceinline__ void issue_two_pages(const LaneCopy& c, int ra, int r
       : "memory");
 }
 
+// Wait, warp-wide, for a ring stage: one try_wait per lane and a vote when
+// the data is there (the usual case); otherwise all lanes retry together
+// until the phase completes or about a second has passed (returns false).
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
+  if (__all_sync(0xFFFFFFFFu, done)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
+    if (__all_sync(0xFFFFFFFFu, done)) return true;
+    if (__shfl_sync(0xFFFFFFFFu, global_timer_ns() - t0 > 1000000000ull ? 1 : 0, 0)) return false;
+  }
+}
+
 // Per-warp attention state of the current pair.
 struct WarpState {
   float o[8][4];    // O^T tiles: tile i rows d = 16g+2i (c0,c1) and 16g+2i+1 (c2,c3), cols heads 2t,2t+1
@@ -768,6 +787,9 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
   __shared__ long long red[kNW];
   __shared__ int wstart_b[kNW], wstart_cu[kNW];
+  // per warp: (page-head row, valid tokens) of items [32 chunk, 32 chunk + 64),
+  // item k at k % 64, written as each 32-item chunk map is resolved
+  __shared__ int2 s_items[kNW][64];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -919,11 +941,11 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       nxt = map_chunk(p, wr0, 32, n, seq, lane);
       nres = false;
     }
-    // valid-page bits of the two chunk maps (bit l: item 32 chunk + l has a valid page)
-    uint32_t vcur = resolve_chunk(p, cur);
-    uint32_t vnxt = 0;
+    int2* const tab = s_items[warp];
+    resolve_chunk(p, cur);
+    tab[lane] = make_int2(cur.row, cur.nv);
+    __syncwarp();
 
-    bool ok = true;  // false after a wait gave up: stop waiting, computing and issuing
     // Launched right behind the append of the same decode step
     // (nvfp4kv_append_decode_attention), this grid ran everything above while
     // the append was still writing the new tokens' pages: wait for it before
@@ -934,8 +956,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     const LaneCopy lc = lane_copy<F>(p, lane);
     const uint32_t wring_u32 = smem_u32(wring);
     for (int j = 0; j < pre; ++j) {
-      const int row = __shfl_sync(0xFFFFFFFFu, cur.row, j);
-      issue_page_cpasync<F>(lc, row, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
+      issue_page_cpasync<F>(lc, tab[j].x, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
     }
     int issued = pre;
     int chunk = 0;   // the chunk `cur` maps
@@ -945,12 +966,18 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     load_q<F>(p, q_first, s, g, t);  // the first piece's q, fetched before the prefill
     int nseg = 0;
     int i = 0;
+    // resolve the next chunk's map into the item table
+#define NVFP4KV_RESOLVE_NXT()                                          \
+  {                                                                     \
+    resolve_chunk(p, nxt);                                              \
+    tab[(32 * (chunk + 1) + lane) & 63] = make_int2(nxt.row, nxt.nv);   \
+    __syncwarp();                                                       \
+  }
     // the chunk maps hold items [32 chunk, 32 chunk + 64): move them up to item k
 #define NVFP4KV_ADVANCE_TO(k)                                   \
   while (((k) >> 5) != chunk) {                                 \
-    if (!nres) vnxt = resolve_chunk(p, nxt);                    \
+    if (!nres) NVFP4KV_RESOLVE_NXT();                           \
     cur = nxt;                                                  \
-    vcur = vnxt;                                                \
     ++chunk;                                                    \
     nres = true;                                                \
     if ((chunk + 1) * 32 < n) {                                 \
@@ -958,8 +985,6 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       nres = false;                                             \
     }                                                           \
   }
-    // a field of item k (k in the two mapped chunks)
-#define NVFP4KV_ITEM(field, k) __shfl_sync(0xFFFFFFFFu, ((k) >> 5) == chunk ? cur.field : nxt.field, (k) & 31)
     while (i < n) {
       // ---- one piece: items [i, iend) of one (sequence, KV head) pair -------------
       NVFP4KV_ADVANCE_TO(i)
@@ -971,29 +996,29 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       ++nseg;
       if (nseg > 1) load_q<F>(p, fetch_q(p, pair, g, t), s, g, t);
       int j = i;
+      // the next item at which the chunk maps need work: the next chunk's start,
+      // or half way through this chunk while the next one's rows are unresolved
+#define NVFP4KV_NEXT_EVENT() (nres ? 32 * (chunk + 1) : min(32 * (chunk + 1), 32 * chunk + 16))
+      int ev = NVFP4KV_NEXT_EVENT();
       // two pages per step
       for (; j + 1 < iend; j += 2) {
-        NVFP4KV_ADVANCE_TO(j)
-        // the next chunk's rows are first needed at item 32 chunk + 32 - kStages - 1;
-        // resolving them half way through the chunk leaves their loads time to land
-        if (!nres && (j & 31) >= 16) {
-          vnxt = resolve_chunk(p, nxt);
-          nres = true;
+        if (j >= ev) {
+          NVFP4KV_ADVANCE_TO(j)
+          // the next chunk's rows are first needed at item 32 chunk + 32 - kStages - 1;
+          // resolving them half way through the chunk leaves their loads time to land
+          if (!nres && (j & 31) >= 16) {
+            NVFP4KV_RESOLVE_NXT();
+            nres = true;
+          }
+          ev = NVFP4KV_NEXT_EVENT();
         }
         const int st1 = st + 1 == kStages ? 0 : st + 1;
         const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
-        if (ok) {
-          // every lane waits; the outcome is made warp-uniform before it is used.
-          // The second stage's barrier fires only after each lane's earlier copies
-          // (those of the first stage) have landed too, so one wait covers both.
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(wbar + 8 * st1, ph1))) {
-            ok = false;
-            if (lane == 0) flag_error(p.status, kDevErrTimeout);
-          }
-        }
-        if (ok) {
-          const int nv0 = __shfl_sync(0xFFFFFFFFu, cur.nv, j & 31);
-          const int nv1 = NVFP4KV_ITEM(nv, j + 1);
+        // The second stage's barrier fires only after each lane's earlier copies
+        // (those of the first stage) have landed too, so one wait covers both.
+        if (!stage_wait(wbar + 8 * st1, ph1)) goto timed_out;
+        {
+          const int nv0 = tab[j & 63].y, nv1 = tab[(j + 1) & 63].y;
           const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + st1 * kStageBytes};
           const int nvs[2] = {nv0, nv1};
           if ((nv0 & nv1) == kPage)
@@ -1004,8 +1029,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
           // refill the freed stages with items j + kStages and j + 1 + kStages
           const int ja = j + kStages, jb = ja + 1;
           if (jb < n) {
-            const int ra = NVFP4KV_ITEM(row, ja);
-            const int rb = NVFP4KV_ITEM(row, jb);
+            const int ra = tab[ja & 63].x, rb = tab[jb & 63].x;
             if constexpr (F == kFmtMxfp4) {
               issue_page_cpasync<F>(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
               issue_page_cpasync<F>(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
@@ -1015,7 +1039,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
             }
             issued = jb + 1;
           } else if (ja < n) {
-            issue_page_cpasync<F>(lc, NVFP4KV_ITEM(row, ja), wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            issue_page_cpasync<F>(lc, tab[ja & 63].x, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
             issued = ja + 1;
           }
         }
@@ -1026,24 +1050,19 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         // the piece's last page on its own
         NVFP4KV_ADVANCE_TO(j)
         if (!nres && (j & 31) >= 16) {
-          vnxt = resolve_chunk(p, nxt);
+          NVFP4KV_RESOLVE_NXT();
           nres = true;
         }
-        if (ok) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(wbar + 8 * st, ph))) {
-            ok = false;
-            if (lane == 0) flag_error(p.status, kDevErrTimeout);
-          }
-        }
-        if (ok) {
-          const int nv0 = __shfl_sync(0xFFFFFFFFu, cur.nv, j & 31);
+        if (!stage_wait(wbar + 8 * st, ph)) goto timed_out;
+        {
+          const int nv0 = tab[j & 63].y;
           const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + st * kStageBytes};
           const int nvs[2] = {nv0, 0};
           if (nv0) process_pages<2, false, F>(stg, nvs, s, g, t);
           __syncwarp();
           const int ja = j + kStages;
           if (ja < n) {
-            issue_page_cpasync<F>(lc, NVFP4KV_ITEM(row, ja), wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            issue_page_cpasync<F>(lc, tab[ja & 63].x, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
             issued = ja + 1;
           }
         }
@@ -1051,15 +1070,9 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         ph = st == 0 ? ph ^ 1u : ph;
         ++j;
       }
-#undef NVFP4KV_ITEM
+#undef NVFP4KV_NEXT_EVENT
 #undef NVFP4KV_ADVANCE_TO
-      if (iend == n && !ok) {
-        // drain: wait (bounded) for every copy still in flight before the ring is reused
-        for (int jj = issued - kStages; jj < issued; ++jj) {
-          if (jj < 0) continue;
-          mbar_wait(wbar + 8 * (jj % kStages), (uint32_t)((jj / kStages) & 1));
-        }
-      }
+#undef NVFP4KV_RESOLVE_NXT
       __syncwarp();
       // a piece that ends before the warp range does is complete unless it is the
       // first; a cut piece becomes record 2 gwarp (the warp's first piece) or
@@ -1069,6 +1082,16 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       const int slot = (iend == n && nseg > 1) ? 1 : 0;
       finish_piece<F>(p, s, pair, complete, p.part + (2 * gwarp + slot) * kRecFloats, g, t);
       i = iend;
+    }
+    return;
+  timed_out:
+    // a wait gave up: flag it, wait (bounded) for every copy still in flight so
+    // that none lands after the warp has gone, and leave; the call's outputs
+    // are then unspecified, but every access stays in bounds
+    if (lane == 0) flag_error(p.status, kDevErrTimeout);
+    for (int jj = issued - kStages; jj < issued; ++jj) {
+      if (jj < 0) continue;
+      mbar_wait(wbar + 8 * (jj % kStages), (uint32_t)((jj / kStages) & 1));
     }
   }
 }
