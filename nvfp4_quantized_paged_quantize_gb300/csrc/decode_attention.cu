@@ -50,13 +50,13 @@ namespace {
 #define NVFP4KV_DECODE_WARPS 4
 #endif
 #ifndef NVFP4KV_DECODE_STAGES
-#define NVFP4KV_DECODE_STAGES 6
+#define NVFP4KV_DECODE_STAGES 4
 #endif
 #ifndef NVFP4KV_DECODE_CTAS_PER_SM
 #define NVFP4KV_DECODE_CTAS_PER_SM 3
 #endif
 #ifndef NVFP4KV_DECODE_QK_CHAINS
-#define NVFP4KV_DECODE_QK_CHAINS 2  // independent QK accumulator chains per page (1 or 2)
+#define NVFP4KV_DECODE_QK_CHAINS 1  // independent QK accumulator chains per page (1 or 2)
 #endif
 constexpr int kNW = NVFP4KV_DECODE_WARPS;              // warps per CTA (each streams its own pages)
 constexpr int kStages = NVFP4KV_DECODE_STAGES;         // ring stages per warp (2 pages in compute)
@@ -192,7 +192,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 // finish times but did not shorten the launch: the slowest warps are spread
 // over all SMs.)
 __device__ __forceinline__ long long cta_start(long long c, long long W, long long N) {
-  const long long q = W / N, rem = W % N;
+  // W < 2^31 (checked on the host): 32-bit division
+  const int q = (int)W / (int)N, rem = (int)W - q * (int)N;
   return c * q + (c < rem ? c : rem);
 }
 
@@ -289,64 +290,6 @@ __device__ __forceinline__ LaneCopy lane_copy(const DecodeParams& p, int lane) {
   return c;
 }
 
-template <int F>
-__device__ __forceinline__ void issue_page_cpasync(const LaneCopy& c, int row, uint32_t st, uint32_t bar,
-                                                   int lane) {
-  // predicated copies (no branch): nothing is copied for an invalid page (row < 0)
-  const uint8_t* src = c.src + (size_t)(row < 0 ? 0 : row) * ph_bytes(F);
-  const uint32_t dst = st + c.off;
-  const uint32_t v5 = (row >= 0 && c.fifth) ? 1u : 0u;
-  asm volatile(
-      "{\n .reg .pred p, q;\n"
-      " setp.ge.s32 p, %2, 0;\n"
-      " setp.ne.u32 q, %3, 0;\n"
-      " @p cp.async.cg.shared.global [%0], [%1], 16;\n"
-      " @p cp.async.cg.shared.global [%0+512], [%1+512], 16;\n"
-      " @p cp.async.cg.shared.global [%0+1024], [%1+1024], 16;\n"
-      " @p cp.async.cg.shared.global [%0+1536], [%1+1536], 16;\n"
-      " @q cp.async.cg.shared.global [%0+2048], [%1+2048], 16;\n"
-      // fires once all of this lane's earlier copies have landed (also for an
-      // invalid page, which copies nothing): a stage's barrier therefore covers
-      // every stage issued before it as well
-      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%4];\n"
-      "}\n" ::"r"(dst), "l"(src), "r"(row), "r"(v5), "r"(bar)
-      : "memory");
-}
-
-// Two NVFP4 page-heads (288 pieces of 16 bytes: 9 per lane), into stages a and
-// b: lane l copies pieces l + 32 k of the pair of page-heads, i.e. a's pieces
-// l, l + 32, l + 64, l + 96, then a's l + 128 (l < 16) or b's l - 16 (l >= 16),
-// then b's l + 16, l + 48, l + 80, l + 112; then arrives on both barriers.
-__device__ __forceinline__ void issue_two_pages(const LaneCopy& c, int ra, int rb, uint32_t sta, uint32_t stb,
-                                                uint32_t bara, uint32_t barb, int lane) {
-  const uint8_t* srca = c.src + (size_t)(ra < 0 ? 0 : ra) * kPageHeadBytes;
-  const uint8_t* srcb = c.src + (size_t)(rb < 0 ? 0 : rb) * kPageHeadBytes;
-  const uint32_t dsta = sta + c.off, dstb = stb + c.off;
-  const bool lo = lane < 16;
-  const uint32_t dst4 = lo ? dsta + 2048 : dstb - 256;
-  const uint8_t* src4 = lo ? srca + 2048 : srcb - 256;
-  const uint32_t v4 = (lo ? ra : rb) >= 0 ? 1u : 0u;
-  asm volatile(
-      "{\n .reg .pred pa, pb, p4;\n"
-      " setp.ge.s32 pa, %4, 0;\n"
-      " setp.ge.s32 pb, %5, 0;\n"
-      " setp.ne.u32 p4, %6, 0;\n"
-      " @pa cp.async.cg.shared.global [%0], [%2], 16;\n"
-      " @pa cp.async.cg.shared.global [%0+512], [%2+512], 16;\n"
-      " @pa cp.async.cg.shared.global [%0+1024], [%2+1024], 16;\n"
-      " @pa cp.async.cg.shared.global [%0+1536], [%2+1536], 16;\n"
-      " @p4 cp.async.cg.shared.global [%7], [%8], 16;\n"
-      " @pb cp.async.cg.shared.global [%1+256], [%3+256], 16;\n"
-      " @pb cp.async.cg.shared.global [%1+768], [%3+768], 16;\n"
-      " @pb cp.async.cg.shared.global [%1+1280], [%3+1280], 16;\n"
-      " @pb cp.async.cg.shared.global [%1+1792], [%3+1792], 16;\n"
-      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%9];\n"
-      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%10];\n"
-      "}\n" ::"r"(dsta), "r"(dstb), "l"(srca), "l"(srcb), "r"(ra), "r"(rb), "r"(v4), "r"(dst4), "l"(src4),
-      "r"(bara), "r"(barb)
-      : "memory");
-}
-
 // Wait, warp-wide, for a ring stage: one try_wait per lane and a vote when
 // the data is there (the usual case); otherwise all lanes retry together
 // until the phase completes or about a second has passed (returns false).
@@ -364,6 +307,74 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
     if (__all_sync(0xFFFFFFFFu, done)) return true;
     if (__shfl_sync(0xFFFFFFFFu, global_timer_ns() - t0 > 1000000000ull ? 1 : 0, 0)) return false;
   }
+}
+
+// An item of a warp's range as the loop uses it: the byte offset of its
+// page-head in the pool and its valid tokens (0: nothing to copy or attend).
+struct alignas(16) ItemEntry {
+  long long off;
+  int nv;
+  int pad;
+};
+
+// cp.async staging of one page-head at byte offset `off` of the pool: lane l
+// copies the 16-byte pieces l, l + 32, ... (NVFP4: lanes 0-15 five of the 144,
+// the others four; MXFP4: lanes 0-7 five of the 136), predicated, none when nv
+// is 0, then arrives (no-increment) on the stage's mbarrier, which expects 32
+// arrivals; it fires once all of the lane's earlier copies have landed, so a
+// stage's barrier covers every stage issued before it as well.
+template <int F>
+__device__ __forceinline__ void issue_page_off(const LaneCopy& c, long long off, int nv, uint32_t st, uint32_t bar) {
+  const uint8_t* src = c.src + off;
+  const uint32_t dst = st + c.off;
+  const uint32_t v5 = (nv > 0 && c.fifth) ? 1u : 0u;
+  asm volatile(
+      "{\n .reg .pred p, q;\n"
+      " setp.gt.s32 p, %2, 0;\n"
+      " setp.ne.u32 q, %3, 0;\n"
+      " @p cp.async.cg.shared.global [%0], [%1], 16;\n"
+      " @p cp.async.cg.shared.global [%0+512], [%1+512], 16;\n"
+      " @p cp.async.cg.shared.global [%0+1024], [%1+1024], 16;\n"
+      " @p cp.async.cg.shared.global [%0+1536], [%1+1536], 16;\n"
+      " @q cp.async.cg.shared.global [%0+2048], [%1+2048], 16;\n"
+      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%4];\n"
+      "}\n" ::"r"(dst), "l"(src), "r"(nv), "r"(v5), "r"(bar)
+      : "memory");
+}
+
+// Two NVFP4 page-heads (288 pieces of 16 bytes: 9 per lane), into stages a and
+// b: lane l copies pieces l + 32 k of the pair of page-heads, i.e. a's pieces
+// l, l + 32, l + 64, l + 96, then a's l + 128 (l < 16) or b's l - 16 (l >= 16),
+// then b's l + 16, l + 48, l + 80, l + 112; then arrives on both barriers.
+// Nothing is copied for an entry with no valid tokens (a bad page id).
+__device__ __forceinline__ void issue_two_off(const LaneCopy& c, const ItemEntry& a, const ItemEntry& b,
+                                              uint32_t sta, uint32_t stb, uint32_t bara, uint32_t barb,
+                                              bool lo) {
+  const uint8_t* srca = c.src + a.off;
+  const uint8_t* srcb = c.src + b.off;
+  const uint32_t dsta = sta + c.off, dstb = stb + c.off;
+  const uint32_t dst4 = lo ? dsta + 2048 : dstb - 256;
+  const uint8_t* src4 = lo ? srca + 2048 : srcb - 256;
+  const int n4 = lo ? a.nv : b.nv;
+  asm volatile(
+      "{\n .reg .pred pa, pb, p4;\n"
+      " setp.gt.s32 pa, %4, 0;\n"
+      " setp.gt.s32 pb, %5, 0;\n"
+      " setp.gt.s32 p4, %6, 0;\n"
+      " @pa cp.async.cg.shared.global [%0], [%2], 16;\n"
+      " @pa cp.async.cg.shared.global [%0+512], [%2+512], 16;\n"
+      " @pa cp.async.cg.shared.global [%0+1024], [%2+1024], 16;\n"
+      " @pa cp.async.cg.shared.global [%0+1536], [%2+1536], 16;\n"
+      " @p4 cp.async.cg.shared.global [%7], [%8], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+256], [%3+256], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+768], [%3+768], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+1280], [%3+1280], 16;\n"
+      " @pb cp.async.cg.shared.global [%1+1792], [%3+1792], 16;\n"
+      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%9];\n"
+      " cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%10];\n"
+      "}\n" ::"r"(dsta), "r"(dstb), "l"(srca), "l"(srcb), "r"(a.nv), "r"(b.nv), "r"(n4), "r"(dst4), "l"(src4),
+      "r"(bara), "r"(barb)
+      : "memory");
 }
 
 // Per-warp attention state of the current pair.
@@ -490,7 +501,8 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, const QRaw& raw, W
 }
 
 // Phase 1 of a step: S^T = Khat q^T for NP pages (16 tokens x G heads each),
-// two independent accumulator chains per page (tiles 0-3 and 4-7).
+// one accumulator chain per page (or two, tiles 0-3 and 4-7, with
+// NVFP4KV_DECODE_QK_CHAINS 2: shorter chains, four more adds per page).
 // MXFP4 pages carry their scales relative to the page's largest exponent (per
 // K and per V, so every product stays inside f16): kx[k] = 2^(K's largest)
 // multiplies the page's scores, ve[k] (V's largest) enters the softmax exponent.
@@ -789,7 +801,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
   __shared__ int wstart_b[kNW], wstart_cu[kNW];
   // per warp: (page-head row, valid tokens) of items [32 chunk, 32 chunk + 64),
   // item k at k % 64, written as each 32-item chunk map is resolved
-  __shared__ int2 s_items[kNW][64];
+  __shared__ ItemEntry s_items[kNW][64];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -941,9 +953,17 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
       nxt = map_chunk(p, wr0, 32, n, seq, lane);
       nres = false;
     }
-    int2* const tab = s_items[warp];
+    ItemEntry* const tab = s_items[warp];
+    // an item's entry: computed by its lane once per chunk, used by the loop
+    auto entry_of = [&](const ItemMap& m) {
+      ItemEntry e;
+      e.off = m.row < 0 ? 0 : (long long)m.row * ph_bytes(F);
+      e.nv = m.nv;
+      e.pad = 0;
+      return e;
+    };
     resolve_chunk(p, cur);
-    tab[lane] = make_int2(cur.row, cur.nv);
+    tab[lane] = entry_of(cur);
     __syncwarp();
 
     // Launched right behind the append of the same decode step
@@ -956,7 +976,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
     const LaneCopy lc = lane_copy<F>(p, lane);
     const uint32_t wring_u32 = smem_u32(wring);
     for (int j = 0; j < pre; ++j) {
-      issue_page_cpasync<F>(lc, tab[j].x, wring_u32 + j * kStageBytes, wbar + 8 * j, lane);
+      issue_page_off<F>(lc, tab[j].off, tab[j].nv, wring_u32 + j * kStageBytes, wbar + 8 * j);
     }
     int issued = pre;
     int chunk = 0;   // the chunk `cur` maps
@@ -970,7 +990,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
 #define NVFP4KV_RESOLVE_NXT()                                          \
   {                                                                     \
     resolve_chunk(p, nxt);                                              \
-    tab[(32 * (chunk + 1) + lane) & 63] = make_int2(nxt.row, nxt.nv);   \
+    tab[(32 * (chunk + 1) + lane) & 63] = entry_of(nxt);                \
     __syncwarp();                                                       \
   }
     // the chunk maps hold items [32 chunk, 32 chunk + 64): move them up to item k
@@ -1018,7 +1038,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         // (those of the first stage) have landed too, so one wait covers both.
         if (!stage_wait(wbar + 8 * st1, ph1)) goto timed_out;
         {
-          const int nv0 = tab[j & 63].y, nv1 = tab[(j + 1) & 63].y;
+          const int nv0 = tab[j & 63].nv, nv1 = tab[(j + 1) & 63].nv;
           const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + st1 * kStageBytes};
           const int nvs[2] = {nv0, nv1};
           if ((nv0 & nv1) == kPage)
@@ -1029,17 +1049,17 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
           // refill the freed stages with items j + kStages and j + 1 + kStages
           const int ja = j + kStages, jb = ja + 1;
           if (jb < n) {
-            const int ra = tab[ja & 63].x, rb = tab[jb & 63].x;
+            const ItemEntry ea = tab[ja & 63], eb = tab[jb & 63];
             if constexpr (F == kFmtMxfp4) {
-              issue_page_cpasync<F>(lc, ra, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
-              issue_page_cpasync<F>(lc, rb, wring_u32 + st1 * kStageBytes, wbar + 8 * st1, lane);
+              issue_page_off<F>(lc, ea.off, ea.nv, wring_u32 + st * kStageBytes, wbar + 8 * st);
+              issue_page_off<F>(lc, eb.off, eb.nv, wring_u32 + st1 * kStageBytes, wbar + 8 * st1);
             } else {
-              issue_two_pages(lc, ra, rb, wring_u32 + st * kStageBytes, wring_u32 + st1 * kStageBytes,
-                              wbar + 8 * st, wbar + 8 * st1, lane);
+              issue_two_off(lc, ea, eb, wring_u32 + st * kStageBytes, wring_u32 + st1 * kStageBytes,
+                            wbar + 8 * st, wbar + 8 * st1, lane < 16);
             }
             issued = jb + 1;
           } else if (ja < n) {
-            issue_page_cpasync<F>(lc, tab[ja & 63].x, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            issue_page_off<F>(lc, tab[ja & 63].off, tab[ja & 63].nv, wring_u32 + st * kStageBytes, wbar + 8 * st);
             issued = ja + 1;
           }
         }
@@ -1055,14 +1075,14 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm) decode_kernel(const Deco
         }
         if (!stage_wait(wbar + 8 * st, ph)) goto timed_out;
         {
-          const int nv0 = tab[j & 63].y;
+          const int nv0 = tab[j & 63].nv;
           const uint8_t* const stg[2] = {wring + st * kStageBytes, wring + st * kStageBytes};
           const int nvs[2] = {nv0, 0};
           if (nv0) process_pages<2, false, F>(stg, nvs, s, g, t);
           __syncwarp();
           const int ja = j + kStages;
           if (ja < n) {
-            issue_page_cpasync<F>(lc, tab[ja & 63].x, wring_u32 + st * kStageBytes, wbar + 8 * st, lane);
+            issue_page_off<F>(lc, tab[ja & 63].off, tab[ja & 63].nv, wring_u32 + st * kStageBytes, wbar + 8 * st);
             issued = ja + 1;
           }
         }

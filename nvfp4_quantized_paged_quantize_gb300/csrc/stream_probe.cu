@@ -23,7 +23,8 @@ namespace {
 
 constexpr int kNW = 4;              // decode pattern: warps per CTA, as the decode
 constexpr int kCtasPerSm = 3;       // decode pattern: CTAs per SM, as the decode
-constexpr int kStages = 6;          // ring stages per warp (decode pattern) or per CTA (whole pages)
+constexpr int kStages = 4;          // decode pattern: ring stages per warp, as the decode
+constexpr int kPageStages = 6;      // whole pages: ring stages per CTA
 constexpr int kPageCtasPerSm = 2;   // whole pages: CTAs (one warp each) per SM
 constexpr int kMaxPageBytes = 16 * kPageHeadBytes;  // whole pages: up to 16 KV heads per stage
 
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kNW * 32) probe_decode_pattern(const ProbePara
 // Whole pages: one warp per CTA streams its range of pages with bulk copies.
 __global__ void __launch_bounds__(32) probe_whole_pages(const ProbeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ __align__(8) uint64_t bars[kPageStages];
   const int lane = threadIdx.x;
   long long W;
   int b, cu;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(32) probe_whole_pages(const ProbeParams p) {
   locate(p, 1, r0, &Wd, &b, &cu);
   const uint32_t bytes = (uint32_t)p.hkv * kPageHeadBytes;
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(bars + s), 1);
+    for (int s = 0; s < kPageStages; ++s) mbar_init(smem_u32(bars + s), 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -202,39 +203,39 @@ __global__ void __launch_bounds__(32) probe_whole_pages(const ProbeParams p) {
   auto issue = [&](int i) {
     const int id = unit_page(p, r0 + i, 1, b, cu, np, &head);  // lane-uniform
     if (lane != 0) return;
-    const uint32_t bar = smem_u32(bars + i % kStages);
+    const uint32_t bar = smem_u32(bars + i % kPageStages);
     if (id >= 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
       asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                   ::"r"(smem_u32(smem + (size_t)(i % kStages) * bytes)),
+                   ::"r"(smem_u32(smem + (size_t)(i % kPageStages) * bytes)),
                    "l"(p.pages + (size_t)id * bytes), "r"(bytes), "r"(bar)
                    : "memory");
     } else {
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
     }
   };
-  const int pre = n < kStages ? n : kStages;
+  const int pre = n < kPageStages ? n : kPageStages;
   for (int i = 0; i < pre; ++i) issue(i);
   int issued = pre;
   bool ok = true;
   for (int i = 0; i < n; ++i) {
-    const bool done = mbar_wait(smem_u32(bars + i % kStages), (uint32_t)((i / kStages) & 1));
+    const bool done = mbar_wait(smem_u32(bars + i % kPageStages), (uint32_t)((i / kPageStages) & 1));
     if (!__all_sync(0xFFFFFFFFu, done)) {
       ok = false;
       if (lane == 0) flag_error(p.status, kDevErrTimeout);
       break;
     }
-    acc ^= *reinterpret_cast<const uint32_t*>(smem + (size_t)(i % kStages) * bytes + 4 * lane);
+    acc ^= *reinterpret_cast<const uint32_t*>(smem + (size_t)(i % kPageStages) * bytes + 4 * lane);
     __syncwarp();
-    if (i + kStages < n) {
-      issue(i + kStages);
-      issued = i + kStages + 1;
+    if (i + kPageStages < n) {
+      issue(i + kPageStages);
+      issued = i + kPageStages + 1;
     }
   }
   if (!ok) {
-    for (int j = issued - kStages; j < issued; ++j)
-      if (j >= 0) mbar_wait(smem_u32(bars + j % kStages), (uint32_t)((j / kStages) & 1));
+    for (int j = issued - kPageStages; j < issued; ++j)
+      if (j >= 0) mbar_wait(smem_u32(bars + j % kPageStages), (uint32_t)((j / kPageStages) & 1));
   }
   if (acc != 0) atomicXor(p.sink, acc);
 }
@@ -263,11 +264,11 @@ cudaError_t launch_stream_probe(const nvfp4kv_cache& c, const int32_t* page_tabl
     if (e != cudaSuccess) return e;
     probe_decode_pattern<<<num_sms * kCtasPerSm, kNW * 32, smem, stream>>>(p);
   } else {
-    const int smem = kStages * c.num_kv_heads * kPageHeadBytes;
+    const int smem = kPageStages * c.num_kv_heads * kPageHeadBytes;
     static PerDeviceOnce once;
     const cudaError_t e = once.run([] {
       return cudaFuncSetAttribute(probe_whole_pages, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kStages * kMaxPageBytes);
+                                  kPageStages * kMaxPageBytes);
     });
     if (e != cudaSuccess) return e;
     probe_whole_pages<<<num_sms * kPageCtasPerSm, 32, smem, stream>>>(p);
