@@ -10,23 +10,29 @@
 //
 // extend_attention_kernel: causal attention of the chunk's queries over their
 // sequence's workspace rows (key j = row cu_prefix[b] + j; chunk token t sees
-// keys 0 .. prefix + t), on the fifth-generation tensor cores.
+// keys 0 .. prefix + t), on the fifth-generation tensor cores, run by CTA
+// pairs (clusters of two, on two SMs) with the pair form of the MMA.
 //   - A CTA owns 128 query rows of one (sequence, KV head): 128 / G tokens x
-//     the G query heads that share the KV head, so each K/V tile feeds all G.
-//   - Warps 4-7 write the Q rows (f16) into TMEM, then load K/V tiles of 128
-//     keys (one tile ahead, into registers), convert E4M3 -> f16 (exact) and
-//     store them as B operands in shared memory (K K-major, V MN-major) in a
-//     three-stage ring.
-//   - Warp 8 issues, from one thread, S = Q K^T and O += P V with the A
-//     operand (Q, P) read from TMEM and f32 accumulators in TMEM (two S
-//     buffers, one O), and commits each to an mbarrier.  Only the B operands
-//     pass through shared memory.
+//     the G query heads that share the KV head, so each K/V tile feeds all G;
+//     a pair owns two adjacent such m-tiles (256 rows).
+//   - Warps 4-7 of each CTA write its Q rows (f16) into its TMEM, then load
+//     its half of each K/V tile of 128 keys (one tile ahead, into registers):
+//     keys 64 rank .. +63 of K and head dims 64 rank .. +63 of V, convert E4M3
+//     -> f16 (exact) and store them as B operands in shared memory (K K-major,
+//     V MN-major) in a six-stage ring.  Each K/V byte is converted once per
+//     256 query rows.
+//   - Warp 8 of rank 0 issues, from one thread, S = Q K^T and O += P V for
+//     the pair (M = 256): A (Q, P) is read from each CTA's TMEM, B from both
+//     CTAs' halves, f32 accumulators land in each CTA's TMEM (two S buffers,
+//     one O); each group is committed to the mbarrier of that name in both
+//     CTAs.
 //   - Warps 0-3 own one query row per thread (TMEM lane = row): they read the
 //     S row, mask, run a lazy base-2 online softmax (the running max moves
 //     only when it grows by 2^8, rescaling O in TMEM), and write P (f16) into
 //     TMEM.  At the end: O * s_ws(V) / l -> fp32 out.
 // Every wait is bounded: a stalled pipeline flags NVFP4KV_DEVERR_TIMEOUT,
-// drains its MMAs and frees its TMEM.
+// drains its MMAs, and both CTAs meet at a cluster barrier before freeing
+// their TMEM.
 #include "nvfp4kv_device.cuh"
 #include "nvfp4kv_launch.h"
 #include "fp8_quotient.cuh"
@@ -91,18 +97,22 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_to_ws_kernel(ChunkParams 
 // extend attention
 // ---------------------------------------------------------------------------
 
-constexpr int kTileM = 128;  // query rows per CTA (TMEM lanes)
-constexpr int kTileN = 128;  // keys per K/V tile
+constexpr int kTileM = 128;          // query rows per CTA (TMEM lanes); a CTA pair takes 256
+constexpr int kTileN = 128;          // keys per K/V tile
+constexpr int kHalfN = kTileN / 2;   // keys of K, and head dims of V, that each CTA of the pair stages
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 4;
 constexpr int kThreads = (kSoftmaxWarps + kLoadWarps + 1) * 32;  // + the MMA warp
 constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
 constexpr uint32_t kLBO = 128;   // next core matrix along K
-constexpr uint32_t kSBO = 2048;  // next 8-row (M / N) group: 16 core matrices of 128 B
-constexpr uint32_t kTileBytes = kTileM * kHeadDim * 2;  // one f16 operand tile, 32 KB
-constexpr int kStages = 3;                              // K / V ring depth
-constexpr uint32_t kOffK = 0, kOffV = kStages * kTileBytes;
-constexpr uint32_t kSmemBytes = 2 * kStages * kTileBytes;  // 192 KB: one CTA per SM
+constexpr uint32_t kSBO = 2048;  // next 8-row (N) group: 16 core matrices of 128 B
+constexpr uint32_t kHalfBytes = kHalfN * kHeadDim * 2;  // a CTA's half of one f16 B tile, 16 KB
+#ifndef NVFP4KV_EXTEND_STAGES
+#define NVFP4KV_EXTEND_STAGES 6
+#endif
+constexpr int kStages = NVFP4KV_EXTEND_STAGES;  // K / V ring depth
+constexpr uint32_t kOffK = 0, kOffV = kStages * kHalfBytes;
+constexpr uint32_t kSmemBytes = 2 * kStages * kHalfBytes;  // 192 KB at 6 stages: one CTA per SM
 // TMEM columns: S[0] 0-127, S[1] 128-255, O 256-383 (f32); Q 384-447 and
 // P 448-511 (f16 pairs: the A operands of S = Q K^T and O += P V)
 constexpr uint32_t kTmemCols = 512;
@@ -139,8 +149,55 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// One arrival, released at cluster scope, on the mbarrier of cluster rank 0
+// that sits at this shared-memory offset.
+__device__ __forceinline__ void arrive_rank0(uint32_t bar) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(bar));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Every thread of both CTAs: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return done;
+}
+
+// Wait (acquire at cluster scope: the arrivals may come from the other CTA)
+// until the phase of the given parity completes; false after about `limit_ns`.
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// The same for a whole warp, with one outcome for all its lanes.
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (__all_sync(0xFFFFFFFFu, try_wait_cluster(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (__all_sync(0xFFFFFFFFu, try_wait_cluster(bar, parity))) return true;
+    if (__shfl_sync(0xFFFFFFFFu, global_timer_ns() - t0 > limit_ns ? 1 : 0, 0)) return false;
+  }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -178,16 +235,19 @@ struct Barriers {
   uint64_t drain;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Barriers bars;
   __shared__ uint32_t s_tmem;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // blockIdx.x & 1
   const int b = blockIdx.y, hk = blockIdx.z;
   const int tokens_per_tile = kTileM >> p.log2_group;
-  const int mt = (int)gridDim.x - 1 - (int)blockIdx.x;  // the longest tiles first
-  const int t0 = mt * tokens_per_tile;
+  // the pair takes m-tiles 2 mp (rank 0) and 2 mp + 1 (rank 1), the latest (longest) pairs first
+  const int mp = (int)(gridDim.x >> 1) - 1 - (int)(blockIdx.x >> 1);
+  const int tp = 2 * mp * tokens_per_tile;                  // the pair's first token
+  const int t0 = tp + (int)rank * tokens_per_tile;          // this CTA's first token
 
   // the sequence: chunk length C, prefix P, first workspace row
   const int64_t q0 = __ldg(p.cu_q + b);
@@ -199,9 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
     C = C < 0 ? 0 : (C > p.max_q_len ? p.max_q_len : C);
     P = P < 0 ? 0 : P;
   }
-  if (t0 >= C) return;  // no query of this tile: the whole CTA leaves before any set-up
-  const int64_t t_hi = (t0 + tokens_per_tile < C ? t0 + tokens_per_tile : C) - 1;
-  const int64_t nkeys = P + t_hi + 1;  // keys 0 .. P + t_hi
+  // no query in the pair: both CTAs leave before any set-up (the test is the same in both)
+  if (tp >= C) return;
+  const int64_t t_hi = (tp + 2 * tokens_per_tile < C ? tp + 2 * tokens_per_tile : C) - 1;
+  const int64_t nkeys = P + t_hi + 1;  // keys 0 .. P + t_hi: the pair's last query sees them all
   const int ntiles = (int)((nkeys + kTileN - 1) / kTileN);
 
   const uint32_t sbase = smem_u32(smem);
@@ -211,22 +272,26 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
   const uint32_t b_s[2] = {smem_u32(&bars.s_full[0]), smem_u32(&bars.s_full[1])};
   const uint32_t b_drain = smem_u32(&bars.drain);
 
+  // Rank 0's q_full, kv_full and p_full take one arrival per loader or softmax
+  // warp of both CTAs; s_full, o_done and kv_empty in both CTAs are arrived on
+  // by rank 0's MMA commits, multicast to the pair.
   if (threadIdx.x == 0) {
-    mbar_init(b_q, kLoadWarps * 32);
+    mbar_init(b_q, 2 * kLoadWarps);
     for (int st = 0; st < kStages; ++st) {
-      mbar_init(b_kvf0 + 8 * st, kLoadWarps * 32);
+      mbar_init(b_kvf0 + 8 * st, 2 * kLoadWarps);
       mbar_init(b_kve0 + 8 * st, 1);
     }
     mbar_init(b_s[0], 1);
     mbar_init(b_s[1], 1);
-    mbar_init(b_p, kSoftmaxWarps * 32);
+    mbar_init(b_p, 2 * kSoftmaxWarps);
     mbar_init(b_o, 1);
     mbar_init(b_drain, 1);
     fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  // both CTAs' barriers and TMEM exist before either CTA signals the other
   tc::fence_before_sync();
-  __syncthreads();
+  cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
   const int G = p.group;
@@ -234,17 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
   if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
     // ------------------------------------------------------------ loaders
     const int l = threadIdx.x - kSoftmaxWarps * 32;  // 0 .. 127
-    // K / V tiles: lane (key 8 g + (lane & 7), part lane >> 3) of a warp's 32 keys;
-    // a tile's 16-byte loads are issued one step ahead (into registers) so that
-    // their latency overlaps the wait for the stage they go to
+    // This CTA's half of each tile: K rows (keys) 64 rank .. 64 rank + 63 and V
+    // columns (head dims) 64 rank .. 64 rank + 63 of all 128 keys.  Lane parts:
+    //   K: key 16 lw + 8 g + (lane & 7) of the half (g < 2), bytes 16 part + 64 h (h < 2)
+    //   V: key 32 lw + 8 g + (lane & 7) (g < 4), bytes 64 rank + 16 part
+    // A tile's 16-byte loads are issued one step ahead (into registers) so that
+    // their latency overlaps the wait for the stage they go to.
     const int lw = warp - kSoftmaxWarps;
     const int part = lane >> 3;
-    uint4 xk[4][2], xv[4][2];
+    uint4 xk[2][2], xv[4];
     auto load_tile = [&](int i) {
+      const int64_t base = (int64_t)i * kTileN;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int key = lw * 32 + g * 8 + (lane & 7);
-        const int64_t j = (int64_t)i * kTileN + key;
+      for (int g = 0; g < 2; ++g) {
+        const int64_t j = base + kHalfN * (int)rank + lw * 16 + g * 8 + (lane & 7);
         const int64_t row = row0 + j;
         bool live = j < nkeys;
         if (live && (row < 0 || row >= p.total_rows)) {
@@ -253,10 +321,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
         }
         const int64_t off = (row * p.hkv + hk) * kHeadDim + part * 16;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2; ++h)
           xk[g][h] = live ? __ldg(reinterpret_cast<const uint4*>(p.ws_k + off + h * 64)) : make_uint4(0, 0, 0, 0);
-          xv[g][h] = live ? __ldg(reinterpret_cast<const uint4*>(p.ws_v + off + h * 64)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int64_t j = base + lw * 32 + g * 8 + (lane & 7);
+        const int64_t row = row0 + j;
+        bool live = j < nkeys;
+        if (live && (row < 0 || row >= p.total_rows)) {
+          flag_error(p.status, NVFP4KV_DEVERR_ROW);
+          live = false;
         }
+        const int64_t off = (row * p.hkv + hk) * kHeadDim + kHalfN * (int)rank + part * 16;
+        xv[g] = live ? __ldg(reinterpret_cast<const uint4*>(p.ws_v + off)) : make_uint4(0, 0, 0, 0);
       }
     };
     load_tile(0);
@@ -282,74 +360,81 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
         tc::tmem_st32(tq + 32 * half, w);
       }
       tc::fence_before_sync();
-      mbar_arrive(b_q);
+      __syncwarp();
+      if (lane == 0) arrive_rank0(b_q);
     }
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % kStages;
-      if (i >= kStages && !mbar_wait(b_kve0 + 8 * s, ((i / kStages) - 1) & 1, kWaitNs)) {
+      if (i >= kStages && !warp_wait_cluster(b_kve0 + 8 * s, ((i / kStages) - 1) & 1, kWaitNs)) {
         ok = false;
         break;
       }
-      const uint32_t sK = sK0 + s * kTileBytes, sV = sV0 + s * kTileBytes;
+      const uint32_t sK = sK0 + s * kHalfBytes, sV = sV0 + s * kHalfBytes;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int key = lw * 32 + g * 8 + (lane & 7);
+      for (int g = 0; g < 2; ++g) {
+        const int key = lw * 16 + g * 8 + (lane & 7);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int d0 = h * 64 + part * 16;
           st_shared_v4(sK + kmajor_off(key, d0), e4m3x8_to_f16x8(xk[g][h].x, xk[g][h].y));
           st_shared_v4(sK + kmajor_off(key, d0 + 8), e4m3x8_to_f16x8(xk[g][h].z, xk[g][h].w));
-          st_shared_v4(sV + mnmajor_off(d0, key), e4m3x8_to_f16x8(xv[g][h].x, xv[g][h].y));
-          st_shared_v4(sV + mnmajor_off(d0 + 8, key), e4m3x8_to_f16x8(xv[g][h].z, xv[g][h].w));
         }
       }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int key = lw * 32 + g * 8 + (lane & 7);
+        st_shared_v4(sV + mnmajor_off(part * 16, key), e4m3x8_to_f16x8(xv[g].x, xv[g].y));
+        st_shared_v4(sV + mnmajor_off(part * 16 + 8, key), e4m3x8_to_f16x8(xv[g].z, xv[g].w));
+      }
       tc::fence_smem_to_async();
-      mbar_arrive(b_kvf0 + 8 * s);
+      __syncwarp();
+      if (lane == 0) arrive_rank0(b_kvf0 + 8 * s);
       if (i + 1 < ntiles) load_tile(i + 1);
     }
     if (!ok) flag_error(p.status, NVFP4KV_DEVERR_TIMEOUT);
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t id_qk = tc::idesc_f16_f32(kTileM, kTileN, false, false);
-      constexpr uint32_t id_pv = tc::idesc_f16_f32(kTileM, kHeadDim, false, true);
-      bool ok = mbar_wait(b_q, 0, kWaitNs);
+    // ------------------------------------------------------------ MMA issue (rank 0)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t id_qk = tc::idesc_f16_f32(2 * kTileM, kTileN, false, false);
+      constexpr uint32_t id_pv = tc::idesc_f16_f32(2 * kTileM, kHeadDim, false, true);
+      bool ok = wait_cluster(b_q, 0, kWaitNs);
       for (int i = 0; i <= ntiles && ok; ++i) {
         if (i < ntiles) {
           const int s = i % kStages;
-          if (!mbar_wait(b_kvf0 + 8 * s, (i / kStages) & 1, kWaitNs)) {
+          if (!wait_cluster(b_kvf0 + 8 * s, (i / kStages) & 1, kWaitNs)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t sK = sK0 + s * kTileBytes;
+          const uint32_t sK = sK0 + s * kHalfBytes;
 #pragma unroll
           for (int kk = 0; kk < kHeadDim / 16; ++kk)
             tc::mma_f16_tmem_a(tmem + (i & 1) * kTileN, tmem + kTmemQ + kk * 8, tc::smem_desc(sK + kk * 256, kLBO, kSBO),
                                id_qk, kk > 0);
-          tc::commit(b_s[i & 1]);
+          tc::commit_multicast(b_s[i & 1], 3);
         }
         if (i >= 1) {
           const int pi = i - 1;  // P V of the previous tile
-          if (!mbar_wait(b_p, pi & 1, kWaitNs)) {
+          if (!wait_cluster(b_p, pi & 1, kWaitNs)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t sV = sV0 + (pi % kStages) * kTileBytes;
+          const uint32_t sV = sV0 + (pi % kStages) * kHalfBytes;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
             tc::mma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8, tc::smem_desc(sV + kk * 256, kLBO, kSBO), id_pv,
                                (pi > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(b_o);
-          if (pi + kStages < ntiles) tc::commit(b_kve0 + 8 * (pi % kStages));  // a loader waits for this stage
+          tc::commit_multicast(b_o, 3);
+          // the loaders of both CTAs wait for this stage
+          if (pi + kStages < ntiles) tc::commit_multicast(b_kve0 + 8 * (pi % kStages), 3);
         }
       }
       if (!ok) flag_error(p.status, NVFP4KV_DEVERR_TIMEOUT);
-      // nothing this thread issued may still be running when the TMEM is freed
+      // nothing this thread issued may still be running when either CTA frees its TMEM
       tc::commit(b_drain);
-      mbar_wait(b_drain, 0, kWaitNs);
+      wait_cluster(b_drain, 0, kWaitNs);
     }
     __syncwarp();
   } else {
@@ -362,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
-      if (!mbar_wait(b_s[i & 1], (i >> 1) & 1, kWaitNs)) {
+      if (!warp_wait_cluster(b_s[i & 1], (i >> 1) & 1, kWaitNs)) {
         ok = false;
         break;
       }
@@ -412,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
       const float lt = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (i >= 1) {
         // the previous P V must be done before P is overwritten and O rescaled
-        if (!mbar_wait(b_o, (i - 1) & 1, kWaitNs)) {
+        if (!warp_wait_cluster(b_o, (i - 1) & 1, kWaitNs)) {
           ok = false;
           break;
         }
@@ -435,9 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
       tc::tmem_st32(tmem + lane_base + kTmemP, *reinterpret_cast<const uint32_t(*)[32]>(&ph[0]));
       tc::tmem_st32(tmem + lane_base + kTmemP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&ph[32]));
       tc::fence_before_sync();
-      mbar_arrive(b_p);
+      __syncwarp();
+      if (lane == 0) arrive_rank0(b_p);
     }
-    if (ok && mbar_wait(b_o, (ntiles - 1) & 1, kWaitNs)) {
+    if (ok && warp_wait_cluster(b_o, (ntiles - 1) & 1, kWaitNs)) {
       tc::fence_after_sync();
       const float inv = live && l > 0.0f ? p.out_scale / l : 0.0f;
       float4* dst = reinterpret_cast<float4*>(
@@ -457,8 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_attention_kernel(ExtendPar
       flag_error(p.status, NVFP4KV_DEVERR_TIMEOUT);
     }
   }
+  // Both CTAs are done with the pair's TMEM and barriers (rank 0's MMAs
+  // drained, every signal to the other CTA sent) before either frees or leaves.
   tc::fence_before_sync();
-  __syncthreads();
+  cluster_sync();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
@@ -525,8 +613,9 @@ cudaError_t launch_extend_attention(const uint16_t* q, const int64_t* cu_q, int3
     return cudaFuncSetAttribute(extend_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr != cudaSuccess) return attr;
+  // CTA pairs (clusters of two along x): an even number of m-tiles
   const int64_t tiles = ((int64_t)max_q_len * p.group + kTileM - 1) / kTileM;
-  const dim3 grid((unsigned)tiles, (unsigned)batch, (unsigned)num_kv_heads);
+  const dim3 grid((unsigned)((tiles + 1) / 2 * 2), (unsigned)batch, (unsigned)num_kv_heads);
   extend_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -3,6 +3,14 @@
 // descriptors, the instruction descriptor of kind::f16, the single-thread MMA
 // issue with its mbarrier commit, and the warp-wide TMEM loads and stores.
 //
+// Everything here is the CTA-pair form (.cta_group::2): two CTAs of a
+// cluster, ranks 0 and 1, on two SMs.  Each allocates the same TMEM columns;
+// one thread of rank 0 issues an MMA of M = 256 whose rows 0-127 live in rank
+// 0's TMEM and rows 128-255 in rank 1's (A read from TMEM, D written to it),
+// while the shared-memory B operand is split by N: each CTA holds half of its
+// columns at the same shared-memory address.  Every tcgen05 instruction of a
+// kernel uses the same CTA-group form.
+//
 // Operand layouts in shared memory are the no-swizzle canonical ones: a "core
 // matrix" is 8 rows of 16 bytes stored as 128 contiguous bytes.
 //  - K-major operand (rows = M or N, K contiguous within a row): core matrix
@@ -17,17 +25,18 @@
 namespace nvfp4kv {
 namespace tc {
 
-// Allocate ncols (a power of two >= 32) TMEM columns for this CTA; the TMEM
-// address is written to shared memory at dst.  Executed by one whole warp.
+// Allocate ncols (a power of two >= 32) TMEM columns in both CTAs of the
+// pair; the TMEM address is written to shared memory at dst.  Executed by one
+// whole warp in each of the two CTAs.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
-// Free the allocation (the same warp that allocated, after every TMEM access).
+// Free the allocation (the allocating warps, after every TMEM access of the pair).
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 // Order tcgen05 operations against thread synchronisation (barriers, mbarrier
@@ -56,32 +65,33 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn_maj
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D (TMEM) = A * B (+ D when accumulate != 0); issued by a single thread.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D (TMEM) = A * B (+ D when accumulate != 0) with A read from TMEM: lane r
-// holds row r, each 32-bit column two consecutive K elements (the lower K index
-// in the low half); one kind::f16 MMA reads 8 columns (K = 16).
+// D (TMEM) = A * B (+ D when accumulate != 0) over the pair, with A read from
+// TMEM: in each CTA lane r holds its row r, each 32-bit column two consecutive
+// K elements (the lower K index in the low half); one kind::f16 MMA reads 8
+// columns (K = 16).  Issued by one thread of rank 0.
 __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive once on the mbarrier when every MMA this thread issued so far is done.
+// Arrive once on the issuing CTA's mbarrier when every MMA this thread issued
+// so far is done.
 __device__ __forceinline__ void commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
                : "memory");
+}
+
+// The same, arriving on the mbarrier at this shared-memory offset in each CTA
+// of cta_mask (bit k: cluster rank k).
+__device__ __forceinline__ void commit_multicast(uint32_t mbar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(mbar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 // Warp-wide TMEM load: thread i gets lane (lane field of taddr) + i, 32

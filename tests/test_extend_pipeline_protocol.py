@@ -1,12 +1,16 @@
 """Model check of the extend-attention kernel's synchronisation protocol (host only).
 
-The kernel (csrc/extend_attention.cu) runs three roles in a CTA around
-mbarriers: loader warps fill a three-stage K/V ring and write Q; one thread
-issues the tensor-core MMAs (S = Q K^T into two S buffers, O += P V) and
-commits each group to an mbarrier; softmax warps read S, rescale O and write P.
-The tensor core finishes issued MMAs in order, asynchronously.  This model
-replays each role's sequence of waits, arrivals, commits and buffer accesses,
-in the kernel's order, under random interleavings, and checks:
+The kernel (csrc/extend_attention.cu) runs on a pair of CTAs (ranks 0 and 1 of
+a cluster) around mbarriers.  In each CTA, loader warps fill that CTA's half of
+a K/V ring and write its Q; softmax warps read its S rows, rescale its O and
+write its P.  One thread of rank 0 issues the pair's tensor-core MMAs (S = Q K^T
+into two S buffers, O += P V), which read both CTAs' halves and write both
+CTAs' S and O, and commits each group to the mbarrier of that name in both
+CTAs (multicast).  The loaders and softmax warps of both CTAs arrive on rank
+0's barriers (q_full, kv_full, p_full take one arrival per CTA here).  The
+tensor core finishes issued MMAs in order, asynchronously.  This model replays
+each role's sequence of waits, arrivals, commits and buffer accesses, in the
+kernel's order, under random interleavings, and checks:
 
 - every wait targets the completion it means: the barrier has at most one
   more completed phase than the one waited for (else the parity would alias);
@@ -18,7 +22,8 @@ import random
 
 import pytest
 
-STAGES, SBUF = 3, 2
+STAGES, SBUF = 6, 2
+RANKS = (0, 1)
 
 
 class Barrier:
@@ -32,44 +37,59 @@ class Barrier:
             self.pending = self.count
 
 
+def both(name):
+    return [f"{name}@{r}" for r in RANKS]
+
+
 def roles(n):
-    """The kernel's three roles as action lists (see the module docstring)."""
-    loader = [("write", "Q", 0), ("arrive", "q_full")]
-    for i in range(n):
-        s = i % STAGES
-        if i >= STAGES:
-            loader.append(("wait", f"kv_empty{s}", i // STAGES - 1))
-        loader += [("write", f"KV{s}", i), ("arrive", f"kv_full{s}")]
-    mma = [("wait", "q_full", 0)]
+    """The kernel's roles as action lists (see the module docstring); a
+    buffer or barrier name ends in @rank, the CTA that holds it."""
+    progs = {}
+    for r in RANKS:
+        loader = [("write", f"Q@{r}", 0), ("arrive", "q_full@0")]
+        for i in range(n):
+            s = i % STAGES
+            if i >= STAGES:
+                loader.append(("wait", f"kv_empty{s}@{r}", i // STAGES - 1))
+            loader += [("write", f"KV{s}@{r}", i), ("arrive", f"kv_full{s}@0")]
+        softmax = []
+        for i in range(n):
+            softmax += [("wait", f"s_full{i % SBUF}@{r}", i // SBUF), ("read", f"S{i % SBUF}@{r}", i)]
+            if i >= 1:
+                softmax += [("wait", f"o_done@{r}", i - 1), ("write", f"O@{r}", i)]   # the lazy rescale of O
+            softmax += [("write", f"P@{r}", i), ("arrive", "p_full@0")]
+        softmax += [("wait", f"o_done@{r}", n - 1), ("read", f"O@{r}", n)]
+        progs[f"loader{r}"], progs[f"softmax{r}"] = loader, softmax
+    mma = [("wait", "q_full@0", 0)]
     for i in range(n + 1):
         if i < n:
             s = i % STAGES
-            mma += [("wait", f"kv_full{s}", i // STAGES),
-                    ("issue", "S", i, [("Q", 0), (f"KV{s}", i)], [(f"S{i % SBUF}", i)]),
-                    ("commit", f"s_full{i % SBUF}")]
+            mma += [("wait", f"kv_full{s}@0", i // STAGES),
+                    ("issue", "S", i, [(b, 0) for b in both("Q")] + [(b, i) for b in both(f"KV{s}")],
+                     [(b, i) for b in both(f"S{i % SBUF}")]),
+                    ("commit", both(f"s_full{i % SBUF}"))]
         if i >= 1:
             pi = i - 1
-            mma += [("wait", "p_full", pi),
-                    ("issue", "PV", pi, [("P", pi), (f"KV{pi % STAGES}", pi)], [("O", pi)]),
-                    ("commit", "o_done")]
+            mma += [("wait", "p_full@0", pi),
+                    ("issue", "PV", pi, [(b, pi) for b in both("P")] + [(b, pi) for b in both(f"KV{pi % STAGES}")],
+                     [(b, pi) for b in both("O")]),
+                    ("commit", both("o_done"))]
             if pi + STAGES < n:
-                mma.append(("commit", f"kv_empty{pi % STAGES}"))
-    mma += [("commit", "drain"), ("wait", "drain", 0)]
-    softmax = []
-    for i in range(n):
-        softmax += [("wait", f"s_full{i % SBUF}", i // SBUF), ("read", f"S{i % SBUF}", i)]
-        if i >= 1:
-            softmax += [("wait", "o_done", i - 1), ("write", "O", i)]   # the lazy rescale of O
-        softmax += [("write", "P", i), ("arrive", "p_full")]
-    softmax += [("wait", "o_done", n - 1), ("read", "O", n)]
-    return {"loader": loader, "mma": mma, "softmax": softmax}
+                mma.append(("commit", both(f"kv_empty{pi % STAGES}")))
+    mma += [("commit", ["drain@0"]), ("wait", "drain@0", 0)]
+    progs["mma"] = mma
+    return progs
 
 
 def run(n, seed):
     rng = random.Random(seed)
-    bars = {name: Barrier(1) for name in ["q_full", "p_full", "o_done", "drain"] +
-            [f"kv_full{s}" for s in range(STAGES)] + [f"kv_empty{s}" for s in range(STAGES)] +
-            [f"s_full{b}" for b in range(SBUF)]}
+    # rank 0's q_full, kv_full and p_full take one arrival per CTA
+    bars = {"q_full@0": Barrier(2), "p_full@0": Barrier(2), "drain@0": Barrier(1)}
+    bars.update({f"kv_full{s}@0": Barrier(2) for s in range(STAGES)})
+    for r in RANKS:
+        bars.update({f"o_done@{r}": Barrier(1)})
+        bars.update({f"kv_empty{s}@{r}": Barrier(1) for s in range(STAGES)})
+        bars.update({f"s_full{b}@{r}": Barrier(1) for b in range(SBUF)})
     progs = roles(n)
     pc = {r: 0 for r in progs}
     content = {}          # buffer -> tile it holds
@@ -102,7 +122,8 @@ def run(n, seed):
                 busy[buf] -= 1
             completed += 1
             while commits and commits[0][1] <= completed:
-                bars[commits.pop(0)[0]].arrive()
+                for name in commits.pop(0)[0]:
+                    bars[name].arrive()
             continue
         a = progs[r][pc[r]]
         pc[r] += 1
@@ -115,12 +136,13 @@ def run(n, seed):
         elif kind == "commit":
             commits.append((a[1], issued))
             while commits and commits[0][1] <= completed:
-                bars[commits.pop(0)[0]].arrive()
+                for name in commits.pop(0)[0]:
+                    bars[name].arrive()
         elif kind == "write":
             check_write(a[1], a[2])
             content[a[1]] = a[2]
         elif kind == "read":
-            want = a[2] if a[1] != "O" else n - 1
+            want = a[2] if not a[1].startswith("O") else n - 1
             assert content.get(a[1]) == want, f"{r} read {a[1]} holding {content.get(a[1])}, wanted {want}"
             consumed[a[1]] = a[2]
         elif kind == "issue":
@@ -129,11 +151,11 @@ def run(n, seed):
                 want = t
                 assert content.get(buf) == want, f"{name}({tile}) reads {buf} holding {content.get(buf)}"
             for buf, t in writes:
-                if buf == "O":
-                    assert content.get("O") in (None, tile - 1, tile), f"PV({tile}) on O of {content.get('O')}"
+                if buf.startswith("O"):
+                    assert content.get(buf) in (None, tile - 1, tile), f"PV({tile}) on {buf} of {content.get(buf)}"
                 else:
                     check_write(buf, t)
-                    if buf.startswith("S") and t >= SBUF:   # the softmax is done with the tile before
+                    if buf.startswith("S") and t >= SBUF:   # that CTA's softmax is done with the tile before
                         assert consumed.get(buf) == t - SBUF, f"S({t}) issued before {buf} of {t - SBUF} was read"
             for buf, _ in reads + writes:
                 busy[buf] = busy.get(buf, 0) + 1
@@ -144,16 +166,19 @@ def run(n, seed):
 
 @pytest.mark.parametrize("n", list(range(1, 11)) + [17])
 def test_protocol_under_random_interleavings(n):
-    for seed in range(300):
+    for seed in range(200):
         run(n, seed)
 
 
 @pytest.mark.parametrize("drop", [
-    ("loader", "kv_empty"),   # a stage refilled while its P V may still run
-    ("softmax", "o_done"),    # P overwritten / O rescaled under a running P V
-    ("mma", "p_full"),        # P V issued before the softmax wrote P
-    ("mma", "kv_full"),       # S issued before the loaders filled the stage
-    ("softmax", "s_full"),    # S read before the tensor core wrote it
+    ("loader0", "kv_empty"),   # a stage refilled while its P V may still run
+    ("loader1", "kv_empty"),
+    ("softmax0", "o_done"),    # P overwritten / O rescaled under a running P V
+    ("softmax1", "o_done"),
+    ("mma", "p_full"),         # P V issued before the softmax wrote P
+    ("mma", "kv_full"),        # S issued before the loaders filled the stage
+    ("softmax0", "s_full"),    # S read before the tensor core wrote it
+    ("softmax1", "s_full"),
 ])
 def test_model_catches_each_missing_wait(drop, monkeypatch):
     # the checks have teeth: removing any one kind of wait from a role breaks them
@@ -168,4 +193,20 @@ def test_model_catches_each_missing_wait(drop, monkeypatch):
     monkeypatch.setitem(globals(), "roles", mutated)
     with pytest.raises(AssertionError):
         for seed in range(300):
-            run(6, seed)
+            run(9, seed)
+
+
+def test_model_catches_a_count_of_one_arrival(monkeypatch):
+    # rank 0's kv_full must wait for both CTAs' halves: with one arrival per
+    # phase it completes on whichever CTA is first, and an MMA reads a half
+    # that is not yet written
+    orig = Barrier.__init__
+
+    def one(self, count):
+        orig(self, 1)
+
+    monkeypatch.setattr(Barrier, "__init__", one)
+    with pytest.raises(AssertionError):
+        for seed in range(300):
+            run(9, seed)
+
