@@ -327,11 +327,9 @@ int nvfp4kv_dequant_to_fp8_workspace(const nvfp4kv_cache* cache, const int32_t* 
       !aligned(ws_v, 16))
     return NVFP4KV_ERR_INVALID_ARGUMENT;
   if (device_status && !aligned(device_status, 4)) return NVFP4KV_ERR_INVALID_ARGUMENT;
-  int nsm = 0;
-  if ((st = current_num_sms(&nsm)) != NVFP4KV_OK) return st;
   return cuda_status(nvfp4kv::launch_dequant_fp8(*cache, page_table, max_pages_per_seq, prefix_lens, cu_prefix,
                                                  batch, total_rows, k_ws_scale, v_ws_scale, ws_k, ws_v,
-                                                 device_status, nsm, reinterpret_cast<cudaStream_t>(stream)));
+                                                 device_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4kv_stream_probe(const nvfp4kv_cache* cache, const int32_t* page_table, int32_t max_pages_per_seq,

@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, kUnit ? 8 : 5) dequant_fp8_kernel(De
 cudaError_t launch_dequant_fp8(const nvfp4kv_cache& c, const int32_t* page_table, int32_t max_pages,
                                const int32_t* prefix_lens, const int64_t* cu_prefix, int32_t batch,
                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
-                               uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream) {
+                               uint8_t* ws_v, int32_t* device_status, cudaStream_t stream) {
   DequantParams p;
   p.pages = c.pages;
   p.num_pages = c.num_pages;

@@ -47,7 +47,7 @@ cudaError_t launch_quantize_append(const nvfp4kv_cache& c, const uint16_t* k, co
 cudaError_t launch_dequant_fp8(const nvfp4kv_cache& c, const int32_t* page_table, int32_t max_pages,
                                const int32_t* prefix_lens, const int64_t* cu_prefix, int32_t batch,
                                int64_t total_rows, float k_ws_scale, float v_ws_scale, uint8_t* ws_k,
-                               uint8_t* ws_v, int32_t* device_status, int num_sms, cudaStream_t stream);
+                               uint8_t* ws_v, int32_t* device_status, cudaStream_t stream);
 
 // Quantize-append plus the FP8 workspace rows of the same tokens, one pass.
 cudaError_t launch_quantize_append_fp8(const nvfp4kv_cache& c, const uint16_t* k, const uint16_t* v,
